@@ -1,0 +1,190 @@
+"""fp64 CPU oracle for bf16 RMSNorm and fused RMSNorm+RoPE -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it, and this package imports nothing from
+the product path: the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, binary64, sequential sums); this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+bfloat16 tensors travel as ``numpy.uint16`` arrays of bit patterns.
+
+Definition followed (the pages print no formula; see ``oracle.c`` for the
+page sections cited):
+    n_j = x_j * w_j / sqrt(mean(x^2) + eps), then per-head RoPE
+    a' = a c - b s, b' = a s + b c, rounded once to bfloat16 (RNE).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+INTERLEAVED = 0
+SPLIT_HALF = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, -O2).
+
+    ``-ffp-contract=off`` keeps every multiply and add separately rounded on
+    both x86-64 and AArch64 hosts.
+    """
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            lib.oracle_widen_bf16.argtypes = [P, P, I64]
+            lib.oracle_widen_bf16.restype = None
+            lib.oracle_round_bf16.argtypes = [P, P, I64]
+            lib.oracle_round_bf16.restype = None
+            lib.oracle_rms_norm.argtypes = [P, P, P, I64, I64, ctypes.c_float, P]
+            lib.oracle_rms_norm.restype = ctypes.c_int
+            lib.oracle_rms_norm_rope.argtypes = [
+                P, P, P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_float,
+                I64, I64, P]
+            lib.oracle_rms_norm_rope.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _u16(a, name):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"{name} must hold bfloat16 bit patterns as uint16")
+    return a
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """Exact binary64 values of bfloat16 bit patterns."""
+    bits = _u16(bits, "bits")
+    out = np.empty(bits.shape, np.float64)
+    _load().oracle_widen_bf16(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def round_bf16(values: np.ndarray) -> np.ndarray:
+    """Round binary64 values straight to bfloat16 (RNE); returns bit patterns."""
+    values = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(values.shape, np.uint16)
+    _load().oracle_round_bf16(_ptr(values), _ptr(out), values.size)
+    return out
+
+
+def _row_blocks(rows, threads):
+    threads = max(1, min(threads, rows))
+    step = -(-rows // threads)
+    return [(r0, min(rows, r0 + step)) for r0 in range(0, rows, step)]
+
+
+def rms_norm(x, w, eps, *, threads: int = 1, exact: bool = False):
+    """Oracle RMSNorm over the last axis of ``x`` (uint16 bf16 bits).
+
+    Returns the bf16 bit patterns, or ``(bits, exact_values)`` when ``exact``.
+    ``threads`` > 1 runs disjoint row ranges concurrently (ctypes releases the
+    GIL during the call); the arithmetic per row is unchanged.
+    """
+    x = _u16(x, "x")
+    H = x.shape[-1]
+    rows = x.size // H if H else 0
+    x2 = x.reshape(rows, H)
+    w = None if w is None else _u16(w, "w")
+    if w is not None and w.size != H:
+        raise ValueError("w must have hidden elements")
+    y = np.empty_like(x2)
+    ye = np.empty(x2.shape, np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        rc = lib.oracle_rms_norm(
+            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), r1 - r0, H,
+            ctypes.c_float(eps), None if ye is None else _ptr(ye[r0:r1]))
+        if rc != 0:
+            raise MemoryError("oracle_rms_norm failed")
+
+    _run_blocks(run, rows, threads)
+    y = y.reshape(x.shape)
+    return (y, ye.reshape(x.shape)) if exact else y
+
+
+def rms_norm_rope(x, w, cos, sin, heads, head_dim, mode, eps, *,
+                  table_rows=None, threads: int = 1, exact: bool = False):
+    """Oracle fused RMSNorm + RoPE.
+
+    ``x``: uint16 [rows, heads*head_dim]; ``cos``/``sin``: float32
+    [table_rows, head_dim/2]; row r uses table row ``r % table_rows``
+    (``table_rows`` defaults to the tables' first dimension).
+    """
+    x = _u16(x, "x")
+    H = heads * head_dim
+    if x.shape[-1] != H:
+        raise ValueError("last axis of x must be heads*head_dim")
+    rows = x.size // H
+    x2 = x.reshape(rows, H)
+    w = None if w is None else _u16(w, "w")
+    cos = np.ascontiguousarray(cos, dtype=np.float32)
+    sin = np.ascontiguousarray(sin, dtype=np.float32)
+    P = head_dim // 2
+    if table_rows is None:
+        table_rows = cos.size // P
+    if cos.size < table_rows * P or sin.size < table_rows * P:
+        raise ValueError("tables too small")
+    y = np.empty_like(x2)
+    ye = np.empty(x2.shape, np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        rc = lib.oracle_rms_norm_rope(
+            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(cos), _ptr(sin),
+            r1 - r0, heads, head_dim, mode, ctypes.c_float(eps), table_rows,
+            r0, None if ye is None else _ptr(ye[r0:r1]))
+        if rc != 0:
+            raise RuntimeError(f"oracle_rms_norm_rope failed ({rc})")
+
+    _run_blocks(run, rows, threads)
+    y = y.reshape(x.shape)
+    return (y, ye.reshape(x.shape)) if exact else y
+
+
+def _run_blocks(fn, rows, threads):
+    if rows == 0:
+        return
+    blocks = _row_blocks(rows, threads)
+    if len(blocks) == 1:
+        fn(blocks[0])
+        return
+    with ThreadPoolExecutor(max_workers=len(blocks)) as ex:
+        for f in [ex.submit(fn, b) for b in blocks]:
+            f.result()

@@ -1,0 +1,187 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for bf16 RMSNorm and the fused
+ * RMSNorm + rotary-embedding (RoPE) forms.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent definition that the
+ * CUDA path is checked against.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load it.  It shares no code, header,
+ * constant or helper with the CUDA library, and it includes no CUDA header.
+ *
+ * What it follows:
+ *   - "cuda-kernels" skill page (Hugging Face), section "Kernel-Specific
+ *     Guidelines / RMSNorm": the input layout is [..., hidden_size], the
+ *     default epsilon is 1e-6, and the weight may be absent (treated as ones).
+ *   - same page, "Kernel-Specific Guidelines / RoPE": the per-head layouts
+ *     [batch, seq, heads, head_dim] (1D text) and [batch, t*h*w, heads,
+ *     head_dim] (3D video).
+ *   - "ltx-kernels" README, opening list (`ops_cpp`): the two fused ops
+ *     rms_norm_rope (interleaved pairs) and rms_norm_split_rope (split-half
+ *     pairs).
+ *   - The pages print no formula for either operation.  The definition used:
+ *       ms   = (1/H) * sum_j x_j^2                     (mean over exactly H)
+ *       n_j  = x_j * w_j / sqrt(ms + eps)               (eps inside the root)
+ *       RoPE, per head h and pair p with c = cos[pos,p], s = sin[pos,p]:
+ *         a' = a*c - b*s,   b' = a*s + b*c
+ *         interleaved: (a, b) = (n[h*D + 2p], n[h*D + 2p + 1])
+ *         split-half : (a, b) = (n[h*D + p],  n[h*D + p + D/2])
+ *       output = one round-to-nearest-even of the exact value to bfloat16.
+ *     The RMSNorm is taken over the full hidden size before any rotation, and
+ *     the rotation acts on the unrounded normalised values.
+ *
+ * All arithmetic is IEEE-754 binary64, summed in plain sequential order, with
+ * no blocking, fusion or reordering.  The build compiles this file with
+ * -ffp-contract=off so that no multiply-add is fused on any host.
+ *
+ * Every exported function is re-entrant (no global state), so callers may run
+ * disjoint row ranges on several threads at once.
+ *
+ * Parity pins (tests in tests/test_oracle.py): brute force over all 65536
+ * bfloat16 patterns for the rounding, hand-computed cases at hidden = 4, the
+ * unit-RMS closed form, exact power-of-two scale invariance, the fp64
+ * library RMSNorm of PyTorch, identity / quarter-turn / half-turn rotations,
+ * pair-norm preservation and the permutation that maps split-half pairing to
+ * interleaved pairing.  No function here is left unpinned.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* A bfloat16 value is the upper 16 bits of an IEEE-754 binary32 value, so
+ * widening is exact: place the bits on top of a binary32 and convert. */
+static double widen_bf16(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a binary64 value straight to bfloat16, round-to-nearest, ties to even,
+ * from the IEEE-754 definition (no intermediate binary32 rounding).
+ *
+ * bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits, so a
+ * precision of 8 significant bits; normal range starts at 2^-126 and the
+ * subnormal spacing is 2^-133.  For |v| in [2^(e-1), 2^e) the spacing of
+ * representable values is 2^(e-8); below the normal range it stays 2^-133. */
+static uint16_t round_to_bf16(double v) {
+    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
+    const uint16_t sign = (uint16_t)(signbit(v) ? 0x8000u : 0u);
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+
+    int e;
+    (void)frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
+    if (e < -125) e = -125;             /* subnormal range: fixed spacing */
+    const double q = ldexp(1.0, e - 8); /* spacing of bf16 values near a */
+    const double n = a / q;             /* exact: q is a power of two */
+    double k = floor(n);
+    const double frac = n - k;          /* exact */
+    if (frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;
+    const double r = k * q;             /* exact; may reach 2^128 */
+
+    /* r is exactly representable in bfloat16 (or is 2^128, which becomes
+     * +inf in binary32), so encoding through binary32 loses nothing. */
+    const float rf = (float)r;
+    uint32_t u;
+    memcpy(&u, &rf, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/* ---- element conversions, exported for the pins ------------------------ */
+
+void oracle_widen_bf16(const uint16_t* in, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = widen_bf16(in[i]);
+}
+
+void oracle_round_bf16(const double* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = round_to_bf16(in[i]);
+}
+
+/* ---- RMSNorm ----------------------------------------------------------- */
+
+/* Normalise one row of H values into n[0..H).  w == NULL means all ones. */
+static void normalise_row(const uint16_t* xr, const uint16_t* w, int64_t H,
+                          float eps, double* n) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < H; ++j) {
+        const double v = widen_bf16(xr[j]);
+        ss += v * v;
+    }
+    const double ms = ss / (double)H;
+    const double denom = sqrt(ms + (double)eps);
+    for (int64_t j = 0; j < H; ++j) {
+        const double wj = w ? widen_bf16(w[j]) : 1.0;
+        n[j] = widen_bf16(xr[j]) * wj / denom;
+    }
+}
+
+/* y[r, j] = bf16( x[r, j] * w[j] / sqrt(mean_j x[r, j]^2 + eps) ).
+ *
+ * x, y: row-major [rows, H] bfloat16 bit patterns.  w: [H] or NULL (ones).
+ * y_exact: optional [rows, H] binary64 copy of the values before rounding.
+ * Returns 0, or -1 if scratch memory could not be allocated. */
+int oracle_rms_norm(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                    int64_t rows, int64_t H, float eps, double* y_exact) {
+    double* n = (double*)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+    if (!n) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        normalise_row(x + r * H, w, H, eps, n);
+        for (int64_t j = 0; j < H; ++j) {
+            if (y_exact) y_exact[r * H + j] = n[j];
+            y[r * H + j] = round_to_bf16(n[j]);
+        }
+    }
+    free(n);
+    return 0;
+}
+
+/* Fused RMSNorm then RoPE.
+ *
+ * x, y: row-major [rows, heads*head_dim].  w: [heads*head_dim] or NULL.
+ * cos_t, sin_t: binary32 tables [table_rows, head_dim/2]; row r of x (counted
+ * from first_row, the global index of the first row passed) uses table row
+ * ((first_row + r) mod table_rows), i.e. x is [batch, table_rows, hidden]
+ * with the sequence position as the inner row index.
+ * mode 0 pairs (2p, 2p+1) inside each head; mode 1 pairs (p, p + head_dim/2).
+ * Returns 0; -1 on allocation failure; -2 on an invalid argument. */
+int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                         const float* cos_t, const float* sin_t,
+                         int64_t rows, int64_t heads, int64_t head_dim,
+                         int mode, float eps, int64_t table_rows,
+                         int64_t first_row, double* y_exact) {
+    if (head_dim <= 0 || head_dim % 2 != 0 || heads <= 0 || table_rows <= 0 ||
+        first_row < 0)
+        return -2;
+    if (mode != 0 && mode != 1) return -2;
+    const int64_t H = heads * head_dim;
+    const int64_t P = head_dim / 2;
+    double* n = (double*)malloc((size_t)H * sizeof(double));
+    double* o = (double*)malloc((size_t)H * sizeof(double));
+    if (!n || !o) { free(n); free(o); return -1; }
+
+    for (int64_t r = 0; r < rows; ++r) {
+        normalise_row(x + r * H, w, H, eps, n);
+        const int64_t pos = (first_row + r) % table_rows;
+        for (int64_t h = 0; h < heads; ++h) {
+            for (int64_t p = 0; p < P; ++p) {
+                int64_t ia, ib;
+                if (mode == 0) { ia = h * head_dim + 2 * p; ib = ia + 1; }
+                else           { ia = h * head_dim + p;     ib = ia + P; }
+                const double c = (double)cos_t[pos * P + p];
+                const double s = (double)sin_t[pos * P + p];
+                const double a = n[ia];
+                const double b = n[ib];
+                o[ia] = a * c - b * s;
+                o[ib] = a * s + b * c;
+            }
+        }
+        for (int64_t j = 0; j < H; ++j) {
+            if (y_exact) y_exact[r * H + j] = o[j];
+            y[r * H + j] = round_to_bf16(o[j]);
+        }
+    }
+    free(n);
+    free(o);
+    return 0;
+}

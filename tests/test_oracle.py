@@ -1,0 +1,344 @@
+"""Pins for the fp64 CPU oracle, checked against what the definition and the
+mathematics fix -- never against the CUDA path.
+
+Each test is chosen so that a plausible slip in the oracle fails it:
+  * rounding: brute force over every bfloat16 pattern, midpoints, ties,
+    overflow and subnormals; plus PyTorch's binary32 -> bfloat16 conversion
+    (a library routine) on binary32 inputs;
+  * RMSNorm: hand cases at hidden = 4 (tests/golden), the unit-RMS closed
+    form (mean over exactly H), exact power-of-two scale invariance (eps
+    inside the root, scaled by 1/alpha^2), a first-order expansion in eps,
+    and PyTorch's float64 library RMSNorm;
+  * RoPE: hand cases (pair indices, signs, table row per position), the
+    identity at angle 0, quarter and half turns, pair-norm preservation and
+    the permutation that maps split-half pairing onto interleaved pairing.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases_h4.txt")
+
+
+def f32_to_bits(v):
+    return (np.asarray(v, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bits_of(values):
+    """bf16 bit patterns of values that are exactly representable."""
+    f = np.asarray(values, np.float32)
+    assert np.all((f.view(np.uint32) & 0xFFFF) == 0)
+    return f32_to_bits(f)
+
+
+# ---------------------------------------------------------------- rounding --
+
+def test_widen_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle_mod.widen_bf16(bits)
+    with np.errstate(invalid="ignore"):
+        ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(vals), nan)
+    assert np.array_equal(vals[~nan], ref[~nan])
+
+
+def test_round_identity_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle_mod.widen_bf16(bits)
+    back = oracle_mod.round_bf16(vals)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(back[finite], bits[finite])
+    # NaN stays NaN (quiet, sign kept)
+    nb = back[~finite]
+    assert np.all((nb & 0x7F80) == 0x7F80) and np.all((nb & 0x7F) != 0)
+
+
+def test_round_midpoints_ties_to_even(oracle_mod):
+    # consecutive positive finite patterns b, b+1 (b+1 may be +inf = 0x7F80)
+    b = np.arange(0, 0x7F80, dtype=np.uint16)
+    lo = oracle_mod.widen_bf16(b)
+    hi = oracle_mod.widen_bf16((b + 1).astype(np.uint16))
+    hi[-1] = 2.0 ** 128                     # the value "after" the max finite
+    mid = (lo + hi) / 2                     # exact in binary64
+    even = np.where(b % 2 == 0, b, b + 1).astype(np.uint16)
+    assert np.array_equal(oracle_mod.round_bf16(mid), even)
+    delta = (hi - lo) * 2.0 ** -20
+    assert np.array_equal(oracle_mod.round_bf16(mid + delta), (b + 1).astype(np.uint16))
+    assert np.array_equal(oracle_mod.round_bf16(mid - delta), b)
+    # negative side mirrors the positive side
+    assert np.array_equal(oracle_mod.round_bf16(-mid), even | np.uint16(0x8000))
+
+
+def test_round_special_values(oracle_mod):
+    r = oracle_mod.round_bf16
+    cases = [
+        (0.0, 0x0000), (-0.0, 0x8000), (np.inf, 0x7F80), (-np.inf, 0xFF80),
+        (2.0 ** -133, 0x0001),             # smallest subnormal
+        (2.0 ** -134, 0x0000),             # half of it: tie -> even (0)
+        (1.5 * 2.0 ** -134, 0x0001),
+        (3.0 * 2.0 ** -134, 0x0002),       # tie between 1 and 2 -> 2
+        (2.0 ** -126, 0x0080),             # smallest normal
+        ((2 - 2 ** -7) * 2.0 ** 127, 0x7F7F),   # largest finite
+        ((2 - 2 ** -8) * 2.0 ** 127, 0x7F80),   # its upper midpoint -> inf
+        (1e300, 0x7F80),
+        (1.0 + 2 ** -8, 0x3F80),           # tie, 1.0 is even
+        (1.0 + 3 * 2 ** -8, 0x3F82),       # tie, 1+2^-6 (..010) is even
+        (1.0 + 2 ** -8 + 2 ** -50, 0x3F81),  # just above the tie
+    ]
+    vals = np.array([v for v, _ in cases], np.float64)
+    got = r(vals)
+    assert [int(g) for g in got] == [b for _, b in cases]
+
+
+def test_round_direct_not_through_binary32(oracle_mod):
+    # A binary64 just above a bf16 midpoint whose nearest binary32 IS the
+    # midpoint: direct rounding goes up, rounding through binary32 would tie
+    # to even (down).
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert np.float64(np.float32(v)) == 1.0 + 2.0 ** -8
+    assert int(oracle_mod.round_bf16(np.array([v]))[0]) == 0x3F81
+
+
+def test_round_matches_torch_on_binary32(oracle_mod):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    f = (rng.standard_normal(1 << 18)
+         * np.exp2(rng.integers(-140, 128, 1 << 18))).astype(np.float32)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod.round_bf16(f.astype(np.float64))
+    ok = np.isfinite(f)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+# ------------------------------------------------------------- hand cases --
+
+def _parse_golden():
+    cases = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        f = [s.strip() for s in line.split(" | ")]
+        name, kind, eps, xs, ws, tab, hd, exact, bits = f
+        rows = [list(map(float, r.split())) for r in xs.split(";")]
+        x = np.array(rows, np.float64)
+        w = None if ws == "-" else np.array(list(map(float, ws.split())))
+        cos = sin = None
+        if tab != "-":
+            c, s = tab.split(";")
+            cos = np.array(list(map(float, c.split())), np.float32)
+            sin = np.array(list(map(float, s.split())), np.float32)
+        heads = head_dim = None
+        if hd != "-":
+            heads, head_dim = map(int, hd.split(","))
+        cases.append(dict(
+            name=name, kind=kind, eps=float(eps), x=x, w=w, cos=cos, sin=sin,
+            heads=heads, head_dim=head_dim,
+            exact=np.array(list(map(float, exact.split()))).reshape(x.shape),
+            bits=np.array([int(b, 16) for b in bits.split()],
+                          np.uint16).reshape(x.shape)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _parse_golden(), ids=lambda c: c["name"])
+def test_hand_cases(oracle_mod, case):
+    x = bits_of(case["x"])
+    w = None if case["w"] is None else bits_of(case["w"])
+    if case["kind"] == "norm":
+        y, ye = oracle_mod.rms_norm(x, w, case["eps"], exact=True)
+    else:
+        mode = (oracle_mod.INTERLEAVED if case["kind"] == "rope_interleaved"
+                else oracle_mod.SPLIT_HALF)
+        y, ye = oracle_mod.rms_norm_rope(
+            x, w, case["cos"], case["sin"], case["heads"], case["head_dim"],
+            mode, case["eps"], exact=True)
+    assert np.array_equal(y, case["bits"]), [hex(v) for v in y.ravel()]
+    np.testing.assert_allclose(ye, case["exact"], rtol=4e-16, atol=1e-300)
+
+
+def test_eps_first_order(oracle_mod):
+    # x = (3, 4, 0, 0): y0 = 1.2 (1 + e/6.25)^(-1/2) = 1.2 - 0.096 e + O(e^2).
+    # eps outside the root would give 1.2 - 0.48 e instead.
+    e = float(np.float32(1e-6))
+    x = bits_of([[3, 4, 0, 0]])
+    _, ye = oracle_mod.rms_norm(x, None, 1e-6, exact=True)
+    assert abs(ye[0, 0] - (1.2 - 0.096 * e)) < 2e-14
+    assert abs(ye[0, 1] - (1.6 - 0.128 * e)) < 2e-14
+
+
+# --------------------------------------------------------- RMSNorm pins --
+
+def _rows(seed, rows, H, dist="normal"):
+    if dist == "normal":
+        return synth.normal_bf16(seed, 0, rows * H).reshape(rows, H)
+    return synth.uniform_bf16(seed, 0, rows * H, -4, 4).reshape(rows, H)
+
+
+@pytest.mark.parametrize("H", [4, 24, 2048, 5120])
+def test_unit_rms_closed_form(oracle_mod, H):
+    x = _rows(11, 16, H)
+    _, ye = oracle_mod.rms_norm(x, None, 0.0, exact=True)
+    np.testing.assert_allclose((ye ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    # with eps: mean(n^2) = ms / (ms + eps)
+    eps = 0.25
+    _, ye = oracle_mod.rms_norm(x, None, eps, exact=True)
+    ms = (oracle_mod.widen_bf16(x) ** 2).mean(axis=1)
+    np.testing.assert_allclose((ye ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-13)
+
+
+@pytest.mark.parametrize("k", [-3, 1, 5])
+def test_scale_invariance_exact(oracle_mod, k):
+    x = _rows(12, 8, 264)
+    w = synth.normal_bf16(12, 2, 264, 1.0, 0.1)
+    xs = (x.astype(np.int32) + (k << 7)).astype(np.uint16)   # x * 2^k, exact
+    assert np.array_equal(oracle_mod.widen_bf16(xs), oracle_mod.widen_bf16(x) * 2.0 ** k)
+    # eps = 0: identical output
+    y0, e0 = oracle_mod.rms_norm(x, w, 0.0, exact=True)
+    y1, e1 = oracle_mod.rms_norm(xs, w, 0.0, exact=True)
+    assert np.array_equal(y0, y1) and np.array_equal(e0, e1)
+    # eps > 0: n(2^k x; eps) == n(x; eps / 4^k) exactly
+    eps = float(np.float32(1e-3))
+    _, ea = oracle_mod.rms_norm(xs, w, eps, exact=True)
+    _, eb = oracle_mod.rms_norm(x, w, eps / 4.0 ** k, exact=True)
+    assert np.array_equal(ea, eb)
+
+
+def test_weight_none_is_ones(oracle_mod):
+    x = _rows(13, 4, 40)
+    ones = bits_of(np.ones(40))
+    assert np.array_equal(oracle_mod.rms_norm(x, None, 1e-6),
+                          oracle_mod.rms_norm(x, ones, 1e-6))
+
+
+def test_matches_torch_rms_norm_fp64(oracle_mod):
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    for H, eps in [(24, 1e-6), (2048, 1e-5), (3072, 1e-6)]:
+        x = _rows(14, 8, H, "uniform")
+        w = synth.normal_bf16(14, 2, H, 1.0, 0.1)
+        _, ye = oracle_mod.rms_norm(x, w, eps, exact=True)
+        xt = torch.from_numpy(oracle_mod.widen_bf16(x))
+        wt = torch.from_numpy(oracle_mod.widen_bf16(w))
+        ref = F.rms_norm(xt, (H,), wt, eps=float(np.float32(eps))).numpy()
+        np.testing.assert_allclose(ye, ref, rtol=1e-12, atol=1e-300)
+
+
+def test_threaded_rows_identical(oracle_mod):
+    x = _rows(15, 37, 96)
+    w = synth.normal_bf16(15, 2, 96, 1.0, 0.1)
+    assert np.array_equal(oracle_mod.rms_norm(x, w, 1e-6, threads=1),
+                          oracle_mod.rms_norm(x, w, 1e-6, threads=5))
+    c, s = synth.rope_table_1d(7, 8)
+    a = oracle_mod.rms_norm_rope(x, w, c, s, 12, 8, 0, 1e-6, threads=1)
+    b = oracle_mod.rms_norm_rope(x, w, c, s, 12, 8, 0, 1e-6, threads=4)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------- RoPE pins --
+
+def _const_tables(rows, P, c, s):
+    return (np.full((rows, P), c, np.float32), np.full((rows, P), s, np.float32))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_identity_at_angle_zero(oracle_mod, mode):
+    heads, D = 4, 16
+    x = _rows(21, 9, heads * D)
+    w = synth.normal_bf16(21, 2, heads * D, 1.0, 0.1)
+    c, s = _const_tables(3, D // 2, 1.0, 0.0)
+    y, ye = oracle_mod.rms_norm_rope(x, w, c, s, heads, D, mode, 1e-6, exact=True)
+    yn, yne = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    assert np.array_equal(y, yn) and np.array_equal(ye, yne)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_quarter_and_half_turn(oracle_mod, mode):
+    heads, D = 3, 8
+    P = D // 2
+    x = _rows(22, 5, heads * D)
+    _, n = oracle_mod.rms_norm(x, None, 1e-6, exact=True)
+    n = n.reshape(5, heads, D)
+    if mode == 0:
+        a, b = n[..., 0::2], n[..., 1::2]
+    else:
+        a, b = n[..., :P], n[..., P:]
+    # quarter turn (c = 0, s = 1): (a, b) -> (-b, a)
+    c, s = _const_tables(1, P, 0.0, 1.0)
+    _, q = oracle_mod.rms_norm_rope(x, None, c, s, heads, D, mode, 1e-6, exact=True)
+    q = q.reshape(5, heads, D)
+    qa, qb = (q[..., 0::2], q[..., 1::2]) if mode == 0 else (q[..., :P], q[..., P:])
+    assert np.array_equal(qa, -b) and np.array_equal(qb, a)
+    # half turn (c = -1, s = 0): negation
+    c, s = _const_tables(1, P, -1.0, 0.0)
+    _, hh = oracle_mod.rms_norm_rope(x, None, c, s, heads, D, mode, 1e-6, exact=True)
+    assert np.array_equal(hh.reshape(5, heads, D), -n)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_preserves_pair_norm(oracle_mod, mode):
+    heads, D = 4, 32
+    P = D // 2
+    x = _rows(23, 64, heads * D)
+    w = synth.normal_bf16(23, 2, heads * D, 1.0, 0.1)
+    cos, sin = synth.rope_table_1d(64, D)
+    _, n = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    _, r = oracle_mod.rms_norm_rope(x, w, cos, sin, heads, D, mode, 1e-6, exact=True)
+    n = n.reshape(64, heads, D)
+    r = r.reshape(64, heads, D)
+    if mode == 0:
+        n2 = n[..., 0::2] ** 2 + n[..., 1::2] ** 2
+        r2 = r[..., 0::2] ** 2 + r[..., 1::2] ** 2
+    else:
+        n2 = n[..., :P] ** 2 + n[..., P:] ** 2
+        r2 = r[..., :P] ** 2 + r[..., P:] ** 2
+    c2s2 = (cos.astype(np.float64) ** 2 + sin.astype(np.float64) ** 2)[:, None, :]
+    np.testing.assert_allclose(r2, n2 * c2s2, rtol=1e-13, atol=1e-300)
+
+
+def test_split_half_is_permuted_interleaved(oracle_mod):
+    heads, D = 5, 16
+    P = D // 2
+    rows = 12
+    x = _rows(24, rows, heads * D)
+    w = synth.normal_bf16(24, 2, heads * D, 1.0, 0.1)
+    cos, sin = synth.rope_table_3axis(2, 2, 3, D, (2, 3, 3))
+    # Q maps split-half index p -> 2p and p + P -> 2p + 1 inside each head
+    perm = np.empty(D, np.int64)
+    perm[0::2] = np.arange(P)
+    perm[1::2] = np.arange(P) + P
+    full = (np.arange(heads)[:, None] * D + perm[None, :]).ravel()
+    xq = x[:, full]
+    wq = w[full]
+    ys, es = oracle_mod.rms_norm_rope(x, w, cos, sin, heads, D, 1, 1e-6, exact=True)
+    yi, ei = oracle_mod.rms_norm_rope(xq, wq, cos, sin, heads, D, 0, 1e-6, exact=True)
+    inv = np.argsort(full)
+    np.testing.assert_allclose(ei[:, inv], es, rtol=1e-15, atol=1e-300)
+    assert np.array_equal(yi[:, inv], ys)
+
+
+def test_rope_position_is_row_mod_table_rows(oracle_mod):
+    # batch of 3 sequences of 4 positions: rows 4..7 and 8..11 repeat 0..3
+    heads, D = 2, 8
+    x = _rows(25, 4, heads * D)
+    xb = np.concatenate([x, x, x])
+    cos, sin = synth.rope_table_1d(4, D)
+    y1 = oracle_mod.rms_norm_rope(x, None, cos, sin, heads, D, 0, 1e-6)
+    yb = oracle_mod.rms_norm_rope(xb, None, cos, sin, heads, D, 0, 1e-6)
+    assert np.array_equal(yb, np.concatenate([y1, y1, y1]))
+    # and per-row tables with table_rows == rows give the same answer
+    cb, sb = np.concatenate([cos] * 3), np.concatenate([sin] * 3)
+    assert np.array_equal(
+        oracle_mod.rms_norm_rope(xb, None, cb, sb, heads, D, 0, 1e-6), yb)
+
+
+def test_rope_rejects_bad_arguments(oracle_mod):
+    x = _rows(26, 2, 8)
+    c, s = _const_tables(1, 4, 1.0, 0.0)
+    with pytest.raises(RuntimeError):
+        oracle_mod.rms_norm_rope(x, None, c, s, 1, 8, 2, 1e-6)

@@ -1,0 +1,99 @@
+"""The pins are strong enough: each plausible mistake, planted in a private
+copy of the oracle's C source, makes at least one pin fail.
+
+Everything here runs on the CPU; the real oracle is never modified.
+"""
+import importlib.util
+import os
+import shutil
+
+import pytest
+
+import test_oracle as pins
+
+ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("eps_outside_root", "sqrt(ms + (double)eps)", "(sqrt(ms) + (double)eps)"),
+    ("mean_over_h_minus_1", "ss / (double)H", "ss / (double)(H - 1)"),
+    ("sum_not_mean", "ss / (double)H", "ss"),
+    ("weight_ignored", "w ? widen_bf16(w[j]) : 1.0", "1.0"),
+    ("weight_divides", "widen_bf16(xr[j]) * wj / denom", "widen_bf16(xr[j]) / wj / denom"),
+    ("rope_sign_a", "o[ia] = a * c - b * s;", "o[ia] = a * c + b * s;"),
+    ("rope_sign_b", "o[ib] = a * s + b * c;", "o[ib] = b * c - a * s;"),
+    ("rope_cos_sin_swapped", "o[ib] = a * s + b * c;", "o[ib] = a * c + b * s;"),
+    ("split_pairs_adjacent", "ia = h * head_dim + p;     ib = ia + P;",
+     "ia = h * head_dim + 2 * p; ib = ia + 1;"),
+    ("interleaved_pairs_split", "ia = h * head_dim + 2 * p; ib = ia + 1;",
+     "ia = h * head_dim + p;     ib = ia + P;"),
+    ("table_column_off_by_one", "cos_t[pos * P + p]", "cos_t[pos * P + (p + 1) % P]"),
+    ("position_ignores_first_row", "(first_row + r) % table_rows", "r % table_rows"),
+    ("position_fixed", "(first_row + r) % table_rows", "0"),
+    ("round_ties_away", "frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)",
+     "frac >= 0.5"),
+    ("round_truncates", "if (frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;",
+     ""),
+    ("subnormal_spacing", "if (e < -125) e = -125;", "if (e < -126) e = -126;"),
+    ("precision_9_bits", "ldexp(1.0, e - 8)", "ldexp(1.0, e - 9)"),
+]
+
+
+def _pin_calls():
+    hand = {c["name"]: c for c in pins._parse_golden()}
+    calls = [
+        ("widen", pins.test_widen_all_patterns, ()),
+        ("identity", pins.test_round_identity_all_patterns, ()),
+        ("midpoints", pins.test_round_midpoints_ties_to_even, ()),
+        ("specials", pins.test_round_special_values, ()),
+        ("direct", pins.test_round_direct_not_through_binary32, ()),
+        ("eps_order", pins.test_eps_first_order, ()),
+        ("unit_rms", pins.test_unit_rms_closed_form, (24,)),
+        ("scale", pins.test_scale_invariance_exact, (1,)),
+        ("torch", pins.test_matches_torch_rms_norm_fp64, ()),
+        ("threaded", pins.test_threaded_rows_identical, ()),
+        ("identity0", pins.test_rope_identity_at_angle_zero, (0,)),
+        ("quarter0", pins.test_rope_quarter_and_half_turn, (0,)),
+        ("quarter1", pins.test_rope_quarter_and_half_turn, (1,)),
+        ("pairnorm0", pins.test_rope_preserves_pair_norm, (0,)),
+        ("pairnorm1", pins.test_rope_preserves_pair_norm, (1,)),
+        ("perm", pins.test_split_half_is_permuted_interleaved, ()),
+        ("position", pins.test_rope_position_is_row_mod_table_rows, ()),
+    ]
+    for name, case in hand.items():
+        calls.append(("hand_" + name, pins.test_hand_cases, (case,)))
+    return calls
+
+
+def _load_mutant(tmp_path, name, old, new):
+    d = tmp_path / f"oracle_{name}"
+    d.mkdir()
+    shutil.copy(os.path.join(ORACLE_DIR, "__init__.py"), d / "__init__.py")
+    src = open(os.path.join(ORACLE_DIR, "oracle.c")).read()
+    assert src.count(old) >= 1, f"mutation anchor missing: {old!r}"
+    (d / "oracle.c").write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location(
+        f"oracle_{name}", d / "__init__.py", submodule_search_locations=[str(d)])
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build(force=True)
+    return mod
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    mod = _load_mutant(tmp_path, "none", "oracle", "oracle")
+    for _, fn, args in _pin_calls():
+        fn(mod, *args)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    mod = _load_mutant(tmp_path, name, old, new)
+    caught = []
+    for pin, fn, args in _pin_calls():
+        try:
+            fn(mod, *args)
+        except (AssertionError, RuntimeError, ValueError, MemoryError):
+            caught.append(pin)
+    assert caught, f"no pin caught mutant {name}"
