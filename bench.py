@@ -1,0 +1,478 @@
+"""Benchmark: achieved HBM GB/s and us/call of bf16 RMSNorm / fused
+RMSNorm+RoPE on GB300, through the C ABI of libltxk.so.
+
+One step = one call per shape of the chosen workload (default: the bf16
+RMSNorm shape sweep [2x1024x2048], [4x1024x2048], [2x4096x3072],
+[4x4096x3072]).  Inputs are seeded, synthetic and resident in HBM before the
+timed region; L2 is flushed (a 2x-L2 write) between steps, outside the
+events.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ltxk|reference]
+
+--impl reference times the fp64 CPU oracle on this host's cores on a bounded
+row sample of the same workload (the method's plain definition, not a GPU
+implementation).  Under torchrun (N > 1) every rank runs the workload on its
+own GPU (weak scaling, no data exchange); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("achieved HBM GB/s (% of GB300 peak) for bf16 RMSNorm / "
+          "RMSNorm+RoPE; µs/call")
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "rope_element_dit_gb300", "csrc")
+
+WORKLOAD_TITLES = {
+    "sweep": "bf16 RMSNorm shape sweep [2x1024x2048], [4x1024x2048], "
+             "[2x4096x3072], [4x4096x3072]; N(0,1) with 1% x50 outliers, "
+             "w ~ N(1,0.1), eps 1e-6, seeds 1-4",
+    "small": "bf16 RMSNorm [1x1024x2048], N(0,1), w ~ N(1,0.1), eps 1e-6, seed 0",
+    "rope_interleaved": "fused RMSNorm + interleaved RoPE, x [2, 4096, 32x128], "
+                        "fp32 cos/sin [4096, 64] (theta 1e4), seed 5",
+    "rope_split": "fused RMSNorm + split-half RoPE, x [1, 6144, 32x64], 3-axis "
+                  "positions 8x24x32, fp32 cos/sin [6144, 32], seed 6",
+    "stress": "bf16 RMSNorm [4x16384x4096], [262143x2560], [65536x5120], "
+              "U(-4,4), eps 1e-5, seeds 7-9",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="sweep", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ltxk", choices=["ltxk", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, digest):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split("\t")
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload \
+                and parts[2] == digest:
+            return int(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+    QUERY = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 11:
+                continue
+            if self.bus_id and self.bus_id not in f[2].lower() and \
+                    f[2].lower()[-12:] != self.bus_id[-12:]:
+                continue
+            rows.append((ts, f))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.25] or \
+            sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+        sm = [float(f[3]) for _, f in inside if f[3].replace(".", "").isdigit()]
+        mx = [float(f[4]) for _, f in inside if f[4].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for _, f in inside:
+            for name, v in zip(names, f[7:11]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max((float(f[5]) for _, f in inside
+                                    if f[5].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------- oracle timing --
+
+def cpu_oracle_time(cases, inputs, row_frac, threads):
+    """Run the oracle over the first ceil(row_frac * rows) rows of every case;
+    returns (seconds, algorithmic bytes)."""
+    import oracle
+    t = 0.0
+    b = 0
+    for c, inp in zip(cases, inputs):
+        r = max(1, math.ceil(c.rows * row_frac))
+        x = inp["x"][:r]
+        t0 = time.perf_counter()
+        if c.mode is None:
+            oracle.rms_norm(x, inp["w"], c.eps, threads=threads)
+        else:
+            oracle.rms_norm_rope(x, inp["w"], inp["cos"], inp["sin"], c.heads, c.head_dim,
+                                 c.mode, c.eps, table_rows=c.seq_len, threads=threads)
+        t += time.perf_counter() - t0
+        b += 4 * r * c.hidden + 2 * c.hidden + (
+            8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0)
+    return t, b
+
+
+def cpu_baseline(cases, inputs, seconds):
+    threads = os.cpu_count() or 1
+    # calibrate on a 1% row sample, then size the sample to ~`seconds`
+    t, _ = cpu_oracle_time(cases, inputs, 0.01, threads)
+    frac = min(1.0, max(0.01, 0.01 * seconds / max(t, 1e-6)))
+    reps = 1
+    if frac >= 1.0:
+        t_full, _ = cpu_oracle_time(cases, inputs, 1.0, threads)
+        reps = max(1, int(seconds / max(t_full, 1e-6)))
+    tot_t, tot_b = 0.0, 0
+    for _ in range(reps):
+        tt, bb = cpu_oracle_time(cases, inputs, frac, threads)
+        tot_t += tt
+        tot_b += bb
+    sample = (f"fp64 C oracle, {threads} threads over row blocks, first "
+              f"{frac * 100:.1f}% of the rows of every shape"
+              + (f", {reps} repetitions" if reps > 1 else "")
+              + f", {tot_t:.1f} s")
+    return {"value": round(tot_b / tot_t / 1e9, 3), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "sample": sample}
+
+
+def run_reference(args, cases, inputs, world, rank):
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    budget = 120.0      # seconds of oracle work for the whole run
+    t1, _ = cpu_oracle_time(cases, inputs, 0.01, threads)
+    per_step = budget / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1e-4, 0.01 * per_step / max(t1, 1e-9)))
+    for _ in range(args.warmup):
+        cpu_oracle_time(cases, inputs, frac, threads)
+    tt = 0.0
+    bb = 0
+    for _ in range(args.steps):
+        t, b = cpu_oracle_time(cases, inputs, frac, threads)
+        tt += t
+        bb += b
+    value = bb / tt / 1e9
+    sample = (f"fp64 C oracle on {threads} host threads; each step the first "
+              f"{frac * 100:.3g}% of the rows of every shape")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TITLES[args.workload], "row_fraction": frac},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- GPU timing --
+
+def kernel_name(plan, mode):
+    import rope_element_dit_gb300 as L
+    if plan.kernel == L.KERNEL_ROWS_VEC:
+        km = 0 if mode is None else (1 if mode == 0 else 2)
+        return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
+    km = 0 if mode is None else (1 if mode == 0 else 2)
+    return f"rows_elem_kernel<{km}>"
+
+
+def run_ltxk(args, cases, inputs, world, rank, local):
+    import torch
+    import rope_element_dit_gb300 as L
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    props = torch.cuda.get_device_properties(dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    # resident inputs and outputs
+    dev_bufs = []
+    for c, inp in zip(cases, inputs):
+        d = {"x": torch.from_numpy(inp["x"].view(np.int16)).to(dev),
+             "w": torch.from_numpy(inp["w"].view(np.int16)).to(dev),
+             "y": torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)}
+        if c.mode is not None:
+            d["cos"] = torch.from_numpy(inp["cos"]).to(dev)
+            d["sin"] = torch.from_numpy(inp["sin"]).to(dev)
+        dev_bufs.append(d)
+
+    def launch(i, x=None, y=None):
+        c, d = cases[i], dev_bufs[i]
+        x = d["x"] if x is None else x
+        y = d["y"] if y is None else y
+        if c.mode is None:
+            st = L.ltxk_rms_norm(y.data_ptr(), x.data_ptr(), d["w"].data_ptr(), c.rows,
+                                 c.hidden, c.eps, sptr)
+        else:
+            st = L.ltxk_rms_norm_rope_seq(y.data_ptr(), x.data_ptr(), d["w"].data_ptr(),
+                                          d["cos"].data_ptr(), d["sin"].data_ptr(), c.rows,
+                                          c.heads, c.head_dim, c.mode, c.eps, c.seq_len,
+                                          sptr)
+        if st != L.OK:
+            raise L.LtxkError(st, "bench launch")
+
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+
+    n = len(cases)
+    bytes_per_launch = [synth.algorithmic_bytes(c) for c in cases]
+    bytes_per_step = sum(bytes_per_launch)
+    plans = []
+    for c in cases:
+        op = L.OP_RMS_NORM if c.mode is None else L.OP_RMS_NORM_ROPE
+        st, p = L.ltxk_plan_launch(op, c.rows, c.hidden, c.head_dim, c.mode or 0, True)
+        plans.append(kernel_name(p, c.mode))
+
+    for i in range(args.warmup):
+        flush_l2(i)
+        for j in range(n):
+            launch(j)
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+          for _ in range(args.steps)]
+    bus = getattr(props, "pci_bus_id", None)
+    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.6)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush_l2(i)
+        ev[i][0].record(stream)
+        for j in range(n):
+            launch(j)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    if not args.no_clocks:
+        time.sleep(0.3)
+        sampler.stop()
+
+    per_launch = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(n)]
+                           for i in range(args.steps)], dtype=np.float64)   # ms
+    step_ms = per_launch.sum(axis=1)
+    total_s = step_ms.sum() / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * bytes_per_step * args.steps / total_s / 1e9
+
+    # dominant kernel: the kernel instance with the largest share of time
+    by_kernel = {}
+    for j, name in enumerate(plans):
+        k = by_kernel.setdefault(name, {"bytes": 0, "ms": 0.0, "launches": 0})
+        k["bytes"] += bytes_per_launch[j] * args.steps
+        k["ms"] += per_launch[:, j].sum()
+        k["launches"] += args.steps
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+    peak, peak_kind = measured_peak()
+    achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
+    digest = source_digest()
+    traffic = recorded_traffic(dom_name, args.workload, digest)
+
+    per_shape = []
+    for j, c in enumerate(cases):
+        us = per_launch[:, j] * 1e3
+        med = float(np.median(us))
+        per_shape.append({
+            "case": c.name, "kernel": plans[j], "bytes": bytes_per_launch[j],
+            "us_median": round(med, 3), "us_p10": round(float(np.percentile(us, 10)), 3),
+            "us_p90": round(float(np.percentile(us, 90)), 3),
+            "gbps_median": round(bytes_per_launch[j] / med / 1e3, 1),
+            "frac_of_peak": round(bytes_per_launch[j] / med / 1e3 / peak, 4)})
+
+    # e2e: host (pinned) -> device copy of x, the call, device -> host copy of y
+    e2e = None
+    if not args.no_e2e:
+        hx = [torch.from_numpy(inp["x"].view(np.int16)).reshape(-1).pin_memory()
+              for inp in inputs]
+        hy = [torch.empty(c.rows * c.hidden, dtype=torch.int16).pin_memory() for c in cases]
+        dx = [torch.empty_like(d["x"]).reshape(-1) for d in dev_bufs]
+        h2d = sum(h.numel() * 2 for h in hx)
+        d2h = sum(h.numel() * 2 for h in hy)
+        e_ms = []
+        for i in range(args.e2e_steps + 3):
+            flush_l2(i)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for j in range(n):
+                dx[j].copy_(hx[j], non_blocking=True)
+                launch(j, x=dx[j])
+                hy[j].copy_(dev_bufs[j]["y"], non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                e_ms.append(e0.elapsed_time(e1))
+        e2e_s = sum(e_ms) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": round(world * bytes_per_step * len(e_ms) / e2e_s / 1e9, 2),
+               "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s / len(e_ms) * 1e3, 4),
+               "note": "pinned host x -> HBM, ltxk call, HBM y -> pinned host, per "
+                       "shape, one stream; weight and tables resident"}
+
+    clocks = sampler.summary(t0, t1) if not args.no_clocks else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases, inputs, args.cpu_seconds)
+
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(float(step_ms.mean()), 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload,
+                   "l2": f"flushed between steps by a {2 * l2 >> 20} MiB write "
+                         "outside the timed events",
+                   "bytes_per_step": bytes_per_step, "per_shape": per_shape,
+                   "parallelism": f"{world} independent GPU(s), rows of a batch per GPU"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(dom["bytes"] / dom["launches"]),
+                     "launches": dom["launches"], "source_digest": digest},
+        "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu,
+        "gpu_launches": n * args.steps,
+        "device": props.name,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    cases = synth.WORKLOADS[args.workload]
+    inputs = [synth.make_inputs(c) for c in cases]
+    if args.impl == "reference":
+        run_reference(args, cases, inputs, world, rank)
+        return
+    run_ltxk(args, cases, inputs, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

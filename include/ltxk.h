@@ -1,0 +1,161 @@
+/*
+ * ltxk.h -- C ABI of libltxk.so: bf16 RMSNorm and fused RMSNorm + rotary
+ * position embedding (RoPE) on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Where the operations come from
+ *   RMSNorm: "cuda-kernels" skill page (Hugging Face), sections "Kernel-
+ *   Specific Guidelines / RMSNorm" (layout [..., hidden_size], epsilon
+ *   default 1e-6, the weight may be absent) and "RMSNorm Micro-benchmarks"
+ *   (bf16 activations shaped [batch x seq x hidden]).  The pages print no
+ *   formula; the operation implemented is, per row r of x [rows, hidden]:
+ *       y[r, j] = bf16_rne( x[r, j] * w[j] / sqrt(mean_j x[r, j]^2 + eps) )
+ *   computed in fp32 with one rounding to bfloat16 at the end.
+ *   Fused form: "ltx-kernels" README, opening list (`ops_cpp`: fused element
+ *   ops rms_norm_rope and rms_norm_split_rope) and the skill page's "Kernel-
+ *   Specific Guidelines / RoPE" ([batch, seq, heads, head_dim] text layout,
+ *   [batch, t*h*w, heads, head_dim] video layout).  The RMSNorm runs over the
+ *   full hidden = heads * head_dim with the full-length weight; then, in
+ *   registers and before the single bf16 rounding, every head is rotated pair
+ *   by pair with c = cos[pos, p], s = sin[pos, p]:
+ *       a' = a*c - b*s,   b' = a*s + b*c
+ *   LTXK_ROPE_INTERLEAVED pairs (a, b) = (h*D + 2p, h*D + 2p + 1);
+ *   LTXK_ROPE_SPLIT_HALF  pairs (a, b) = (h*D + p,  h*D + p + D/2).
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers (or managed memory) of the current
+ *     CUDA device.  bfloat16 data travel as void* (IEEE-754 binary32 upper
+ *     halves, little-endian).  All tensors are dense and row-major.
+ *   - The caller owns and allocates every buffer (the out-variant convention
+ *     of the pages' `Tensor! out` ops); the library allocates no device
+ *     memory and keeps no per-call state.
+ *   - Work is queued asynchronously on `stream` (NULL = the legacy default
+ *     stream); the call returns once the launch is queued.
+ *   - Arguments are validated on the host BEFORE any CUDA call; on error
+ *     nothing is launched and an ltxk_status is returned.
+ *   - out == x (in place) is allowed: every row is read completely before
+ *     any element of it is written.  Any other overlap of out with x, w or
+ *     the tables is rejected with LTXK_ERR_OVERLAP.
+ *   - rows == 0 is a no-op returning LTXK_OK.
+ *   - Pointers need only the 2-byte (bf16) / 4-byte (fp32) alignment of
+ *     their type.  16-byte-aligned pointers with hidden % 8 == 0 (and, for
+ *     the fused form, head_dim % 8 == 0 interleaved or % 16 == 0 split-half)
+ *     take the vectorised kernels; anything else takes the element-wise
+ *     kernel, which computes the same values.  There is no CPU fallback.
+ *   - Numerics: the sum of squares is kept in fp32, so rows whose sum of
+ *     squares exceeds FLT_MAX (elements of magnitude about 2^63 and up)
+ *     overflow; with eps == 0 an all-zero row yields NaN (0/0).
+ */
+#ifndef LTXK_H_
+#define LTXK_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LTXK_API __attribute__((visibility("default")))
+#else
+#define LTXK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (a CUDA runtime stream handle). */
+struct CUstream_st;
+typedef struct CUstream_st* ltxk_stream_t;
+
+typedef enum {
+    LTXK_OK = 0,
+    LTXK_ERR_NULL = 1,      /* a required pointer is NULL */
+    LTXK_ERR_SHAPE = 2,     /* rows < 0, hidden <= 0, heads*head_dim overflow,
+                               odd head_dim, seq_len <= 0, size limits */
+    LTXK_ERR_ALIGN = 3,     /* a pointer lacks its element's alignment */
+    LTXK_ERR_MODE = 4,      /* unknown RoPE pairing mode */
+    LTXK_ERR_OVERLAP = 5,   /* out partially overlaps x, or overlaps w/cos/sin */
+    LTXK_ERR_CUDA = 6       /* a CUDA runtime call or the launch failed; see
+                               ltxk_last_cuda_error() */
+} ltxk_status;
+
+enum { LTXK_ROPE_INTERLEAVED = 0, LTXK_ROPE_SPLIT_HALF = 1 };
+
+/* Largest hidden size (elements per row) the library accepts. */
+#define LTXK_MAX_HIDDEN (1 << 30)
+
+/*
+ * ltxk_rms_norm -- y = x * w / sqrt(mean(x^2) + eps) per row, bf16 in/out.
+ *   out    [rows, hidden] bf16, written.
+ *   x      [rows, hidden] bf16, read.
+ *   w      [hidden] bf16, or NULL for a weight of ones (the pages'
+ *          elementwise_affine=False case).
+ *   rows   >= 0.  hidden in [1, LTXK_MAX_HIDDEN].
+ *   eps    added to the mean square inside the square root (default on the
+ *          pages: 1e-6).
+ * Returns an ltxk_status.
+ */
+LTXK_API int ltxk_rms_norm(void* out, const void* x, const void* w, int64_t rows,
+                  int64_t hidden, float eps, ltxk_stream_t stream);
+
+/*
+ * ltxk_rms_norm_rope -- RMSNorm over hidden = heads*head_dim, then RoPE per
+ * head, with PER-ROW tables: row r uses cos[r, :] and sin[r, :].
+ *   out, x  [rows, heads*head_dim] bf16.   w as for ltxk_rms_norm.
+ *   cos,sin [rows, head_dim/2] fp32 (device).
+ *   heads >= 1, head_dim >= 2 and even, mode = LTXK_ROPE_*.
+ * For x shaped [batch, seq, heads*head_dim] with one [seq, head_dim/2] table
+ * per sequence, use ltxk_rms_norm_rope_seq instead of repeating the table.
+ */
+LTXK_API int ltxk_rms_norm_rope(void* out, const void* x, const void* w,
+                       const float* cos, const float* sin, int64_t rows,
+                       int heads, int head_dim, int mode, float eps,
+                       ltxk_stream_t stream);
+
+/*
+ * ltxk_rms_norm_rope_seq -- as ltxk_rms_norm_rope, with tables shared by all
+ * sequences of a batch: cos, sin are [seq_len, head_dim/2] and row r uses
+ * table row (r mod seq_len), i.e. x is [batch, seq_len, heads*head_dim].
+ * seq_len >= 1; rows need not be a multiple of seq_len.
+ */
+LTXK_API int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w,
+                           const float* cos, const float* sin, int64_t rows,
+                           int heads, int head_dim, int mode, float eps,
+                           int64_t seq_len, ltxk_stream_t stream);
+
+/* Human-readable name of an ltxk_status (static string, never NULL). */
+LTXK_API const char* ltxk_status_string(int status);
+
+/* cudaError_t value behind the calling thread's last LTXK_ERR_CUDA (0 if
+ * none yet). */
+LTXK_API int ltxk_last_cuda_error(void);
+
+/* ---- launch plan (host-only introspection; no CUDA call) -------------- */
+
+enum {
+    LTXK_KERNEL_NONE = 0,       /* rows == 0: nothing to launch */
+    LTXK_KERNEL_ROWS_VEC = 1,   /* 16-byte vectors, row in registers */
+    LTXK_KERNEL_ROWS_ELEM = 2   /* element-wise, two passes over the row */
+};
+
+enum { LTXK_OP_RMS_NORM = 0, LTXK_OP_RMS_NORM_ROPE = 1 };
+
+typedef struct {
+    int kernel;          /* LTXK_KERNEL_* */
+    int group_warps;     /* warps that share one row */
+    int vec_per_lane;    /* 16-byte vectors each lane keeps in registers */
+    int block_threads;   /* threads per CTA */
+    int rows_per_cta;    /* rows a CTA works on at a time */
+} ltxk_plan;
+
+/*
+ * ltxk_plan_launch -- the kernel choice the entry points make, for the
+ * given problem.  `vector_ok` says whether every pointer is 16-byte aligned.
+ * `mode` is ignored for LTXK_OP_RMS_NORM.  Returns an ltxk_status (the same
+ * shape and mode checks as the entry points).
+ */
+LTXK_API int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim,
+                     int mode, int vector_ok, ltxk_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LTXK_H_ */

@@ -1,0 +1,51 @@
+"""bf16 comparison for parity checks -- TEST INFRASTRUCTURE.
+
+Tolerance: at most 1 bfloat16 ulp between the tested output and the
+oracle's correctly rounded value, on every element.  It is measured as the
+distance between the two bit patterns on the ordered integer line of
+bfloat16 values (sign-magnitude mapped to a monotone integer, +0 and -0 both
+at 0), which is well defined at binade edges and at zero.  A distance of 1
+means the two values are neighbours; that happens when the exact value lies
+within the test side's fp32 error of a rounding midpoint.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def ordinal(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def is_nan(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+
+
+def ulp_distance(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    return np.abs(ordinal(got) - ordinal(ref))
+
+
+def compare_bf16(got: np.ndarray, ref: np.ndarray, max_ulps: int = 1) -> dict:
+    """Element-by-element check; returns statistics and ``ok``."""
+    got = np.asarray(got, dtype=np.uint16).reshape(-1)
+    ref = np.asarray(ref, dtype=np.uint16).reshape(-1)
+    if got.shape != ref.shape:
+        raise ValueError(f"shape mismatch {got.shape} vs {ref.shape}")
+    nan_mismatch = int(np.count_nonzero(is_nan(got) != is_nan(ref)))
+    d = ulp_distance(got, ref)
+    d = np.where(is_nan(got) & is_nan(ref), 0, d)
+    worst = int(d.max()) if d.size else 0
+    bad = np.flatnonzero(d > max_ulps)
+    return {
+        "elements": int(got.size),
+        "exact": int(np.count_nonzero(d == 0)),
+        "one_ulp": int(np.count_nonzero(d == 1)),
+        "over_tolerance": int(bad.size),
+        "max_ulps": worst,
+        "nan_mismatch": nan_mismatch,
+        "first_bad": [int(i) for i in bad[:8]],
+        "ok": bad.size == 0 and nan_mismatch == 0,
+    }

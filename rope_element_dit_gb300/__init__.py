@@ -1,0 +1,188 @@
+"""Python binding of libltxk.so: bf16 RMSNorm and fused RMSNorm + RoPE on
+one GB300 GPU.
+
+The functions named ``ltxk_*`` mirror the C ABI in ``include/ltxk.h`` one to
+one (integer device pointers in, an ``ltxk_status`` integer out).  The
+``rms_norm`` / ``rms_norm_rope`` helpers marshal torch CUDA tensors into
+those calls and raise :class:`LtxkError` on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU path, and
+importing this package fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libltxk.so")
+
+OK = 0
+ERR_NULL = 1
+ERR_SHAPE = 2
+ERR_ALIGN = 3
+ERR_MODE = 4
+ERR_OVERLAP = 5
+ERR_CUDA = 6
+
+ROPE_INTERLEAVED = 0
+ROPE_SPLIT_HALF = 1
+
+OP_RMS_NORM = 0
+OP_RMS_NORM_ROPE = 1
+
+KERNEL_NONE = 0
+KERNEL_ROWS_VEC = 1
+KERNEL_ROWS_ELEM = 2
+
+# Every entry point include/ltxk.h declares.
+EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
+           "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
+
+
+class LtxkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = f"{where}: {ltxk_status_string(status)} (status {status})"
+        if status == ERR_CUDA:
+            msg += f", cudaError {ltxk_last_cuda_error()}"
+        super().__init__(msg)
+        self.status = status
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("group_warps", ctypes.c_int),
+                ("vec_per_lane", ctypes.c_int), ("block_threads", ctypes.c_int),
+                ("rows_per_cta", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first with "
+            "`python -m rope_element_dit_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.ltxk_rms_norm.argtypes = [P, P, P, I64, I64, F32, P]
+    lib.ltxk_rms_norm_rope.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, P]
+    lib.ltxk_rms_norm_rope_seq.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, P]
+    for f in ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq"):
+        getattr(lib, f).restype = I32
+    lib.ltxk_status_string.argtypes = [I32]
+    lib.ltxk_status_string.restype = ctypes.c_char_p
+    lib.ltxk_last_cuda_error.argtypes = []
+    lib.ltxk_last_cuda_error.restype = I32
+    lib.ltxk_plan_launch.argtypes = [I32, I64, I64, I32, I32, I32, ctypes.POINTER(Plan)]
+    lib.ltxk_plan_launch.restype = I32
+    return lib
+
+
+_lib = _load()
+
+
+# ---- the C ABI, same names -------------------------------------------------
+
+def ltxk_rms_norm(out, x, w, rows, hidden, eps, stream) -> int:
+    return _lib.ltxk_rms_norm(out, x, w, rows, hidden, eps, stream)
+
+
+def ltxk_rms_norm_rope(out, x, w, cos, sin, rows, heads, head_dim, mode, eps,
+                       stream) -> int:
+    return _lib.ltxk_rms_norm_rope(out, x, w, cos, sin, rows, heads, head_dim,
+                                   mode, eps, stream)
+
+
+def ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads, head_dim, mode,
+                           eps, seq_len, stream) -> int:
+    return _lib.ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads,
+                                       head_dim, mode, eps, seq_len, stream)
+
+
+def ltxk_status_string(status: int) -> str:
+    return _lib.ltxk_status_string(status).decode()
+
+
+def ltxk_last_cuda_error() -> int:
+    return _lib.ltxk_last_cuda_error()
+
+
+def ltxk_plan_launch(op, rows, hidden, head_dim, mode, vector_ok):
+    """Returns (status, Plan)."""
+    p = Plan()
+    st = _lib.ltxk_plan_launch(op, rows, hidden, head_dim, mode,
+                               1 if vector_ok else 0, ctypes.byref(p))
+    return st, p
+
+
+# ---- torch marshalling -----------------------------------------------------
+
+def _check(status, where):
+    if status != OK:
+        raise LtxkError(status, where)
+
+
+def _stream_handle(tensor, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(tensor.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def rms_norm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
+    """y = x * weight / sqrt(mean(x^2, -1) + eps) over the last axis (bf16)."""
+    import torch
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    if out is None:
+        out = torch.empty_like(x)
+    st = ltxk_rms_norm(_dev_ptr(out, "out", torch.bfloat16),
+                       _dev_ptr(x, "x", torch.bfloat16),
+                       _dev_ptr(weight, "weight", torch.bfloat16),
+                       rows, hidden, eps, _stream_handle(x, stream))
+    _check(st, "ltxk_rms_norm")
+    return out
+
+
+def rms_norm_rope(x, weight, cos, sin, heads: int, head_dim: int,
+                  mode: int = ROPE_INTERLEAVED, eps: float = 1e-6,
+                  seq_len: int | None = None, out=None, stream=None):
+    """RMSNorm over the last axis (heads*head_dim), then RoPE per head.
+
+    ``cos``/``sin`` are fp32 ``[seq_len, head_dim/2]`` with row r of x using
+    table row ``r % seq_len`` (``seq_len`` defaults to the tables' length);
+    pass ``seq_len=None`` and tables with one row per row of x for per-row
+    tables.
+    """
+    import torch
+    hidden = heads * head_dim
+    if x.shape[-1] != hidden:
+        raise ValueError("last axis of x must be heads*head_dim")
+    rows = x.numel() // hidden
+    if out is None:
+        out = torch.empty_like(x)
+    table_rows = cos.numel() // (head_dim // 2) if seq_len is None else seq_len
+    args = (_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
+            _dev_ptr(weight, "weight", torch.bfloat16),
+            _dev_ptr(cos, "cos", torch.float32), _dev_ptr(sin, "sin", torch.float32),
+            rows, heads, head_dim, mode, eps)
+    if table_rows == rows and seq_len is None:
+        st = ltxk_rms_norm_rope(*args, _stream_handle(x, stream))
+        _check(st, "ltxk_rms_norm_rope")
+    else:
+        st = ltxk_rms_norm_rope_seq(*args, table_rows, _stream_handle(x, stream))
+        _check(st, "ltxk_rms_norm_rope_seq")
+    return out

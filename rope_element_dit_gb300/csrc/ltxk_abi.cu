@@ -1,0 +1,257 @@
+// ltxk_abi.cu -- the C ABI declared in include/ltxk.h: argument validation
+// (host only, before any CUDA call), the launch plan, and the launches.
+//
+// Operations: bf16 RMSNorm ("cuda-kernels" skill page, "Kernel-Specific
+// Guidelines / RMSNorm") and the fused RMSNorm + RoPE forms ("ltx-kernels"
+// README, opening list: rms_norm_rope, rms_norm_split_rope).  The launch
+// configuration replaces the page's "Thread Configuration" rule (one block
+// of min(hidden/2, max) threads per row) with a persistent grid sized from
+// the SM count and the kernel's occupancy.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+
+#include "ltxk.h"
+#include "ltxk_kernels.cuh"
+#include "ltxk_launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxVplSlots = 16;
+constexpr int kGroupChoices[] = {1, 2, 4, 8, 16, 32};
+
+bool aligned_to(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Do [a, a + na) and [b, b + nb) share a byte?
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int bucket_vpl(int need) {
+  if (need <= 4) return 4;
+  if (need <= 8) return 8;
+  if (need <= 12) return 12;
+  return 16;
+}
+
+int block_for_group(int g) { return g <= 8 ? 256 : 32 * g; }
+
+int kernel_mode(int op, int mode) {
+  if (op == LTXK_OP_RMS_NORM) return ltxk::kPlain;
+  return mode == LTXK_ROPE_INTERLEAVED ? ltxk::kInterleaved : ltxk::kSplitHalf;
+}
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return LTXK_ERR_CUDA;
+}
+
+// Per-device SM count and per-(kernel, device) resident CTAs per SM.
+struct DeviceCache {
+  std::mutex mu;
+  std::unordered_map<int, int> sms;
+  std::unordered_map<const void*, int> occ[64];
+};
+DeviceCache& cache() {
+  static DeviceCache c;
+  return c;
+}
+
+cudaError_t resident_ctas(const void* fn, int block, int* device_sms, int* per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DeviceCache& c = cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  auto it = c.sms.find(dev);
+  if (it == c.sms.end()) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    it = c.sms.emplace(dev, n).first;
+  }
+  *device_sms = it->second;
+  auto jt = c.occ[dev].find(fn);
+  if (jt == c.occ[dev].end()) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, 0);
+    if (e != cudaSuccess) return e;
+    jt = c.occ[dev].emplace(fn, n < 1 ? 1 : n).first;
+  }
+  *per_sm = jt->second;
+  return cudaSuccess;
+}
+
+int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
+  if (rows < 0 || hidden <= 0 || hidden > LTXK_MAX_HIDDEN) return LTXK_ERR_SHAPE;
+  if (rows > 0 && rows > INT64_MAX / 4 / hidden) return LTXK_ERR_SHAPE;
+  if (op == LTXK_OP_RMS_NORM_ROPE) {
+    if (head_dim < 2 || head_dim % 2 != 0 || hidden % head_dim != 0) return LTXK_ERR_SHAPE;
+    if (mode != LTXK_ROPE_INTERLEAVED && mode != LTXK_ROPE_SPLIT_HALF) return LTXK_ERR_MODE;
+  } else if (op != LTXK_OP_RMS_NORM) {
+    return LTXK_ERR_MODE;
+  }
+  return LTXK_OK;
+}
+
+int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool vector_ok,
+              ltxk_plan* p) {
+  const int st = check_shape(op, rows, hidden, head_dim, mode);
+  if (st != LTXK_OK) return st;
+  *p = ltxk_plan{LTXK_KERNEL_NONE, 0, 0, 0, 0};
+  if (rows == 0) return LTXK_OK;
+  const int km = kernel_mode(op, mode);
+  bool vec = vector_ok && hidden % 8 == 0;
+  if (km == ltxk::kInterleaved) vec = vec && head_dim % 8 == 0;
+  if (km == ltxk::kSplitHalf) vec = vec && head_dim % 16 == 0;
+  if (vec) {
+    const int64_t nv = hidden / 8;
+    // split-half slots are (lo, hi) pairs: nv/2 units of two slots each
+    const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
+    const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
+    for (int g : kGroupChoices) {
+      const int64_t need = (units + 32 * g - 1) / (32 * g) * slots_per_unit;
+      if (need <= kMaxVplSlots) {
+        p->kernel = LTXK_KERNEL_ROWS_VEC;
+        p->group_warps = g;
+        p->vec_per_lane = bucket_vpl(static_cast<int>(need));
+        p->block_threads = block_for_group(g);
+        p->rows_per_cta = p->block_threads / (32 * g);
+        return LTXK_OK;
+      }
+    }
+  }
+  p->kernel = LTXK_KERNEL_ROWS_ELEM;
+  p->group_warps = ltxk::kElemBlock / 32;
+  p->vec_per_lane = 0;
+  p->block_threads = ltxk::kElemBlock;
+  p->rows_per_cta = 1;
+  return LTXK_OK;
+}
+
+int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStream_t stream) {
+  ltxk_plan p;
+  int st = make_plan(op, args.rows, args.hidden, args.head_dim, mode, vector_ok, &p);
+  if (st != LTXK_OK || p.kernel == LTXK_KERNEL_NONE) return st;
+  const int km = kernel_mode(op, mode);
+  const void* fn = nullptr;
+  if (p.kernel == LTXK_KERNEL_ROWS_VEC) {
+    switch (km) {
+      case ltxk::kPlain: fn = ltxk::rows_vec_plain_ptr(p.group_warps, p.vec_per_lane); break;
+      case ltxk::kInterleaved:
+        fn = ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
+        break;
+      default: fn = ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane); break;
+    }
+  } else {
+    fn = ltxk::rows_elem_kernel_ptr(km);
+  }
+  if (fn == nullptr) return fail_cuda(cudaErrorInvalidDeviceFunction);
+  int sms = 0, per_sm = 0;
+  cudaError_t e = resident_ctas(fn, p.block_threads, &sms, &per_sm);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  const unsigned grid = static_cast<unsigned>(needed < cap ? needed : cap);
+  ltxk::RowArgs a = args;
+  void* params[] = {&a};
+  e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params, 0, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LTXK_OK;
+}
+
+int rope_common(void* out, const void* x, const void* w, const float* cos, const float* sin,
+                int64_t rows, int heads, int head_dim, int mode, float eps, int64_t table_rows,
+                cudaStream_t stream) {
+  if (out == nullptr || x == nullptr || cos == nullptr || sin == nullptr) return LTXK_ERR_NULL;
+  if (heads < 1 || head_dim < 2 || head_dim % 2 != 0 || table_rows < 1) return LTXK_ERR_SHAPE;
+  const int64_t hidden = static_cast<int64_t>(heads) * head_dim;
+  int st = check_shape(LTXK_OP_RMS_NORM_ROPE, rows, hidden, head_dim, mode);
+  if (st != LTXK_OK) return st;
+  if (table_rows > INT64_MAX / 8 / head_dim) return LTXK_ERR_SHAPE;
+  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2)) ||
+      !aligned_to(cos, 4) || !aligned_to(sin, 4))
+    return LTXK_ERR_ALIGN;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  const uint64_t tbytes = static_cast<uint64_t>(table_rows) * (head_dim / 2) * 4;
+  if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
+  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2) ||
+      overlaps(out, xbytes, cos, tbytes) || overlaps(out, xbytes, sin, tbytes))
+    return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
+                         aligned_to(cos, 16) && aligned_to(sin, 16);
+  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
+                  static_cast<const uint16_t*>(w), cos, sin, rows, table_rows,
+                  static_cast<int>(hidden), head_dim, eps};
+  return launch(LTXK_OP_RMS_NORM_ROPE, mode, a, vector_ok, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ltxk_rms_norm(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
+                  float eps, ltxk_stream_t stream) {
+  if (out == nullptr || x == nullptr) return LTXK_ERR_NULL;
+  int st = check_shape(LTXK_OP_RMS_NORM, rows, hidden, 0, 0);
+  if (st != LTXK_OK) return st;
+  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2))) return LTXK_ERR_ALIGN;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
+  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2)) return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16));
+  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
+                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
+                  static_cast<int>(hidden), 0, eps};
+  return launch(LTXK_OP_RMS_NORM, 0, a, vector_ok, stream);
+}
+
+int ltxk_rms_norm_rope(void* out, const void* x, const void* w, const float* cos,
+                       const float* sin, int64_t rows, int heads, int head_dim, int mode,
+                       float eps, ltxk_stream_t stream) {
+  // Per-row tables: row r uses table row r.  With rows == 0 there is no
+  // table at all; any positive table_rows gives the same (empty) launch.
+  return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps,
+                     rows > 0 ? rows : 1, stream);
+}
+
+int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w, const float* cos,
+                           const float* sin, int64_t rows, int heads, int head_dim, int mode,
+                           float eps, int64_t seq_len, ltxk_stream_t stream) {
+  return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len, stream);
+}
+
+const char* ltxk_status_string(int status) {
+  switch (status) {
+    case LTXK_OK: return "ok";
+    case LTXK_ERR_NULL: return "a required pointer is NULL";
+    case LTXK_ERR_SHAPE: return "invalid shape";
+    case LTXK_ERR_ALIGN: return "pointer not aligned to its element size";
+    case LTXK_ERR_MODE: return "unknown RoPE pairing mode";
+    case LTXK_ERR_OVERLAP: return "output overlaps an input (other than exactly in place)";
+    case LTXK_ERR_CUDA: return "CUDA runtime error (see ltxk_last_cuda_error)";
+    default: return "unknown status";
+  }
+}
+
+int ltxk_last_cuda_error(void) { return g_last_cuda_error; }
+
+int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim, int mode, int vector_ok,
+                     ltxk_plan* plan) {
+  if (plan == nullptr) return LTXK_ERR_NULL;
+  return make_plan(op, rows, hidden, head_dim, mode, vector_ok != 0, plan);
+}
+
+}  // extern "C"

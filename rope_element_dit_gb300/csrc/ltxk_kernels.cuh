@@ -1,0 +1,399 @@
+// ltxk_kernels.cuh -- device code for bf16 RMSNorm and fused RMSNorm + RoPE
+// on sm_103a (GB300).
+//
+// The operation (no formula is printed on the pages; this is the definition
+// the library implements):
+//   per row r:  ms = (1/H) sum_j x_j^2,  n_j = x_j * w_j / sqrt(ms + eps)
+//   fused:      per head and pair (a, b):  a' = a c - b s,  b' = a s + b c
+//   one round-to-nearest-even to bfloat16 at the end.
+// Sources: "cuda-kernels" skill page (Hugging Face), "Kernel-Specific
+// Guidelines / RMSNorm" and "/ RoPE", "Core Kernel Patterns / Vectorized
+// Memory Access" and "/ Warp Shuffle Reductions"; "ltx-kernels" README,
+// opening list (`ops_cpp`: rms_norm_rope, rms_norm_split_rope).
+//
+// The path is bound by HBM bandwidth (4 bytes moved per element against a
+// handful of fp32 operations), so it uses no tensor cores.  Design:
+//   * Each row is read from HBM exactly once, as 16-byte vectors, into
+//     registers; a group of G warps owns one row (G = 1 for hidden <= 4096).
+//   * fp32 sum of squares: per-lane partials, an xor-butterfly over the
+//     warp, then (G > 1) a fixed-order sum of the G warp totals through
+//     shared memory.  Every thread ends with the same bit-identical total.
+//   * inv_rms = rsqrtf(ss / H + eps); y = (x * w) * inv_rms, where x * w is
+//     exact in fp32 (two 8-bit significands), so each output is one fp32
+//     rounding away from (x w) * inv_rms before the final bf16 rounding.
+//   * RoPE rotates (u, v) = (x_a w_a, x_b w_b) (both exact) and scales by
+//     inv_rms afterwards; u c - v s and u s + v c are evaluated with Kahan's
+//     2x2-determinant algorithm (W. Kahan; error bound in Jeannerod, Louvet &
+//     Muller, "Further analysis of Kahan's algorithm for the accurate
+//     computation of 2x2 determinants", Math. Comp. 82, 2013), which keeps
+//     the relative error of a rotated value at a few fp32 ulps even when the
+//     two products nearly cancel.
+//   * Persistent grid: CTAs stride over rows, so any row count (ragged
+//     tails included) is spread over all SMs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ltxk {
+
+enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2 };
+
+struct RowArgs {
+  uint16_t* out;            // [rows, hidden] bf16
+  const uint16_t* x;        // [rows, hidden] bf16
+  const uint16_t* w;        // [hidden] bf16 or nullptr (ones)
+  const float* cos_t;       // [table_rows, head_dim/2] fp32 (fused only)
+  const float* sin_t;
+  int64_t rows;
+  int64_t table_rows;       // row r uses table row r % table_rows
+  int hidden;
+  int head_dim;
+  float eps;
+};
+
+// ---- element helpers -----------------------------------------------------
+
+// The two bf16 halves of a 32-bit word, widened exactly to fp32.
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Round two fp32 values to bf16 (RNE) and pack them, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float bf_to_f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f_to_bf(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// a*b - c*d with Kahan's algorithm: the rounding error of c*d is recovered
+// exactly by an FMA and added back.
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+  const float cd = __fmul_rn(c, d);
+  const float err = __fmaf_rn(-c, d, cd);     // cd - c*d, exact
+  const float dop = __fmaf_rn(a, b, -cd);     // a*b - cd, one rounding
+  return __fadd_rn(dop, err);
+}
+
+__device__ __forceinline__ float sum_of_products(float a, float b, float c, float d) {
+  return diff_of_products(a, b, -c, d);
+}
+
+// ---- memory helpers ------------------------------------------------------
+
+// Streaming 16-byte load: x is read once, so it should not displace L1 lines.
+// A plain (coherent) load, because out may alias x in place.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Read-only 16-byte loads for the weight and the tables (reused by every
+// row, so they stay in L1/L2).  They are volatile so that they stay in
+// program order between the stores: hoisting all of them ahead of the
+// epilogue would hold 4 more registers per slot for data that hits in L1.
+__device__ __forceinline__ uint4 ld_ro16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_ro16f(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Make the compiler treat a packed vector as freshly defined, so that the
+// widened halves computed for the sum of squares are not kept alive into
+// the epilogue (that would double the registers a row needs).
+__device__ __forceinline__ void launder(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void group_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ float sumsq8(uint4 v) {
+  float s = 0.f;
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf_lo(u[i]), b = bf_hi(u[i]);
+    s = __fmaf_rn(a, a, s);
+    s = __fmaf_rn(b, b, s);
+  }
+  return s;
+}
+
+constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
+
+// ---- vectorised row kernel -----------------------------------------------
+//
+// Thread-to-data map.  A row has NV = hidden/8 16-byte vectors.  The GT = 32G
+// threads of a row group own VPL vector slots each:
+//   plain / interleaved: slot k of thread t holds vector k*GT + t, so each
+//     warp-wide access is one contiguous 512-byte span;
+//   split-half: slots come in (lo, hi) pairs; pair j of thread t is the
+//     pair-vector q = j*GT + t, i.e. vector jv = q % QPH of head q / QPH in
+//     the first half (lo) and the same vector in the second half (hi), with
+//     QPH = head_dim/16 pair-vectors per head.  Both elements of every
+//     rotation pair are then in one thread.
+
+template <int G>
+struct GroupShape {
+  static constexpr int kThreadsPerGroup = 32 * G;
+  static constexpr int kBlock = G <= 8 ? 256 : 32 * G;
+  static constexpr int kGroupsPerCta = kBlock / kThreadsPerGroup;
+};
+
+template <int MODE, int G, int VPL>
+__global__ void __launch_bounds__(GroupShape<G>::kBlock)
+rows_vec_kernel(const RowArgs a) {
+  using S = GroupShape<G>;
+  constexpr int GT = S::kThreadsPerGroup;
+  static_assert(MODE != kSplitHalf || VPL % 2 == 0, "split-half slots come in pairs");
+  __shared__ float red[2][S::kGroupsPerCta][G];
+
+  const int tid = threadIdx.x;
+  const int group = tid / GT;
+  const int t = tid % GT;
+  const int warp_in_group = t >> 5;
+  const int lane = tid & 31;
+  const int H = a.hidden;
+  const int NV = H >> 3;
+  const bool has_w = a.w != nullptr;
+
+  // Element offsets (in bf16 units) of this thread's slots; row-invariant.
+  int off[VPL];
+  bool valid[VPL];
+  int pair0[VPL];   // first rotation-pair column of the slot (fused modes)
+  if (MODE == kSplitHalf) {
+    const int P = a.head_dim >> 1;
+    const int QPH = P >> 3;             // pair-vectors per head
+#pragma unroll
+    for (int j = 0; j < VPL / 2; ++j) {
+      const int q = j * GT + t;
+      const bool ok = q < (NV >> 1);
+      const int head = ok ? q / QPH : 0;
+      const int jv = ok ? q - head * QPH : 0;
+      off[2 * j] = head * a.head_dim + jv * 8;
+      off[2 * j + 1] = off[2 * j] + P;
+      valid[2 * j] = valid[2 * j + 1] = ok;
+      pair0[2 * j] = pair0[2 * j + 1] = jv * 8;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * GT + t;
+      valid[k] = v < NV;
+      off[k] = valid[k] ? v * 8 : 0;
+      pair0[k] = (MODE == kInterleaved && valid[k]) ? (off[k] % a.head_dim) >> 1 : 0;
+    }
+  }
+
+  const int64_t row_step = static_cast<int64_t>(gridDim.x) * S::kGroupsPerCta;
+  int parity = 0;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
+       row < a.rows; row += row_step) {
+    const uint16_t* xr = a.x + row * H;
+    uint4 v[VPL];
+#pragma unroll
+    for (int k = 0; k < VPL; ++k)
+      v[k] = valid[k] ? ld_stream16(xr + off[k]) : make_uint4(0u, 0u, 0u, 0u);
+
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) ss += sumsq8(v[k]);
+    ss = warp_sum(ss);
+    if (G > 1) {
+      if (lane == 0) red[parity][group][warp_in_group] = ss;
+      if (S::kGroupsPerCta == 1) __syncthreads();
+      else group_barrier(1 + group, GT);
+      ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < G; ++i) ss += red[parity][group][i];
+      parity ^= 1;
+    }
+    const float inv_rms = rsqrtf(__fdiv_rn(ss, static_cast<float>(H)) + a.eps);
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) launder(v[k]);
+
+    uint16_t* yr = a.out + row * H;
+    const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
+    if (MODE == kPlain) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        if (!valid[k]) continue;
+        const uint4 wv = has_w ? ld_ro16(a.w + off[k]) : ones;
+        const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float lo = __fmul_rn(__fmul_rn(bf_lo(xu[i]), bf_lo(wu[i])), inv_rms);
+          const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
+          o[i] = pack_bf2(lo, hi);
+        }
+        st16(yr + off[k], make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    } else {
+      const int P = a.head_dim >> 1;
+      const int64_t pos = row % a.table_rows;
+      const float* ct = a.cos_t + pos * P;
+      const float* st = a.sin_t + pos * P;
+      if (MODE == kInterleaved) {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+          if (!valid[k]) continue;
+          const uint4 wv = has_w ? ld_ro16(a.w + off[k]) : ones;
+          const float4 c4 = ld_ro16f(ct + pair0[k]);
+          const float4 s4 = ld_ro16f(st + pair0[k]);
+          const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+          const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+          const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+          const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
+            const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
+            const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
+            const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
+            const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
+            o[i] = pack_bf2(ra, rb);
+          }
+          st16(yr + off[k], make_uint4(o[0], o[1], o[2], o[3]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < VPL / 2; ++j) {
+          const int kl = 2 * j, kh = 2 * j + 1;
+          if (!valid[kl]) continue;
+          const uint4 wl = has_w ? ld_ro16(a.w + off[kl]) : ones;
+          const uint4 wh = has_w ? ld_ro16(a.w + off[kh]) : ones;
+          const float4 c0 = ld_ro16f(ct + pair0[kl]), c1 = ld_ro16f(ct + pair0[kl] + 4);
+          const float4 s0 = ld_ro16f(st + pair0[kl]), s1 = ld_ro16f(st + pair0[kl] + 4);
+          const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
+          const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
+          const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
+          const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
+          uint32_t ol[4], oh[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
+            const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
+            const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
+            const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
+            const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
+            const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
+            const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
+            const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
+            const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
+            const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
+            ol[i] = pack_bf2(la, lb);
+            oh[i] = pack_bf2(ha, hb);
+          }
+          st16(yr + off[kl], make_uint4(ol[0], ol[1], ol[2], ol[3]));
+          st16(yr + off[kh], make_uint4(oh[0], oh[1], oh[2], oh[3]));
+        }
+      }
+    }
+  }
+}
+
+// ---- element-wise kernel (any alignment, any hidden) ---------------------
+//
+// One CTA per row (persistent stride over rows), two passes: the first sums
+// the squares, the second re-reads the row and writes it.  In the fused
+// modes each thread owns whole rotation pairs, so out may alias x in place.
+
+constexpr int kElemBlock = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* scratch /* [32] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int i = 0; i < nw; ++i) t += scratch[i];
+  __syncthreads();
+  return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kElemBlock)
+rows_elem_kernel(const RowArgs a) {
+  __shared__ float scratch[32];
+  const int64_t H = a.hidden;
+  const bool has_w = a.w != nullptr;
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const uint16_t* xr = a.x + row * H;
+    uint16_t* yr = a.out + row * H;
+    float ss = 0.f;
+    for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+      const float v = bf_to_f(xr[j]);
+      ss = __fmaf_rn(v, v, ss);
+    }
+    // block_sum ends with a barrier, so every read of this row is done
+    // before any thread writes it (in-place safe), and scratch is free for
+    // the next row.
+    ss = block_sum(ss, scratch);
+    const float inv_rms = rsqrtf(__fdiv_rn(ss, static_cast<float>(H)) + a.eps);
+    if (MODE == kPlain) {
+      for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+        const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
+        yr[j] = f_to_bf(__fmul_rn(__fmul_rn(bf_to_f(xr[j]), wj), inv_rms));
+      }
+    } else {
+      const int64_t D = a.head_dim, P = D >> 1;
+      const int64_t pos = row % a.table_rows;
+      const float* ct = a.cos_t + pos * P;
+      const float* st = a.sin_t + pos * P;
+      for (int64_t q = threadIdx.x; q < (H >> 1); q += blockDim.x) {
+        const int64_t head = q / P, p = q - head * P;
+        const int64_t ia = MODE == kInterleaved ? head * D + 2 * p : head * D + p;
+        const int64_t ib = MODE == kInterleaved ? ia + 1 : ia + P;
+        const float wa = has_w ? bf_to_f(a.w[ia]) : 1.f;
+        const float wb = has_w ? bf_to_f(a.w[ib]) : 1.f;
+        const float u = __fmul_rn(bf_to_f(xr[ia]), wa);
+        const float v = __fmul_rn(bf_to_f(xr[ib]), wb);
+        const float c = ct[p], s = st[p];
+        const float ra = __fmul_rn(diff_of_products(u, c, v, s), inv_rms);
+        const float rb = __fmul_rn(sum_of_products(u, s, v, c), inv_rms);
+        yr[ia] = f_to_bf(ra);
+        yr[ib] = f_to_bf(rb);
+      }
+    }
+  }
+}
+
+}  // namespace ltxk

@@ -1,0 +1,16 @@
+// ltxk_launch.h -- internal interface between the C-ABI front end
+// (ltxk_abi.cu) and the translation units that instantiate the kernels.
+#pragma once
+
+namespace ltxk {
+
+// Kernel function for (group warps, vector slots per lane), or nullptr if
+// that combination is not instantiated.  One function per pairing mode.
+const void* rows_vec_plain_ptr(int group_warps, int vec_per_lane);
+const void* rows_vec_interleaved_ptr(int group_warps, int vec_per_lane);
+const void* rows_vec_split_ptr(int group_warps, int vec_per_lane);
+
+// Element-wise kernel for a mode (0 plain, 1 interleaved, 2 split-half).
+const void* rows_elem_kernel_ptr(int mode);
+
+}  // namespace ltxk

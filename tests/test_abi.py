@@ -1,0 +1,173 @@
+"""Host-side checks of the C ABI: the library loads, exports exactly what
+include/ltxk.h declares, rejects bad arguments before any CUDA call, and
+plans the kernel the shapes call for.  No GPU work happens here: every call
+either fails validation or has rows == 0, and the fake pointers used are
+never dereferenced."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ltxk.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rope_element_dit_gb300 import build
+    build.build()
+    import rope_element_dit_gb300
+    return rope_element_dit_gb300
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LTXK_API\s+[\w\s\*]+?\b(ltxk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for required in ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import ctypes
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert sorted(L.EXPORTS) == declared_functions()
+
+
+def test_exported_symbols_are_only_the_abi(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    text_syms = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {s for s in text_syms if s.startswith("ltxk_")}
+    assert ours == set(declared_functions())
+
+
+# Fake, never-dereferenced device addresses (16-byte aligned, far apart).
+A = 0x7F0000000000
+B = 0x7F0100000000
+W = 0x7F0200000000
+C = 0x7F0300000000
+S = 0x7F0400000000
+
+
+def test_status_strings(L):
+    for st in range(0, 7):
+        assert L.ltxk_status_string(st)
+    assert L.ltxk_status_string(99) == "unknown status"
+
+
+def test_rms_norm_validation(L):
+    f = L.ltxk_rms_norm
+    assert f(None, B, W, 4, 8, 1e-6, None) == L.ERR_NULL
+    assert f(A, None, W, 4, 8, 1e-6, None) == L.ERR_NULL
+    assert f(A, B, W, -1, 8, 1e-6, None) == L.ERR_SHAPE
+    assert f(A, B, W, 4, 0, 1e-6, None) == L.ERR_SHAPE
+    assert f(A, B, W, 4, (1 << 30) + 1, 1e-6, None) == L.ERR_SHAPE
+    assert f(A, B, W, 1 << 62, 1 << 10, 1e-6, None) == L.ERR_SHAPE
+    assert f(A + 1, B, W, 4, 8, 1e-6, None) == L.ERR_ALIGN
+    assert f(A, B + 1, W, 4, 8, 1e-6, None) == L.ERR_ALIGN
+    assert f(A, B, W + 1, 4, 8, 1e-6, None) == L.ERR_ALIGN
+    # out overlaps x partially (x's rows are 16 bytes, out starts 2 bytes in)
+    assert f(A + 2, A, W, 4, 8, 1e-6, None) == L.ERR_OVERLAP
+    # out overlaps w
+    assert f(A, B, A + 8, 4, 8, 1e-6, None) == L.ERR_OVERLAP
+    # rows == 0 is a no-op, also in place; no CUDA call is made
+    assert f(A, B, W, 0, 8, 1e-6, None) == L.OK
+    assert f(A, A, None, 0, 8, 1e-6, None) == L.OK
+
+
+def test_rope_validation(L):
+    f = L.ltxk_rms_norm_rope
+    g = L.ltxk_rms_norm_rope_seq
+    assert f(A, B, W, None, S, 4, 2, 8, 0, 1e-6, None) == L.ERR_NULL
+    assert f(A, B, W, C, None, 4, 2, 8, 0, 1e-6, None) == L.ERR_NULL
+    assert f(A, B, W, C, S, 4, 2, 7, 0, 1e-6, None) == L.ERR_SHAPE      # odd D
+    assert f(A, B, W, C, S, 4, 0, 8, 0, 1e-6, None) == L.ERR_SHAPE      # no heads
+    assert f(A, B, W, C, S, 4, 2, 0, 0, 1e-6, None) == L.ERR_SHAPE
+    assert f(A, B, W, C, S, 4, 1 << 20, 1 << 12, 0, 1e-6, None) == L.ERR_SHAPE
+    assert f(A, B, W, C, S, 4, 2, 8, 2, 1e-6, None) == L.ERR_MODE
+    assert f(A, B, W, C, S, 4, 2, 8, -1, 1e-6, None) == L.ERR_MODE
+    assert f(A, B, W, C + 2, S, 4, 2, 8, 0, 1e-6, None) == L.ERR_ALIGN
+    assert f(A, B, W, C, S + 1, 4, 2, 8, 0, 1e-6, None) == L.ERR_ALIGN
+    assert g(A, B, W, C, S, 4, 2, 8, 0, 1e-6, 0, None) == L.ERR_SHAPE    # seq_len
+    assert g(A, B, W, C, S, 4, 2, 8, 0, 1e-6, -3, None) == L.ERR_SHAPE
+    # out overlaps a table: 4 rows x 16 elements x 2 B = 128 B of out
+    assert g(A, B, W, A + 64, S, 4, 2, 8, 0, 1e-6, 4, None) == L.ERR_OVERLAP
+    assert g(A, B, W, C, A + 100, 4, 2, 8, 1, 1e-6, 4, None) == L.ERR_OVERLAP
+    assert g(A, B, W, C, S, 0, 2, 8, 1, 1e-6, 4, None) == L.OK
+    assert f(A, A, None, C, S, 0, 2, 8, 1, 1e-6, None) == L.OK
+
+
+@pytest.mark.parametrize("op,rows,hidden,D,mode,vec,kernel,G,vpl", [
+    # plain RMSNorm: one warp per row up to 4096, two warps for 5120
+    (0, 16384, 2048, 0, 0, True, 1, 1, 8),
+    (0, 16384, 3072, 0, 0, True, 1, 1, 12),
+    (0, 65536, 4096, 0, 0, True, 1, 1, 16),
+    (0, 262143, 2560, 0, 0, True, 1, 1, 12),
+    (0, 65536, 5120, 0, 0, True, 1, 2, 12),
+    (0, 7, 131072, 0, 0, True, 1, 32, 16),
+    (0, 7, 131080, 0, 0, True, 2, 8, 0),     # beyond the register path
+    (0, 7, 264, 0, 0, True, 1, 1, 4),
+    (0, 7, 4, 0, 0, True, 2, 8, 0),          # hidden % 8 != 0
+    (0, 7, 3072, 0, 0, False, 2, 8, 0),      # unaligned pointers
+    # fused
+    (1, 8192, 4096, 128, 0, True, 1, 1, 16),
+    (1, 6144, 2048, 64, 1, True, 1, 1, 8),
+    (1, 9, 48, 24, 0, True, 1, 1, 4),
+    (1, 9, 48, 24, 1, True, 2, 8, 0),        # split needs head_dim % 16
+    (1, 9, 40, 20, 0, True, 2, 8, 0),        # interleaved needs head_dim % 8
+    (1, 9, 4096, 128, 1, False, 2, 8, 0),
+])
+def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
+    st, p = L.ltxk_plan_launch(op, rows, hidden, D, mode, vec)
+    assert st == L.OK
+    assert (p.kernel, p.group_warps, p.vec_per_lane) == (kernel, G, vpl)
+    if kernel == L.KERNEL_ROWS_VEC:
+        # the slots cover the row exactly once
+        nv = hidden // 8
+        assert 32 * G * vpl >= nv
+        assert p.block_threads == max(256, 32 * G)
+        assert p.rows_per_cta == p.block_threads // (32 * G)
+
+
+def test_plan_rows_zero_and_errors(L):
+    st, p = L.ltxk_plan_launch(0, 0, 4096, 0, 0, True)
+    assert st == L.OK and p.kernel == L.KERNEL_NONE
+    assert L.ltxk_plan_launch(1, 4, 4096, 7, 0, True)[0] == L.ERR_SHAPE
+    assert L.ltxk_plan_launch(1, 4, 4096, 128, 5, True)[0] == L.ERR_MODE
+    assert L.ltxk_plan_launch(7, 4, 4096, 128, 0, True)[0] == L.ERR_MODE
+
+
+def test_product_and_oracle_share_nothing():
+    """Neither side imports the other; they share no source file."""
+    pkg = os.path.join(ROOT, "rope_element_dit_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"\boracle\b", text), f"{fn} names the oracle"
+                assert "synth" not in text, f"{fn} uses the input generator"
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "rope_element_dit_gb300" not in text and "ltxk" not in text, fn
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """Importing the binding with no built library raises ImportError (no
+    silent fallback)."""
+    import importlib.util
+    import shutil
+    d = tmp_path / "pkgcopy"
+    d.mkdir()
+    shutil.copy(os.path.join(ROOT, "rope_element_dit_gb300", "__init__.py"), d / "__init__.py")
+    spec = importlib.util.spec_from_file_location("pkgcopy", d / "__init__.py")
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)

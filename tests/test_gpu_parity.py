@@ -1,0 +1,355 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on the
+same seeded inputs, element by element.
+
+Tolerance (from the definition of the output as one RNE rounding of the exact
+value): at most 1 bf16 ulp between GPU and oracle on every element -- the
+ordinal distance of oracle/compare.py.  The GPU computes in fp32 with a
+relative error of a few 1e-6 (sum of squares, rsqrtf, Kahan-evaluated
+rotation), far below the 2^-8 bf16 spacing, so a difference can only be a
+neighbouring value near a rounding midpoint.
+
+Covers every workload at full size (in the launch configuration the
+benchmark times), small shapes that span several CTAs with ragged tails,
+every kernel family (16-byte vector path, element-wise path), weight-less
+calls, in-place calls, unaligned pointers, guard bands, non-default streams
+and run-to-run determinism.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rope_element_dit_gb300 as L
+import synth
+from oracle.compare import compare_bf16
+
+pytestmark = pytest.mark.gpu
+
+THREADS = min(32, os.cpu_count() or 1)
+CANARY = 0x7FC1          # a NaN pattern the kernels never write
+GUARD = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU parity tests need a CUDA device"
+    torch.cuda.set_device(0)
+    cap = torch.cuda.get_device_capability(0)
+    assert cap == (10, 3), f"expected an sm_103 GPU, got {cap}"
+    return torch.device("cuda:0")
+
+
+def to_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def to_host(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+def guarded(n):
+    """Device buffer of n bf16 with GUARD canary elements on each side;
+    returns (whole, inner view).  The inner view starts 128 bytes in, so its
+    16-byte alignment matches the allocation's."""
+    whole = torch.full((n + 2 * GUARD,), CANARY, dtype=torch.int16, device="cuda")
+    return whole, whole[GUARD:GUARD + n]
+
+
+def check_guard(whole, n):
+    h = to_host(whole)
+    assert np.all(h[:GUARD] == CANARY) and np.all(h[GUARD + n:] == CANARY), \
+        "kernel wrote outside its output"
+
+
+def assert_parity(got, ref, what):
+    r = compare_bf16(got, ref)
+    assert r["ok"], f"{what}: {r}"
+    return r
+
+
+def compare_chunked(got, ref, what, chunk=1 << 26):
+    got = got.reshape(-1)
+    ref = ref.reshape(-1)
+    total = {"elements": 0, "exact": 0, "one_ulp": 0}
+    for s in range(0, got.size, chunk):
+        r = assert_parity(got[s:s + chunk], ref[s:s + chunk], f"{what}[{s}:]")
+        for k in total:
+            total[k] += r[k]
+    return total
+
+
+def dptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def stream_ptr():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def gpu_rms_norm(x_dev, w_dev, rows, hidden, eps, out=None):
+    if out is None:
+        out = torch.empty(rows * hidden, dtype=torch.int16, device="cuda")
+    st = L.ltxk_rms_norm(dptr(out), dptr(x_dev), dptr(w_dev), rows, hidden, eps,
+                         stream_ptr())
+    assert st == L.OK, L.ltxk_status_string(st)
+    return out
+
+
+def gpu_rope(x_dev, w_dev, c_dev, s_dev, rows, heads, D, mode, eps, seq_len=None,
+             out=None):
+    if out is None:
+        out = torch.empty(rows * heads * D, dtype=torch.int16, device="cuda")
+    if seq_len is None:
+        st = L.ltxk_rms_norm_rope(dptr(out), dptr(x_dev), dptr(w_dev), dptr(c_dev),
+                                  dptr(s_dev), rows, heads, D, mode, eps, stream_ptr())
+    else:
+        st = L.ltxk_rms_norm_rope_seq(dptr(out), dptr(x_dev), dptr(w_dev), dptr(c_dev),
+                                      dptr(s_dev), rows, heads, D, mode, eps, seq_len,
+                                      stream_ptr())
+    assert st == L.OK, L.ltxk_status_string(st)
+    return out
+
+
+# ---------------------------------------------------------------- workloads --
+
+ALL_CASES = [c for cases in synth.WORKLOADS.values() for c in cases]
+
+
+@pytest.mark.parametrize("case", ALL_CASES, ids=[c.name for c in ALL_CASES])
+def test_workload_full_size(case):
+    inp = synth.make_inputs(case)
+    x, w = inp["x"], inp["w"]
+    n = case.rows * case.hidden
+    whole, out = guarded(n)
+    xd, wd = to_dev(x), to_dev(w)
+    if case.mode is None:
+        gpu_rms_norm(xd, wd, case.rows, case.hidden, case.eps, out=out)
+        ref = oracle.rms_norm(x, w, case.eps, threads=THREADS)
+    else:
+        cd = torch.from_numpy(inp["cos"]).cuda()
+        sd = torch.from_numpy(inp["sin"]).cuda()
+        mode = case.mode
+        gpu_rope(xd, wd, cd, sd, case.rows, case.heads, case.head_dim, mode, case.eps,
+                 seq_len=case.seq_len, out=out)
+        ref = oracle.rms_norm_rope(x, w, inp["cos"], inp["sin"], case.heads,
+                                   case.head_dim, mode, case.eps, threads=THREADS)
+    torch.cuda.synchronize()
+    check_guard(whole, n)
+    stats = compare_chunked(to_host(out), ref, case.name)
+    assert stats["elements"] == n
+    if case.mode is not None:
+        # the same result through per-row tables (the 11-argument call)
+        reps = case.rows // case.seq_len
+        cd = torch.from_numpy(np.concatenate([inp["cos"]] * reps)).cuda()
+        sd = torch.from_numpy(np.concatenate([inp["sin"]] * reps)).cuda()
+        out2 = gpu_rope(xd, wd, cd, sd, case.rows, case.heads, case.head_dim, case.mode,
+                        case.eps)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, out)
+
+
+# ---------------------------------------------------------- RMSNorm shapes --
+
+NORM_SHAPES = [(1, 4), (3, 8), (37, 24), (9, 40), (1000, 264), (17, 2056),
+               (1001, 3072), (33, 5120), (19, 8200), (3, 131072), (2, 131080),
+               (2049, 2048), (5, 7), (4, 1)]
+
+
+@pytest.mark.parametrize("rows,hidden", NORM_SHAPES)
+@pytest.mark.parametrize("with_w", [True, False])
+def test_rms_norm_shapes(rows, hidden, with_w):
+    seed = 1000 + rows + hidden
+    x = synth.normal_bf16(seed, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(seed, 2, hidden, 1.0, 0.1) if with_w else None
+    whole, out = guarded(rows * hidden)
+    gpu_rms_norm(to_dev(x), None if w is None else to_dev(w), rows, hidden, 1e-6, out=out)
+    torch.cuda.synchronize()
+    check_guard(whole, rows * hidden)
+    assert_parity(to_host(out), oracle.rms_norm(x, w, 1e-6), f"{rows}x{hidden}")
+
+
+@pytest.mark.parametrize("rows,hidden", [(37, 3072), (5, 2056), (3, 24)])
+def test_rms_norm_unaligned_pointers(rows, hidden):
+    """Pointers 2 bytes off a 16-byte boundary take the element-wise kernel
+    and give the same values."""
+    x = synth.normal_bf16(7, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(7, 2, hidden, 1.0, 0.1)
+    xb = to_dev(np.concatenate([np.zeros(1, np.uint16), x.ravel()]))
+    wb = to_dev(np.concatenate([np.zeros(1, np.uint16), w]))
+    whole, out = guarded(rows * hidden + 1)
+    gpu_rms_norm(xb[1:], wb[1:], rows, hidden, 1e-6, out=out[1:])
+    torch.cuda.synchronize()
+    check_guard(whole, rows * hidden + 1)
+    assert_parity(to_host(out[1:]), oracle.rms_norm(x, w, 1e-6), "unaligned")
+
+
+@pytest.mark.parametrize("rows,hidden", [(99, 3072), (7, 5120), (5, 24), (3, 131080)])
+def test_rms_norm_in_place(rows, hidden):
+    x = synth.uniform_bf16(8, 0, rows * hidden, -4, 4).reshape(rows, hidden)
+    w = synth.normal_bf16(8, 2, hidden, 1.0, 0.1)
+    xd = to_dev(x)
+    gpu_rms_norm(xd, to_dev(w), rows, hidden, 1e-5, out=xd)
+    torch.cuda.synchronize()
+    assert_parity(to_host(xd), oracle.rms_norm(x, w, 1e-5), "in place")
+
+
+def test_rms_norm_eps_and_scale_extremes():
+    rows, hidden = 64, 2048
+    x = synth.normal_bf16(9, 0, rows * hidden).reshape(rows, hidden)
+    # rows scaled by 2^-60 .. 2^60 in steps: stresses eps relative to ms
+    k = np.arange(rows) - rows // 2
+    xs = (x.astype(np.int32) + (k[:, None] * 2 << 7)).astype(np.uint16)
+    for eps in (0.0, 1e-6, 1.0):
+        out = gpu_rms_norm(to_dev(xs), None, rows, hidden, eps)
+        torch.cuda.synchronize()
+        assert_parity(to_host(out), oracle.rms_norm(xs, None, eps), f"eps={eps}")
+
+
+def test_rms_norm_zero_rows_and_zero_input():
+    x = np.zeros((8, 2048), np.uint16)
+    out = gpu_rms_norm(to_dev(x), None, 8, 2048, 1e-6)
+    torch.cuda.synchronize()
+    assert np.all(to_host(out) == 0)
+    assert L.ltxk_rms_norm(out.data_ptr(), out.data_ptr(), None, 0, 2048, 1e-6,
+                           stream_ptr()) == L.OK
+
+
+def test_rms_norm_side_stream_and_determinism():
+    rows, hidden = 4096, 3072
+    x = synth.normal_bf16(10, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(10, 2, hidden, 1.0, 0.1)
+    xd, wd = to_dev(x), to_dev(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = gpu_rms_norm(xd, wd, rows, hidden, 1e-6)
+        b = gpu_rms_norm(xd, wd, rows, hidden, 1e-6)
+    s.synchronize()
+    assert torch.equal(a, b)
+    assert_parity(to_host(a), oracle.rms_norm(x, w, 1e-6, threads=THREADS), "stream")
+
+
+# ------------------------------------------------------------- fused shapes --
+
+ROPE_SHAPES = [  # (rows, heads, head_dim, seq_len)
+    (5, 1, 2, 5), (6, 1, 4, 3), (10, 2, 8, 4), (33, 3, 16, 11), (70, 4, 64, 24),
+    (16, 32, 128, 8), (9, 2, 6, 9), (21, 5, 48, 7), (13, 2, 40, 13),
+    (4, 64, 256, 2), (3, 80, 128, 1),
+]
+
+
+@pytest.mark.parametrize("rows,heads,D,seq_len", ROPE_SHAPES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_shapes(rows, heads, D, seq_len, mode):
+    H = heads * D
+    seed = 2000 + rows + H + mode
+    x = synth.normal_bf16(seed, 0, rows * H).reshape(rows, H)
+    w = synth.normal_bf16(seed, 2, H, 1.0, 0.1)
+    cos, sin = synth.rope_table_1d(seq_len, D)
+    whole, out = guarded(rows * H)
+    gpu_rope(to_dev(x), to_dev(w), torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+             rows, heads, D, mode, 1e-6, seq_len=seq_len, out=out)
+    torch.cuda.synchronize()
+    check_guard(whole, rows * H)
+    ref = oracle.rms_norm_rope(x, w, cos, sin, heads, D, mode, 1e-6)
+    assert_parity(to_host(out), ref, f"rope {rows}x{heads}x{D} mode {mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_unaligned_tables_and_no_weight(mode):
+    rows, heads, D, S = 40, 4, 64, 10
+    H = heads * D
+    x = synth.normal_bf16(11, 0, rows * H).reshape(rows, H)
+    cos, sin = synth.rope_table_1d(S, D)
+    # tables 4 bytes past a 16-byte boundary: element-wise kernel
+    cb = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), cos.ravel()])).cuda()
+    sb = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), sin.ravel()])).cuda()
+    out = gpu_rope(to_dev(x), None, cb[1:], sb[1:], rows, heads, D, mode, 1e-6, seq_len=S)
+    torch.cuda.synchronize()
+    ref = oracle.rms_norm_rope(x, None, cos, sin, heads, D, mode, 1e-6)
+    assert_parity(to_host(out), ref, "unaligned tables")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("heads,D", [(32, 128), (2, 6)])
+def test_rope_in_place(mode, heads, D):
+    rows, S = 48, 16
+    H = heads * D
+    x = synth.normal_bf16(12, 0, rows * H).reshape(rows, H)
+    w = synth.normal_bf16(12, 2, H, 1.0, 0.1)
+    cos, sin = synth.rope_table_1d(S, D)
+    xd = to_dev(x)
+    gpu_rope(xd, to_dev(w), torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+             rows, heads, D, mode, 1e-6, seq_len=S, out=xd)
+    torch.cuda.synchronize()
+    ref = oracle.rms_norm_rope(x, w, cos, sin, heads, D, mode, 1e-6)
+    assert_parity(to_host(xd), ref, "rope in place")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_position_zero_equals_plain_norm(mode):
+    """cos = 1, sin = 0 at position 0: the fused output of those rows is the
+    plain RMSNorm output, bit for bit."""
+    c = synth.ROPE_INTERLEAVED[0] if mode == 0 else synth.ROPE_SPLIT[0]
+    rows = 2 * c.seq_len if mode == 0 else c.seq_len
+    x = synth.make_x(c)
+    w = synth.make_w(c)
+    cos, sin = synth.make_tables(c)
+    xd, wd = to_dev(x), to_dev(w)
+    fused = gpu_rope(xd, wd, torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+                     rows, c.heads, c.head_dim, mode, c.eps, seq_len=c.seq_len)
+    plain = gpu_rms_norm(xd, wd, rows, c.hidden, c.eps)
+    torch.cuda.synchronize()
+    f = to_host(fused).reshape(rows, c.hidden)
+    p = to_host(plain).reshape(rows, c.hidden)
+    for r in range(0, rows, c.seq_len):
+        assert np.array_equal(f[r], p[r])
+
+
+def test_rope_cancellation_stress():
+    """Tables chosen so that a*c and b*s nearly cancel: the rotation is
+    evaluated with a compensated difference, so even outputs far smaller
+    than their inputs stay within 1 ulp."""
+    rows, heads, D = 64, 8, 64
+    H = heads * D
+    P = D // 2
+    x = synth.normal_bf16(13, 0, rows * H).reshape(rows, H)
+    xv = synth.bf16_bits_to_f32(x).astype(np.float64).reshape(rows, heads, D)
+    # per row r, choose the angle that zeroes pair 0 of head 0 exactly in
+    # real arithmetic (tan = a/b); fp32 rounding of the table leaves a tiny
+    # residue that the GPU must get right.
+    for mode in (0, 1):
+        if mode == 0:
+            a, b = xv[:, 0, 0], xv[:, 0, 1]
+        else:
+            a, b = xv[:, 0, 0], xv[:, 0, P]
+        theta = np.arctan2(a, b)     # a cos - b sin = 0
+        ang = theta[:, None] + np.zeros((rows, P))
+        cos = np.cos(ang).astype(np.float32)
+        sin = np.sin(ang).astype(np.float32)
+        out = gpu_rope(to_dev(x), None, torch.from_numpy(cos).cuda(),
+                       torch.from_numpy(sin).cuda(), rows, heads, D, mode, 1e-6)
+        torch.cuda.synchronize()
+        ref = oracle.rms_norm_rope(x, None, cos, sin, heads, D, mode, 1e-6)
+        assert_parity(to_host(out), ref, f"cancellation mode {mode}")
+
+
+def test_binding_helpers_match_abi():
+    rows, H = 300, 4096
+    x = synth.normal_bf16(14, 0, rows * H).reshape(rows, H)
+    w = synth.normal_bf16(14, 2, H, 1.0, 0.1)
+    xt = to_dev(x).view(torch.bfloat16)
+    wt = to_dev(w).view(torch.bfloat16)
+    y = L.rms_norm(xt, wt, 1e-6)
+    cos, sin = synth.rope_table_1d(rows, 128)
+    yr = L.rms_norm_rope(xt, wt, torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+                         32, 128, L.ROPE_INTERLEAVED, 1e-6)
+    torch.cuda.synchronize()
+    assert_parity(y.view(torch.int16).cpu().numpy().view(np.uint16),
+                  oracle.rms_norm(x, w, 1e-6), "helper")
+    assert_parity(yr.view(torch.int16).cpu().numpy().view(np.uint16),
+                  oracle.rms_norm_rope(x, w, cos, sin, 32, 128, 0, 1e-6), "helper rope")
+    with pytest.raises(L.LtxkError):
+        L.rms_norm_rope(xt, wt, torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+                        32, 128, 7, 1e-6)
