@@ -336,8 +336,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
           for _ in range(args.steps)]
-    bus = getattr(props, "pci_bus_id", None)
-    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    try:
+        bus = "{:08X}:{:02X}:{:02X}.0".format(props.pci_domain_id, props.pci_bus_id,
+                                              props.pci_device_id)
+    except AttributeError:
+        bus = None
+    sampler = ClockSampler(bus)
     if not args.no_clocks:
         sampler.start()
         time.sleep(0.6)
