@@ -61,7 +61,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build it first with "
-            "`python -m rope_element_dit_gb300.build` (needs nvcc)")
+            "`python rope_element_dit_gb300/build.py` (needs nvcc)")
     lib = ctypes.CDLL(LIB_PATH)
     P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     lib.ltxk_rms_norm.argtypes = [P, P, P, I64, I64, F32, P]

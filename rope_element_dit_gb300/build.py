@@ -1,7 +1,8 @@
 """Build libltxk.so in-tree with nvcc for sm_103a (GB300).
 
 The translation units compile in parallel; one ``-gencode`` target only.
-``python -m rope_element_dit_gb300.build`` runs it from the command line.
+``python rope_element_dit_gb300/build.py`` runs it from the command line (not
+``-m``: importing the package loads the library this script builds).
 """
 from __future__ import annotations
 

@@ -14,8 +14,8 @@ HEADER = os.path.join(ROOT, "include", "ltxk.h")
 
 @pytest.fixture(scope="module")
 def L():
-    from rope_element_dit_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import rope_element_dit_gb300
     return rope_element_dit_gb300
 
