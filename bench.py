@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "registers", "tma"],
+                    help="kernel family for the vectorised cases")
     return ap.parse_args()
 
 
@@ -317,11 +319,17 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         if st != L.OK:
             raise L.LtxkError(st, "bench launch")
 
+    L.ltxk_set_path({"auto": L.PATH_AUTO, "registers": L.PATH_REGISTERS,
+                     "tma": L.PATH_TMA}[args.path])
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(2 * l2, dtype=torch.uint8, device=dev)
 
     def flush_l2(i):
-        flush.fill_(i & 0xFF)
+        # write 2x L2 (evicts everything), then read another 2x L2 so that the
+        # written lines are written back here and L2 is left clean and cold
+        flush_w.fill_(i & 0xFF)
+        flush_r.sum()
 
     n = len(cases)
     bytes_per_launch = [synth.algorithmic_bytes(c) for c in cases]
@@ -338,8 +346,8 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             launch(j)
     torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-          for _ in range(args.steps)]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)] for _ in range(args.steps)]
     # A GPU-side spin before each step's first event gives the host time to
     # queue the whole step, so no launch latency of the host lands inside the
     # events (the spin, like the L2 flush, is outside them).
@@ -349,7 +357,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             launch(j)
     torch.cuda.synchronize()
     host_per_step = (time.perf_counter() - t_host) / 20
-    spin_cycles = int(min(5e6, max(2e5, 4 * host_per_step * 2.0e9)))
+    spin_cycles = int(min(2e6, max(1e5, 4 * host_per_step / n * 2.0e9)))
     try:
         bus = "{:08X}:{:02X}:{:02X}.0".format(props.pci_domain_id, props.pci_bus_id,
                                               props.pci_device_id)
@@ -364,12 +372,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(args.steps):
-        flush_l2(i)
-        torch.cuda._sleep(spin_cycles)
-        ev[i][0].record(stream)
         for j in range(n):
+            flush_l2(i * n + j)
+            torch.cuda._sleep(spin_cycles)
+            ev[i][j][0].record(stream)
             launch(j)
-            ev[i][j + 1].record(stream)
+            ev[i][j][1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if world > 1:
@@ -378,7 +386,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         time.sleep(0.3)
         sampler.stop()
 
-    per_launch = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(n)]
+    per_launch = np.array([[ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(n)]
                            for i in range(args.steps)], dtype=np.float64)   # ms
     step_ms = per_launch.sum(axis=1)
     total_s = step_ms.sum() / 1e3
@@ -468,11 +476,13 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload,
                    "timing": "CUDA events around each launch on the launching stream; "
-                             "a GPU spin before each step keeps host launch latency "
+                             "a GPU spin before each launch keeps host launch latency "
                              "out of the events",
                    "host_us_per_step": round(host_per_step * 1e6, 1),
-                   "l2": f"flushed between steps by a {2 * l2 >> 20} MiB write "
-                         "outside the timed events",
+                   "l2": f"flushed before every launch, outside the timed events: a "
+                         f"{2 * l2 >> 20} MiB write, then a {2 * l2 >> 20} MiB read of "
+                         "another buffer (cold and clean L2 at kernel start)",
+                   "path": args.path,
                    "bytes_per_step": bytes_per_step, "per_shape": per_shape,
                    "parallelism": f"{world} independent GPU(s), rows of a batch per GPU"},
         "frac_of_peak": round(value / world / peak, 4),

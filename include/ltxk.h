@@ -72,8 +72,10 @@ typedef enum {
     LTXK_ERR_ALIGN = 3,     /* a pointer lacks its element's alignment */
     LTXK_ERR_MODE = 4,      /* unknown RoPE pairing mode */
     LTXK_ERR_OVERLAP = 5,   /* out partially overlaps x, or overlaps w/cos/sin */
-    LTXK_ERR_CUDA = 6       /* a CUDA runtime call or the launch failed; see
+    LTXK_ERR_CUDA = 6,      /* a CUDA runtime call or the launch failed; see
                                ltxk_last_cuda_error() */
+    LTXK_ERR_TIMEOUT = 7    /* a kernel gave up waiting for a bulk copy (see
+                               ltxk_fault_status) */
 } ltxk_status;
 
 enum { LTXK_ROPE_INTERLEAVED = 0, LTXK_ROPE_SPLIT_HALF = 1 };
@@ -120,6 +122,43 @@ LTXK_API int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w,
                            int heads, int head_dim, int mode, float eps,
                            int64_t seq_len, ltxk_stream_t stream);
 
+/*
+ * ltxk_fault_status -- did any kernel on the current device give up waiting
+ * since the last call?  The TMA-ring kernel bounds each wait for a bulk copy
+ * of a row (about two seconds); a wait that runs out sets a device fault
+ * word, lets the warp's other copies land, and ends the warp without writing
+ * the rows it had left.  This call waits for the device to finish
+ * (cudaDeviceSynchronize), reads and clears that word, and returns LTXK_OK,
+ * LTXK_ERR_TIMEOUT, or LTXK_ERR_CUDA.  The word lives in the library's
+ * static device memory (4 bytes per device); nothing is allocated.
+ */
+LTXK_API int ltxk_fault_status(void);
+
+/*
+ * ltxk_set_path -- process-wide choice of kernel family for the vectorised
+ * cases (for tuning and for testing every family on the same shapes):
+ * LTXK_PATH_AUTO (default), LTXK_PATH_REGISTERS (rows loaded straight into
+ * registers) or LTXK_PATH_TMA (rows streamed through a shared-memory ring by
+ * bulk copies; used where one warp can own a row, hidden <= 4096).  All
+ * families compute the same values.  Returns the previous setting, or -1
+ * for an unknown value (the setting is then unchanged).
+ */
+enum { LTXK_PATH_AUTO = 0, LTXK_PATH_REGISTERS = 1, LTXK_PATH_TMA = 2 };
+LTXK_API int ltxk_set_path(int path);
+
+/*
+ * ltxk_diag_missing_copy -- diagnostic for the bounded waits: runs the
+ * TMA-ring RMSNorm kernel on x [rows, hidden] (16-byte aligned, hidden a
+ * multiple of 8 and at most 4096) with the bulk copy of every warp's first
+ * row never issued, so that those waits run out after wait_limit_ns
+ * nanoseconds (1e3 .. 1e10).  No copy is left in flight.  Afterwards
+ * ltxk_fault_status() returns LTXK_ERR_TIMEOUT; rows whose copies did land
+ * may have been written to out.  Returns an ltxk_status for the launch.
+ */
+LTXK_API int ltxk_diag_missing_copy(void* out, const void* x, int64_t rows,
+                                    int64_t hidden, uint64_t wait_limit_ns,
+                                    ltxk_stream_t stream);
+
 /* Human-readable name of an ltxk_status (static string, never NULL). */
 LTXK_API const char* ltxk_status_string(int status);
 
@@ -132,7 +171,9 @@ LTXK_API int ltxk_last_cuda_error(void);
 enum {
     LTXK_KERNEL_NONE = 0,       /* rows == 0: nothing to launch */
     LTXK_KERNEL_ROWS_VEC = 1,   /* 16-byte vectors, row in registers */
-    LTXK_KERNEL_ROWS_ELEM = 2   /* element-wise, two passes over the row */
+    LTXK_KERNEL_ROWS_ELEM = 2,  /* element-wise, two passes over the row */
+    LTXK_KERNEL_ROWS_TMA = 3    /* one warp per row, rows streamed by bulk
+                                   copies through a shared-memory ring */
 };
 
 enum { LTXK_OP_RMS_NORM = 0, LTXK_OP_RMS_NORM_ROPE = 1 };
@@ -143,13 +184,16 @@ typedef struct {
     int vec_per_lane;    /* 16-byte vectors each lane keeps in registers */
     int block_threads;   /* threads per CTA */
     int rows_per_cta;    /* rows a CTA works on at a time */
+    int stages;          /* TMA ring: row buffers per warp (else 0) */
+    int smem_bytes;      /* dynamic shared memory per CTA */
 } ltxk_plan;
 
 /*
  * ltxk_plan_launch -- the kernel choice the entry points make, for the
- * given problem.  `vector_ok` says whether every pointer is 16-byte aligned.
- * `mode` is ignored for LTXK_OP_RMS_NORM.  Returns an ltxk_status (the same
- * shape and mode checks as the entry points).
+ * given problem, under the current ltxk_set_path setting.  `vector_ok` says
+ * whether every pointer is 16-byte aligned.  `mode` is ignored for
+ * LTXK_OP_RMS_NORM.  Returns an ltxk_status (the same shape and mode checks
+ * as the entry points).
  */
 LTXK_API int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim,
                      int mode, int vector_ok, ltxk_plan* plan);

@@ -23,6 +23,11 @@ ERR_ALIGN = 3
 ERR_MODE = 4
 ERR_OVERLAP = 5
 ERR_CUDA = 6
+ERR_TIMEOUT = 7
+
+PATH_AUTO = 0
+PATH_REGISTERS = 1
+PATH_TMA = 2
 
 ROPE_INTERLEAVED = 0
 ROPE_SPLIT_HALF = 1
@@ -33,9 +38,11 @@ OP_RMS_NORM_ROPE = 1
 KERNEL_NONE = 0
 KERNEL_ROWS_VEC = 1
 KERNEL_ROWS_ELEM = 2
+KERNEL_ROWS_TMA = 3
 
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
+           "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -51,7 +58,8 @@ class LtxkError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("group_warps", ctypes.c_int),
                 ("vec_per_lane", ctypes.c_int), ("block_threads", ctypes.c_int),
-                ("rows_per_cta", ctypes.c_int)]
+                ("rows_per_cta", ctypes.c_int), ("stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -69,6 +77,12 @@ def _load():
     lib.ltxk_rms_norm_rope_seq.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, P]
     for f in ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq"):
         getattr(lib, f).restype = I32
+    lib.ltxk_fault_status.argtypes = []
+    lib.ltxk_fault_status.restype = I32
+    lib.ltxk_set_path.argtypes = [I32]
+    lib.ltxk_set_path.restype = I32
+    lib.ltxk_diag_missing_copy.argtypes = [P, P, I64, I64, ctypes.c_uint64, P]
+    lib.ltxk_diag_missing_copy.restype = I32
     lib.ltxk_status_string.argtypes = [I32]
     lib.ltxk_status_string.restype = ctypes.c_char_p
     lib.ltxk_last_cuda_error.argtypes = []
@@ -97,6 +111,18 @@ def ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads, head_dim, mode,
                            eps, seq_len, stream) -> int:
     return _lib.ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads,
                                        head_dim, mode, eps, seq_len, stream)
+
+
+def ltxk_fault_status() -> int:
+    return _lib.ltxk_fault_status()
+
+
+def ltxk_set_path(path: int) -> int:
+    return _lib.ltxk_set_path(path)
+
+
+def ltxk_diag_missing_copy(out, x, rows, hidden, wait_limit_ns, stream) -> int:
+    return _lib.ltxk_diag_missing_copy(out, x, rows, hidden, wait_limit_ns, stream)
 
 
 def ltxk_status_string(status: int) -> str:

@@ -5,24 +5,34 @@
 // Guidelines / RMSNorm") and the fused RMSNorm + RoPE forms ("ltx-kernels"
 // README, opening list: rms_norm_rope, rms_norm_split_rope).  The launch
 // configuration replaces the page's "Thread Configuration" rule (one block
-// of min(hidden/2, max) threads per row) with a persistent grid sized from
-// the SM count and the kernel's occupancy.
+// of min(hidden/2, max) threads per row) with persistent grids sized from
+// the SM count and each kernel's occupancy.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <tuple>
 
 #include "ltxk.h"
 #include "ltxk_kernels.cuh"
 #include "ltxk_launch.h"
 
+// Device fault word set by a TMA-ring wait that ran out (one per device).
+static __device__ unsigned int g_ltxk_fault_word;
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_path{LTXK_PATH_AUTO};
 
 constexpr int kMaxVplSlots = 16;
 constexpr int kGroupChoices[] = {1, 2, 4, 8, 16, 32};
+// Dynamic shared memory a TMA-ring CTA aims for: two CTAs per SM share the
+// 228 KB of an SM, so each keeps about 100 KB of rows in flight.
+constexpr uint32_t kTmaSmemTarget = 100u * 1024u;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per mbarrier wait
 
 bool aligned_to(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -55,42 +65,72 @@ int fail_cuda(cudaError_t e) {
   return LTXK_ERR_CUDA;
 }
 
-// Per-device SM count and per-(kernel, device) resident CTAs per SM.
+uint32_t tma_stride(int64_t hidden) {
+  return static_cast<uint32_t>((hidden * 2 + 127) / 128 * 128);
+}
+
+// ---- per-device facts, queried once ---------------------------------------
+
 struct DeviceCache {
   std::mutex mu;
-  std::unordered_map<int, int> sms;
-  std::unordered_map<const void*, int> occ[64];
+  std::map<int, int> sms;
+  std::map<int, unsigned int*> fault_word;
+  std::map<std::tuple<int, const void*, int>, int> occupancy;   // (dev, fn, smem)
+  std::map<std::pair<int, const void*>, int> smem_opt_in;        // bytes set
 };
 DeviceCache& cache() {
   static DeviceCache c;
   return c;
 }
 
-cudaError_t resident_ctas(const void* fn, int block, int* device_sms, int* per_sm) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+cudaError_t device_facts(int* dev, int* sms, unsigned int** fault) {
+  cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   DeviceCache& c = cache();
   std::lock_guard<std::mutex> lock(c.mu);
-  auto it = c.sms.find(dev);
+  auto it = c.sms.find(*dev);
   if (it == c.sms.end()) {
     int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
     if (e != cudaSuccess) return e;
-    it = c.sms.emplace(dev, n).first;
-  }
-  *device_sms = it->second;
-  auto jt = c.occ[dev].find(fn);
-  if (jt == c.occ[dev].end()) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, 0);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_ltxk_fault_word);
     if (e != cudaSuccess) return e;
-    jt = c.occ[dev].emplace(fn, n < 1 ? 1 : n).first;
+    c.fault_word[*dev] = static_cast<unsigned int*>(p);
+    it = c.sms.emplace(*dev, n).first;
   }
-  *per_sm = jt->second;
+  *sms = it->second;
+  if (fault) *fault = c.fault_word[*dev];
   return cudaSuccess;
 }
+
+// Resident CTAs per SM of `fn` with `block` threads and `smem` dynamic bytes;
+// opts the function in to that much dynamic shared memory first.
+cudaError_t resident_ctas(int dev, const void* fn, int block, int smem, int* per_sm) {
+  DeviceCache& c = cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  cudaError_t e;
+  if (smem > 48 * 1024) {
+    int& set = c.smem_opt_in[{dev, fn}];
+    if (set < smem) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      set = smem;
+    }
+  }
+  auto key = std::make_tuple(dev, fn, smem);
+  auto it = c.occupancy.find(key);
+  if (it == c.occupancy.end()) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem);
+    if (e != cudaSuccess) return e;
+    it = c.occupancy.emplace(key, n < 1 ? 1 : n).first;
+  }
+  *per_sm = it->second;
+  return cudaSuccess;
+}
+
+// ---- planning -------------------------------------------------------------
 
 int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
   if (rows < 0 || hidden <= 0 || hidden > LTXK_MAX_HIDDEN) return LTXK_ERR_SHAPE;
@@ -105,10 +145,10 @@ int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
 }
 
 int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool vector_ok,
-              ltxk_plan* p) {
+              int path, ltxk_plan* p) {
   const int st = check_shape(op, rows, hidden, head_dim, mode);
   if (st != LTXK_OK) return st;
-  *p = ltxk_plan{LTXK_KERNEL_NONE, 0, 0, 0, 0};
+  *p = ltxk_plan{LTXK_KERNEL_NONE, 0, 0, 0, 0, 0, 0};
   if (rows == 0) return LTXK_OK;
   const int km = kernel_mode(op, mode);
   bool vec = vector_ok && hidden % 8 == 0;
@@ -121,51 +161,80 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
     for (int g : kGroupChoices) {
       const int64_t need = (units + 32 * g - 1) / (32 * g) * slots_per_unit;
-      if (need <= kMaxVplSlots) {
+      if (need > kMaxVplSlots) continue;
+      p->group_warps = g;
+      p->vec_per_lane = bucket_vpl(static_cast<int>(need));
+      if (g == 1 && path != LTXK_PATH_REGISTERS) {
+        const uint32_t stride = tma_stride(hidden);
+        int stages = static_cast<int>((kTmaSmemTarget - ltxk::kTmaBarBytes) /
+                                      (ltxk::kTmaWarps * stride));
+        stages = stages < 1 ? 1 : (stages > ltxk::kTmaMaxStages ? ltxk::kTmaMaxStages : stages);
+        p->kernel = LTXK_KERNEL_ROWS_TMA;
+        p->block_threads = ltxk::kTmaWarps * 32;
+        p->rows_per_cta = ltxk::kTmaWarps;
+        p->stages = stages;
+        p->smem_bytes = static_cast<int>(ltxk::kTmaBarBytes + ltxk::kTmaWarps * stages * stride);
+      } else {
         p->kernel = LTXK_KERNEL_ROWS_VEC;
-        p->group_warps = g;
-        p->vec_per_lane = bucket_vpl(static_cast<int>(need));
         p->block_threads = block_for_group(g);
         p->rows_per_cta = p->block_threads / (32 * g);
-        return LTXK_OK;
       }
+      return LTXK_OK;
     }
   }
   p->kernel = LTXK_KERNEL_ROWS_ELEM;
   p->group_warps = ltxk::kElemBlock / 32;
-  p->vec_per_lane = 0;
   p->block_threads = ltxk::kElemBlock;
   p->rows_per_cta = 1;
   return LTXK_OK;
 }
 
-int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStream_t stream) {
+const void* kernel_fn(const ltxk_plan& p, int km) {
+  switch (p.kernel) {
+    case LTXK_KERNEL_ROWS_VEC:
+      if (km == ltxk::kPlain) return ltxk::rows_vec_plain_ptr(p.group_warps, p.vec_per_lane);
+      if (km == ltxk::kInterleaved)
+        return ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
+      return ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane);
+    case LTXK_KERNEL_ROWS_TMA:
+      if (km == ltxk::kPlain) return ltxk::rows_tma_plain_ptr(p.vec_per_lane);
+      if (km == ltxk::kInterleaved) return ltxk::rows_tma_interleaved_ptr(p.vec_per_lane);
+      return ltxk::rows_tma_split_ptr(p.vec_per_lane);
+    case LTXK_KERNEL_ROWS_ELEM:
+      return ltxk::rows_elem_kernel_ptr(km);
+    default:
+      return nullptr;
+  }
+}
+
+int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStream_t stream,
+           int path, int skip_first_copy = 0, uint64_t wait_limit_ns = kWaitLimitNs) {
   ltxk_plan p;
-  int st = make_plan(op, args.rows, args.hidden, args.head_dim, mode, vector_ok, &p);
+  int st = make_plan(op, args.rows, args.hidden, args.head_dim, mode, vector_ok, path, &p);
   if (st != LTXK_OK || p.kernel == LTXK_KERNEL_NONE) return st;
   const int km = kernel_mode(op, mode);
-  const void* fn = nullptr;
-  if (p.kernel == LTXK_KERNEL_ROWS_VEC) {
-    switch (km) {
-      case ltxk::kPlain: fn = ltxk::rows_vec_plain_ptr(p.group_warps, p.vec_per_lane); break;
-      case ltxk::kInterleaved:
-        fn = ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
-        break;
-      default: fn = ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane); break;
-    }
-  } else {
-    fn = ltxk::rows_elem_kernel_ptr(km);
-  }
+  const void* fn = kernel_fn(p, km);
   if (fn == nullptr) return fail_cuda(cudaErrorInvalidDeviceFunction);
-  int sms = 0, per_sm = 0;
-  cudaError_t e = resident_ctas(fn, p.block_threads, &sms, &per_sm);
+  int dev = 0, sms = 0, per_sm = 0;
+  unsigned int* fault = nullptr;
+  cudaError_t e = device_facts(&dev, &sms, &fault);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = resident_ctas(dev, fn, p.block_threads, p.smem_bytes, &per_sm);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   const unsigned grid = static_cast<unsigned>(needed < cap ? needed : cap);
-  ltxk::RowArgs a = args;
-  void* params[] = {&a};
-  e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params, 0, stream);
+  if (p.kernel == LTXK_KERNEL_ROWS_TMA) {
+    ltxk::TmaArgs ta{args, p.stages, tma_stride(args.hidden), wait_limit_ns, skip_first_copy,
+                     fault};
+    void* params[] = {&ta};
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params,
+                         static_cast<size_t>(p.smem_bytes), stream);
+  } else {
+    ltxk::RowArgs a = args;
+    void* params[] = {&a};
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params, 0, stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e);
   return LTXK_OK;
 }
@@ -194,7 +263,18 @@ int rope_common(void* out, const void* x, const void* w, const float* cos, const
   ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
                   static_cast<const uint16_t*>(w), cos, sin, rows, table_rows,
                   static_cast<int>(hidden), head_dim, eps};
-  return launch(LTXK_OP_RMS_NORM_ROPE, mode, a, vector_ok, stream);
+  return launch(LTXK_OP_RMS_NORM_ROPE, mode, a, vector_ok, stream, g_path.load());
+}
+
+int norm_checks(void* out, const void* x, const void* w, int64_t rows, int64_t hidden) {
+  if (out == nullptr || x == nullptr) return LTXK_ERR_NULL;
+  int st = check_shape(LTXK_OP_RMS_NORM, rows, hidden, 0, 0);
+  if (st != LTXK_OK) return st;
+  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2))) return LTXK_ERR_ALIGN;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
+  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2)) return LTXK_ERR_OVERLAP;
+  return LTXK_OK;
 }
 
 }  // namespace
@@ -203,19 +283,13 @@ extern "C" {
 
 int ltxk_rms_norm(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
                   float eps, ltxk_stream_t stream) {
-  if (out == nullptr || x == nullptr) return LTXK_ERR_NULL;
-  int st = check_shape(LTXK_OP_RMS_NORM, rows, hidden, 0, 0);
-  if (st != LTXK_OK) return st;
-  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2))) return LTXK_ERR_ALIGN;
-  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
-  if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
-  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2)) return LTXK_ERR_OVERLAP;
-  if (rows == 0) return LTXK_OK;
+  int st = norm_checks(out, x, w, rows, hidden);
+  if (st != LTXK_OK || rows == 0) return st;
   const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16));
   ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
                   static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
                   static_cast<int>(hidden), 0, eps};
-  return launch(LTXK_OP_RMS_NORM, 0, a, vector_ok, stream);
+  return launch(LTXK_OP_RMS_NORM, 0, a, vector_ok, stream, g_path.load());
 }
 
 int ltxk_rms_norm_rope(void* out, const void* x, const void* w, const float* cos,
@@ -233,6 +307,44 @@ int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w, const float*
   return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len, stream);
 }
 
+int ltxk_fault_status(void) {
+  int dev = 0, sms = 0;
+  unsigned int* fault = nullptr;
+  cudaError_t e = device_facts(&dev, &sms, &fault);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e);
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, fault, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(fault, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return LTXK_ERR_TIMEOUT;
+  }
+  return LTXK_OK;
+}
+
+int ltxk_set_path(int path) {
+  if (path != LTXK_PATH_AUTO && path != LTXK_PATH_REGISTERS && path != LTXK_PATH_TMA) return -1;
+  return g_path.exchange(path);
+}
+
+int ltxk_diag_missing_copy(void* out, const void* x, int64_t rows, int64_t hidden,
+                           uint64_t wait_limit_ns, ltxk_stream_t stream) {
+  int st = norm_checks(out, x, nullptr, rows, hidden);
+  if (st != LTXK_OK) return st;
+  if (hidden % 8 != 0 || hidden > 4096 || wait_limit_ns < 1000ull ||
+      wait_limit_ns > 10000000000ull)
+    return LTXK_ERR_SHAPE;
+  if (!aligned_to(out, 16) || !aligned_to(x, 16)) return LTXK_ERR_ALIGN;
+  if (rows == 0) return LTXK_OK;
+  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x), nullptr,
+                  nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, 1e-6f};
+  return launch(LTXK_OP_RMS_NORM, 0, a, true, stream, LTXK_PATH_TMA, 1, wait_limit_ns);
+}
+
 const char* ltxk_status_string(int status) {
   switch (status) {
     case LTXK_OK: return "ok";
@@ -242,6 +354,7 @@ const char* ltxk_status_string(int status) {
     case LTXK_ERR_MODE: return "unknown RoPE pairing mode";
     case LTXK_ERR_OVERLAP: return "output overlaps an input (other than exactly in place)";
     case LTXK_ERR_CUDA: return "CUDA runtime error (see ltxk_last_cuda_error)";
+    case LTXK_ERR_TIMEOUT: return "a kernel gave up waiting for a bulk copy";
     default: return "unknown status";
   }
 }
@@ -251,7 +364,7 @@ int ltxk_last_cuda_error(void) { return g_last_cuda_error; }
 int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim, int mode, int vector_ok,
                      ltxk_plan* plan) {
   if (plan == nullptr) return LTXK_ERR_NULL;
-  return make_plan(op, rows, hidden, head_dim, mode, vector_ok != 0, plan);
+  return make_plan(op, rows, hidden, head_dim, mode, vector_ok != 0, g_path.load(), plan);
 }
 
 }  // extern "C"

@@ -155,10 +155,10 @@ __device__ __forceinline__ float sumsq8(uint4 v) {
 
 constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
 
-// ---- vectorised row kernel -----------------------------------------------
+// ---- slot map, reduction and epilogue shared by the vectorised kernels ----
 //
-// Thread-to-data map.  A row has NV = hidden/8 16-byte vectors.  The GT = 32G
-// threads of a row group own VPL vector slots each:
+// Thread-to-data map.  A row has NV = hidden/8 16-byte vectors.  The GT
+// threads that share a row own VPL vector slots each:
 //   plain / interleaved: slot k of thread t holds vector k*GT + t, so each
 //     warp-wide access is one contiguous 512-byte span;
 //   split-half: slots come in (lo, hi) pairs; pair j of thread t is the
@@ -166,6 +166,144 @@ constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
 //     the first half (lo) and the same vector in the second half (hi), with
 //     QPH = head_dim/16 pair-vectors per head.  Both elements of every
 //     rotation pair are then in one thread.
+
+template <int MODE, int VPL>
+struct SlotMap {
+  int off[VPL];     // element offset of the slot's vector inside the row
+  bool valid[VPL];  // the slot exists (rows need not fill every slot)
+  int pair0[VPL];   // first rotation-pair column of the slot (fused modes)
+
+  __device__ __forceinline__ SlotMap(const RowArgs& a, int GT, int t) {
+    const int NV = a.hidden >> 3;
+    if (MODE == kSplitHalf) {
+      const int P = a.head_dim >> 1;
+      const int QPH = P >> 3;
+#pragma unroll
+      for (int j = 0; j < VPL / 2; ++j) {
+        const int q = j * GT + t;
+        const bool ok = q < (NV >> 1);
+        const int head = ok ? q / QPH : 0;
+        const int jv = ok ? q - head * QPH : 0;
+        off[2 * j] = head * a.head_dim + jv * 8;
+        off[2 * j + 1] = off[2 * j] + P;
+        valid[2 * j] = valid[2 * j + 1] = ok;
+        pair0[2 * j] = pair0[2 * j + 1] = jv * 8;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) {
+        const int v = k * GT + t;
+        valid[k] = v < NV;
+        off[k] = valid[k] ? v * 8 : 0;
+        pair0[k] = (MODE == kInterleaved && valid[k]) ? (off[k] % a.head_dim) >> 1 : 0;
+      }
+    }
+  }
+};
+
+template <int VPL>
+__device__ __forceinline__ float slots_sumsq(const uint4 (&v)[VPL]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) ss += sumsq8(v[k]);
+  return ss;
+}
+
+__device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
+  return rsqrtf(__fdiv_rn(ss, static_cast<float>(a.hidden)) + a.eps);
+}
+
+// Scale (and rotate) the thread's slots of one row and store them.
+template <int MODE, int VPL>
+__device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
+                                             uint4 (&v)[VPL], const SlotMap<MODE, VPL>& m,
+                                             float inv_rms) {
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) launder(v[k]);
+  const bool has_w = a.w != nullptr;
+  uint16_t* yr = a.out + row * a.hidden;
+  const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
+  if (MODE == kPlain) {
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      if (!m.valid[k]) continue;
+      const uint4 wv = has_w ? ld_ro16(a.w + m.off[k]) : ones;
+      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__fmul_rn(bf_lo(xu[i]), bf_lo(wu[i])), inv_rms);
+        const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
+        o[i] = pack_bf2(lo, hi);
+      }
+      st16(yr + m.off[k], make_uint4(o[0], o[1], o[2], o[3]));
+    }
+    return;
+  }
+  const int P = a.head_dim >> 1;
+  const int64_t pos = row % a.table_rows;
+  const float* ct = a.cos_t + pos * P;
+  const float* st = a.sin_t + pos * P;
+  if (MODE == kInterleaved) {
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      if (!m.valid[k]) continue;
+      const uint4 wv = has_w ? ld_ro16(a.w + m.off[k]) : ones;
+      const float4 c4 = ld_ro16f(ct + m.pair0[k]);
+      const float4 s4 = ld_ro16f(st + m.pair0[k]);
+      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+      const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
+        const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
+        const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
+        const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
+        const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
+        o[i] = pack_bf2(ra, rb);
+      }
+      st16(yr + m.off[k], make_uint4(o[0], o[1], o[2], o[3]));
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < VPL / 2; ++j) {
+    const int kl = 2 * j, kh = 2 * j + 1;
+    if (!m.valid[kl]) continue;
+    const uint4 wl = has_w ? ld_ro16(a.w + m.off[kl]) : ones;
+    const uint4 wh = has_w ? ld_ro16(a.w + m.off[kh]) : ones;
+    const float4 c0 = ld_ro16f(ct + m.pair0[kl]), c1 = ld_ro16f(ct + m.pair0[kl] + 4);
+    const float4 s0 = ld_ro16f(st + m.pair0[kl]), s1 = ld_ro16f(st + m.pair0[kl] + 4);
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
+    const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
+    const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
+    const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
+    uint32_t ol[4], oh[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
+      const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
+      const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
+      const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
+      const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
+      const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
+      const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
+      const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
+      const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
+      const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
+      ol[i] = pack_bf2(la, lb);
+      oh[i] = pack_bf2(ha, hb);
+    }
+    st16(yr + m.off[kl], make_uint4(ol[0], ol[1], ol[2], ol[3]));
+    st16(yr + m.off[kh], make_uint4(oh[0], oh[1], oh[2], oh[3]));
+  }
+}
+
+// ---- register kernel: G warps per row, row loaded straight into registers -
 
 template <int G>
 struct GroupShape {
@@ -187,52 +325,19 @@ rows_vec_kernel(const RowArgs a) {
   const int t = tid % GT;
   const int warp_in_group = t >> 5;
   const int lane = tid & 31;
-  const int H = a.hidden;
-  const int NV = H >> 3;
-  const bool has_w = a.w != nullptr;
-
-  // Element offsets (in bf16 units) of this thread's slots; row-invariant.
-  int off[VPL];
-  bool valid[VPL];
-  int pair0[VPL];   // first rotation-pair column of the slot (fused modes)
-  if (MODE == kSplitHalf) {
-    const int P = a.head_dim >> 1;
-    const int QPH = P >> 3;             // pair-vectors per head
-#pragma unroll
-    for (int j = 0; j < VPL / 2; ++j) {
-      const int q = j * GT + t;
-      const bool ok = q < (NV >> 1);
-      const int head = ok ? q / QPH : 0;
-      const int jv = ok ? q - head * QPH : 0;
-      off[2 * j] = head * a.head_dim + jv * 8;
-      off[2 * j + 1] = off[2 * j] + P;
-      valid[2 * j] = valid[2 * j + 1] = ok;
-      pair0[2 * j] = pair0[2 * j + 1] = jv * 8;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      const int v = k * GT + t;
-      valid[k] = v < NV;
-      off[k] = valid[k] ? v * 8 : 0;
-      pair0[k] = (MODE == kInterleaved && valid[k]) ? (off[k] % a.head_dim) >> 1 : 0;
-    }
-  }
+  const SlotMap<MODE, VPL> m(a, GT, t);
 
   const int64_t row_step = static_cast<int64_t>(gridDim.x) * S::kGroupsPerCta;
   int parity = 0;
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
        row < a.rows; row += row_step) {
-    const uint16_t* xr = a.x + row * H;
+    const uint16_t* xr = a.x + row * a.hidden;
     uint4 v[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k)
-      v[k] = valid[k] ? ld_stream16(xr + off[k]) : make_uint4(0u, 0u, 0u, 0u);
+      v[k] = m.valid[k] ? ld_stream16(xr + m.off[k]) : make_uint4(0u, 0u, 0u, 0u);
 
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) ss += sumsq8(v[k]);
-    ss = warp_sum(ss);
+    float ss = warp_sum(slots_sumsq(v));
     if (G > 1) {
       if (lane == 0) red[parity][group][warp_in_group] = ss;
       if (S::kGroupsPerCta == 1) __syncthreads();
@@ -242,90 +347,158 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    const float inv_rms = rsqrtf(__fdiv_rn(ss, static_cast<float>(H)) + a.eps);
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) launder(v[k]);
+    row_epilogue<MODE, VPL>(a, row, v, m, inv_rms_of(ss, a));
+  }
+}
 
-    uint16_t* yr = a.out + row * H;
-    const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
-    if (MODE == kPlain) {
-#pragma unroll
-      for (int k = 0; k < VPL; ++k) {
-        if (!valid[k]) continue;
-        const uint4 wv = has_w ? ld_ro16(a.w + off[k]) : ones;
-        const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float lo = __fmul_rn(__fmul_rn(bf_lo(xu[i]), bf_lo(wu[i])), inv_rms);
-          const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
-          o[i] = pack_bf2(lo, hi);
-        }
-        st16(yr + off[k], make_uint4(o[0], o[1], o[2], o[3]));
+// ---- TMA ring kernel: one warp per row, rows streamed through shared memory -
+//
+// Each warp owns a ring of `stages` row buffers in shared memory.  Lane 0
+// keeps up to `stages` rows of x in flight with 1-D bulk copies
+// (cp.async.bulk, completion counted in bytes on one mbarrier per buffer).
+// For each row the warp waits for its buffer, copies the row into registers
+// (the same slot map as above), immediately hands the buffer back to the
+// copy engine for the row `stages` positions later, and only then reduces,
+// scales and stores.  HBM reads therefore keep flowing while rows are being
+// reduced and written, with no registers held for the rows in flight.
+//
+// Every wait is bounded (a %globaltimer limit).  A wait that runs out sets
+// bit 0 of the device fault word, waits (again bounded) for the copies this
+// warp still has in flight, and returns; the host reads the word with
+// ltxk_fault_status().
+
+constexpr int kTmaWarps = 8;
+constexpr int kTmaMaxStages = 8;
+constexpr uint32_t kTmaBarBytes = kTmaWarps * kTmaMaxStages * 8;   // 512
+
+struct TmaArgs {
+  RowArgs a;
+  int stages;               // row buffers per warp (1..kTmaMaxStages)
+  uint32_t stage_stride;    // bytes between buffers (row bytes rounded to 128)
+  uint64_t wait_limit_ns;   // bound on every mbarrier wait
+  int skip_first_copy;      // diagnostic: never issue the copy of a warp's
+                            // first row (its wait then runs out)
+  unsigned int* fault;      // device fault word
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete, for at most limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// One elected lane: expect `bytes` on the barrier, then start the copy.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+template <int MODE, int VPL>
+__global__ void __launch_bounds__(kTmaWarps * 32)
+rows_tma_kernel(const TmaArgs ta) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const RowArgs& a = ta.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = ta.stages;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.hidden) * 2u;
+  const uint32_t bars = smem_u32(smem) + warp * kTmaMaxStages * 8;
+  const uint32_t ring = smem_u32(smem) + kTmaBarBytes + warp * S * ta.stage_stride;
+  const SlotMap<MODE, VPL> m(a, 32, lane);
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kTmaWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kTmaWarps + warp;
+  // rows of this warp: first + i * nwarps, i = 0, 1, ...; row i uses buffer
+  // i % S in phase (i / S) & 1.
+  if (lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      const int64_t r = first + i * nwarps;
+      if (r >= a.rows) break;
+      if (i == 0 && ta.skip_first_copy) continue;
+      bulk_load(ring + i * ta.stage_stride, a.x + r * a.hidden, row_bytes, bars + 8 * i);
+    }
+  }
+
+  int64_t i = 0;
+  for (int64_t row = first; row < a.rows; row += nwarps, ++i) {
+    const int s = static_cast<int>(i % S);
+    const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bars + 8 * s, parity,
+                                                              ta.wait_limit_ns));
+    if (!ok) {
+      // Record the fault, then wait (bounded) for this warp's other copies
+      // in flight (rows i+1 .. i+S-1) so that none lands after the CTA exits.
+      if (lane == 0) {
+        atomicOr(ta.fault, 1u);
+        for (int64_t j = i + 1; j < i + S && first + j * nwarps < a.rows; ++j)
+          mbar_wait_bounded(bars + 8 * static_cast<int>(j % S),
+                            static_cast<uint32_t>((j / S) & 1), ta.wait_limit_ns);
       }
-    } else {
-      const int P = a.head_dim >> 1;
-      const int64_t pos = row % a.table_rows;
-      const float* ct = a.cos_t + pos * P;
-      const float* st = a.sin_t + pos * P;
-      if (MODE == kInterleaved) {
+      __syncwarp();
+      return;
+    }
+    uint4 v[VPL];
+    const uint32_t buf = ring + s * ta.stage_stride;
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-          if (!valid[k]) continue;
-          const uint4 wv = has_w ? ld_ro16(a.w + off[k]) : ones;
-          const float4 c4 = ld_ro16f(ct + pair0[k]);
-          const float4 s4 = ld_ro16f(st + pair0[k]);
-          const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-          const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-          const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-          const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
-            const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
-            const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
-            const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
-            const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
-            o[i] = pack_bf2(ra, rb);
-          }
-          st16(yr + off[k], make_uint4(o[0], o[1], o[2], o[3]));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < VPL / 2; ++j) {
-          const int kl = 2 * j, kh = 2 * j + 1;
-          if (!valid[kl]) continue;
-          const uint4 wl = has_w ? ld_ro16(a.w + off[kl]) : ones;
-          const uint4 wh = has_w ? ld_ro16(a.w + off[kh]) : ones;
-          const float4 c0 = ld_ro16f(ct + pair0[kl]), c1 = ld_ro16f(ct + pair0[kl] + 4);
-          const float4 s0 = ld_ro16f(st + pair0[kl]), s1 = ld_ro16f(st + pair0[kl] + 4);
-          const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-          const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
-          const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
-          const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
-          const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
-          uint32_t ol[4], oh[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
-            const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
-            const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
-            const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
-            const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
-            const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
-            const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
-            const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
-            const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
-            const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
-            ol[i] = pack_bf2(la, lb);
-            oh[i] = pack_bf2(ha, hb);
-          }
-          st16(yr + off[kl], make_uint4(ol[0], ol[1], ol[2], ol[3]));
-          st16(yr + off[kh], make_uint4(oh[0], oh[1], oh[2], oh[3]));
-        }
+    for (int k = 0; k < VPL; ++k)
+      v[k] = m.valid[k] ? ld_shared16(buf + m.off[k] * 2) : make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) {
+      const int64_t next = row + S * nwarps;
+      if (next < a.rows) {
+        // order this warp's generic-proxy reads of the buffer before the
+        // async-proxy write that refills it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bulk_load(buf, a.x + next * a.hidden, row_bytes, bars + 8 * s);
       }
     }
+    const float ss = warp_sum(slots_sumsq(v));
+    row_epilogue<MODE, VPL>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 

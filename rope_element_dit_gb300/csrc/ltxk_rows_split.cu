@@ -4,6 +4,7 @@
 #include "ltxk_launch.h"
 
 namespace ltxk {
+const void* rows_tma_split_ptr(int vpl) { return select_rows_tma<kSplitHalf>(vpl); }
 const void* rows_vec_split_ptr(int g, int vpl) { return select_rows_vec<kSplitHalf>(g, vpl); }
 
 const void* rows_elem_kernel_ptr(int mode) {

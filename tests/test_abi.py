@@ -57,7 +57,7 @@ S = 0x7F0400000000
 
 
 def test_status_strings(L):
-    for st in range(0, 7):
+    for st in range(0, 8):
         assert L.ltxk_status_string(st)
     assert L.ltxk_status_string(99) == "unknown status"
 
@@ -105,35 +105,71 @@ def test_rope_validation(L):
 
 
 @pytest.mark.parametrize("op,rows,hidden,D,mode,vec,kernel,G,vpl", [
-    # plain RMSNorm: one warp per row up to 4096, two warps for 5120
-    (0, 16384, 2048, 0, 0, True, 1, 1, 8),
-    (0, 16384, 3072, 0, 0, True, 1, 1, 12),
-    (0, 65536, 4096, 0, 0, True, 1, 1, 16),
-    (0, 262143, 2560, 0, 0, True, 1, 1, 12),
+    # plain RMSNorm: one warp per row (TMA ring) up to 4096, then warp groups
+    (0, 16384, 2048, 0, 0, True, 3, 1, 8),
+    (0, 16384, 3072, 0, 0, True, 3, 1, 12),
+    (0, 65536, 4096, 0, 0, True, 3, 1, 16),
+    (0, 262143, 2560, 0, 0, True, 3, 1, 12),
     (0, 65536, 5120, 0, 0, True, 1, 2, 12),
     (0, 7, 131072, 0, 0, True, 1, 32, 16),
     (0, 7, 131080, 0, 0, True, 2, 8, 0),     # beyond the register path
-    (0, 7, 264, 0, 0, True, 1, 1, 4),
+    (0, 7, 264, 0, 0, True, 3, 1, 4),
     (0, 7, 4, 0, 0, True, 2, 8, 0),          # hidden % 8 != 0
     (0, 7, 3072, 0, 0, False, 2, 8, 0),      # unaligned pointers
     # fused
-    (1, 8192, 4096, 128, 0, True, 1, 1, 16),
-    (1, 6144, 2048, 64, 1, True, 1, 1, 8),
-    (1, 9, 48, 24, 0, True, 1, 1, 4),
+    (1, 8192, 4096, 128, 0, True, 3, 1, 16),
+    (1, 6144, 2048, 64, 1, True, 3, 1, 8),
+    (1, 9, 48, 24, 0, True, 3, 1, 4),
     (1, 9, 48, 24, 1, True, 2, 8, 0),        # split needs head_dim % 16
     (1, 9, 40, 20, 0, True, 2, 8, 0),        # interleaved needs head_dim % 8
     (1, 9, 4096, 128, 1, False, 2, 8, 0),
+    (1, 9, 10240, 128, 1, True, 1, 4, 12),
 ])
 def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
     st, p = L.ltxk_plan_launch(op, rows, hidden, D, mode, vec)
     assert st == L.OK
     assert (p.kernel, p.group_warps, p.vec_per_lane) == (kernel, G, vpl)
-    if kernel == L.KERNEL_ROWS_VEC:
+    if kernel in (L.KERNEL_ROWS_VEC, L.KERNEL_ROWS_TMA):
         # the slots cover the row exactly once
         nv = hidden // 8
         assert 32 * G * vpl >= nv
+    if kernel == L.KERNEL_ROWS_VEC:
         assert p.block_threads == max(256, 32 * G)
         assert p.rows_per_cta == p.block_threads // (32 * G)
+        assert p.stages == 0 and p.smem_bytes == 0
+    if kernel == L.KERNEL_ROWS_TMA:
+        stride = (hidden * 2 + 127) // 128 * 128
+        assert p.block_threads == 256 and p.rows_per_cta == 8
+        assert 1 <= p.stages <= 8
+        assert p.smem_bytes == 512 + 8 * p.stages * stride
+        assert p.smem_bytes <= 227 * 1024
+
+
+def test_plan_follows_path_setting(L):
+    try:
+        assert L.ltxk_set_path(L.PATH_REGISTERS) == L.PATH_AUTO
+        st, p = L.ltxk_plan_launch(0, 16384, 3072, 0, 0, True)
+        assert (p.kernel, p.group_warps, p.vec_per_lane) == (L.KERNEL_ROWS_VEC, 1, 12)
+        assert L.ltxk_set_path(L.PATH_TMA) == L.PATH_REGISTERS
+        st, p = L.ltxk_plan_launch(0, 16384, 3072, 0, 0, True)
+        assert p.kernel == L.KERNEL_ROWS_TMA
+        # beyond one warp per row the register kernel stays
+        st, p = L.ltxk_plan_launch(0, 16384, 5120, 0, 0, True)
+        assert p.kernel == L.KERNEL_ROWS_VEC
+        assert L.ltxk_set_path(9) == -1
+    finally:
+        L.ltxk_set_path(L.PATH_AUTO)
+
+
+def test_diag_validation(L):
+    f = L.ltxk_diag_missing_copy
+    assert f(None, B, 4, 8, 10**6, None) == L.ERR_NULL
+    assert f(A, B, 4, 4100, 10**6, None) == L.ERR_SHAPE      # hidden > 4096
+    assert f(A, B, 4, 12, 10**6, None) == L.ERR_SHAPE        # hidden % 8
+    assert f(A, B, 4, 8, 10, None) == L.ERR_SHAPE            # limit too short
+    assert f(A, B, 4, 8, 10**11, None) == L.ERR_SHAPE        # limit too long
+    assert f(A + 2, B, 4, 8, 10**6, None) == L.ERR_ALIGN
+    assert f(A, B, 0, 8, 10**6, None) == L.OK
 
 
 def test_plan_rows_zero_and_errors(L):
