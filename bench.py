@@ -269,10 +269,11 @@ def run_reference(args, cases, inputs, world, rank):
 
 def kernel_name(plan, mode):
     import rope_element_dit_gb300 as L
-    if plan.kernel == L.KERNEL_ROWS_VEC:
-        km = 0 if mode is None else (1 if mode == 0 else 2)
-        return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
     km = 0 if mode is None else (1 if mode == 0 else 2)
+    if plan.kernel == L.KERNEL_ROWS_VEC:
+        return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
+    if plan.kernel == L.KERNEL_ROWS_TMA:
+        return f"rows_tma_kernel<{km}, {plan.vec_per_lane}>"
     return f"rows_elem_kernel<{km}>"
 
 

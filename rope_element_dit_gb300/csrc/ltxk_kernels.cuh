@@ -167,37 +167,50 @@ constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
 //     QPH = head_dim/16 pair-vectors per head.  Both elements of every
 //     rotation pair are then in one thread.
 
-template <int MODE, int VPL>
+template <int MODE, int VPL, int GT>
 struct SlotMap {
-  int off[VPL];     // element offset of the slot's vector inside the row
-  bool valid[VPL];  // the slot exists (rows need not fill every slot)
-  int pair0[VPL];   // first rotation-pair column of the slot (fused modes)
+  // plain / interleaved: slot k is vector k*GT + t, computed on the fly so
+  // the offsets fold into immediate address offsets (no per-slot registers)
+  int t, nv;
+  // split-half: per-slot offsets and validity, computed once per thread
+  int off_[MODE == kSplitHalf ? VPL : 1];
+  bool valid_[MODE == kSplitHalf ? VPL : 1];
+  // fused modes: first rotation-pair column of each slot
+  int pair_[MODE == kPlain ? 1 : VPL];
 
-  __device__ __forceinline__ SlotMap(const RowArgs& a, int GT, int t) {
-    const int NV = a.hidden >> 3;
-    if (MODE == kSplitHalf) {
+  __device__ __forceinline__ SlotMap(const RowArgs& a, int t_) : t(t_), nv(a.hidden >> 3) {
+    if constexpr (MODE == kSplitHalf) {
       const int P = a.head_dim >> 1;
       const int QPH = P >> 3;
 #pragma unroll
       for (int j = 0; j < VPL / 2; ++j) {
         const int q = j * GT + t;
-        const bool ok = q < (NV >> 1);
+        const bool ok = q < (nv >> 1);
         const int head = ok ? q / QPH : 0;
         const int jv = ok ? q - head * QPH : 0;
-        off[2 * j] = head * a.head_dim + jv * 8;
-        off[2 * j + 1] = off[2 * j] + P;
-        valid[2 * j] = valid[2 * j + 1] = ok;
-        pair0[2 * j] = pair0[2 * j + 1] = jv * 8;
+        off_[2 * j] = head * a.head_dim + jv * 8;
+        off_[2 * j + 1] = off_[2 * j] + P;
+        valid_[2 * j] = valid_[2 * j + 1] = ok;
+        pair_[2 * j] = pair_[2 * j + 1] = jv * 8;
       }
-    } else {
+    } else if constexpr (MODE == kInterleaved) {
 #pragma unroll
-      for (int k = 0; k < VPL; ++k) {
-        const int v = k * GT + t;
-        valid[k] = v < NV;
-        off[k] = valid[k] ? v * 8 : 0;
-        pair0[k] = (MODE == kInterleaved && valid[k]) ? (off[k] % a.head_dim) >> 1 : 0;
-      }
+      for (int k = 0; k < VPL; ++k) pair_[k] = valid(k) ? (off(k) % a.head_dim) >> 1 : 0;
     }
+  }
+  // element offset of slot k's vector inside the row
+  __device__ __forceinline__ int off(int k) const {
+    if constexpr (MODE == kSplitHalf) return off_[k];
+    else return (k * GT + t) * 8;
+  }
+  // slot k exists (rows need not fill every slot)
+  __device__ __forceinline__ bool valid(int k) const {
+    if constexpr (MODE == kSplitHalf) return valid_[k];
+    else return k * GT + t < nv;
+  }
+  __device__ __forceinline__ int pair0(int k) const {
+    if constexpr (MODE == kPlain) return 0;
+    else return pair_[k];
   }
 };
 
@@ -214,9 +227,9 @@ __device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
 }
 
 // Scale (and rotate) the thread's slots of one row and store them.
-template <int MODE, int VPL>
+template <int MODE, int VPL, int GT>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
-                                             uint4 (&v)[VPL], const SlotMap<MODE, VPL>& m,
+                                             uint4 (&v)[VPL], const SlotMap<MODE, VPL, GT>& m,
                                              float inv_rms) {
 #pragma unroll
   for (int k = 0; k < VPL; ++k) launder(v[k]);
@@ -226,8 +239,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   if (MODE == kPlain) {
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      if (!m.valid[k]) continue;
-      const uint4 wv = has_w ? ld_ro16(a.w + m.off[k]) : ones;
+      if (!m.valid(k)) continue;
+      const uint4 wv = has_w ? ld_ro16(a.w + m.off(k)) : ones;
       const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
       const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
       uint32_t o[4];
@@ -237,7 +250,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
         o[i] = pack_bf2(lo, hi);
       }
-      st16(yr + m.off[k], make_uint4(o[0], o[1], o[2], o[3]));
+      st16(yr + m.off(k), make_uint4(o[0], o[1], o[2], o[3]));
     }
     return;
   }
@@ -248,10 +261,10 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   if (MODE == kInterleaved) {
 #pragma unroll
     for (int k = 0; k < VPL; ++k) {
-      if (!m.valid[k]) continue;
-      const uint4 wv = has_w ? ld_ro16(a.w + m.off[k]) : ones;
-      const float4 c4 = ld_ro16f(ct + m.pair0[k]);
-      const float4 s4 = ld_ro16f(st + m.pair0[k]);
+      if (!m.valid(k)) continue;
+      const uint4 wv = has_w ? ld_ro16(a.w + m.off(k)) : ones;
+      const float4 c4 = ld_ro16f(ct + m.pair0(k));
+      const float4 s4 = ld_ro16f(st + m.pair0(k));
       const float c[4] = {c4.x, c4.y, c4.z, c4.w};
       const float s[4] = {s4.x, s4.y, s4.z, s4.w};
       const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
@@ -265,18 +278,18 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
         o[i] = pack_bf2(ra, rb);
       }
-      st16(yr + m.off[k], make_uint4(o[0], o[1], o[2], o[3]));
+      st16(yr + m.off(k), make_uint4(o[0], o[1], o[2], o[3]));
     }
     return;
   }
 #pragma unroll
   for (int j = 0; j < VPL / 2; ++j) {
     const int kl = 2 * j, kh = 2 * j + 1;
-    if (!m.valid[kl]) continue;
-    const uint4 wl = has_w ? ld_ro16(a.w + m.off[kl]) : ones;
-    const uint4 wh = has_w ? ld_ro16(a.w + m.off[kh]) : ones;
-    const float4 c0 = ld_ro16f(ct + m.pair0[kl]), c1 = ld_ro16f(ct + m.pair0[kl] + 4);
-    const float4 s0 = ld_ro16f(st + m.pair0[kl]), s1 = ld_ro16f(st + m.pair0[kl] + 4);
+    if (!m.valid(kl)) continue;
+    const uint4 wl = has_w ? ld_ro16(a.w + m.off(kl)) : ones;
+    const uint4 wh = has_w ? ld_ro16(a.w + m.off(kh)) : ones;
+    const float4 c0 = ld_ro16f(ct + m.pair0(kl)), c1 = ld_ro16f(ct + m.pair0(kl) + 4);
+    const float4 s0 = ld_ro16f(st + m.pair0(kl)), s1 = ld_ro16f(st + m.pair0(kl) + 4);
     const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
     const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
@@ -298,8 +311,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       ol[i] = pack_bf2(la, lb);
       oh[i] = pack_bf2(ha, hb);
     }
-    st16(yr + m.off[kl], make_uint4(ol[0], ol[1], ol[2], ol[3]));
-    st16(yr + m.off[kh], make_uint4(oh[0], oh[1], oh[2], oh[3]));
+    st16(yr + m.off(kl), make_uint4(ol[0], ol[1], ol[2], ol[3]));
+    st16(yr + m.off(kh), make_uint4(oh[0], oh[1], oh[2], oh[3]));
   }
 }
 
@@ -325,7 +338,7 @@ rows_vec_kernel(const RowArgs a) {
   const int t = tid % GT;
   const int warp_in_group = t >> 5;
   const int lane = tid & 31;
-  const SlotMap<MODE, VPL> m(a, GT, t);
+  const SlotMap<MODE, VPL, GT> m(a, t);
 
   const int64_t row_step = static_cast<int64_t>(gridDim.x) * S::kGroupsPerCta;
   int parity = 0;
@@ -335,7 +348,7 @@ rows_vec_kernel(const RowArgs a) {
     uint4 v[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k)
-      v[k] = m.valid[k] ? ld_stream16(xr + m.off[k]) : make_uint4(0u, 0u, 0u, 0u);
+      v[k] = m.valid(k) ? ld_stream16(xr + m.off(k)) : make_uint4(0u, 0u, 0u, 0u);
 
     float ss = warp_sum(slots_sumsq(v));
     if (G > 1) {
@@ -347,7 +360,7 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    row_epilogue<MODE, VPL>(a, row, v, m, inv_rms_of(ss, a));
+    row_epilogue<MODE, VPL, GT>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 
@@ -443,7 +456,7 @@ rows_tma_kernel(const TmaArgs ta) {
   const uint32_t row_bytes = static_cast<uint32_t>(a.hidden) * 2u;
   const uint32_t bars = smem_u32(smem) + warp * kTmaMaxStages * 8;
   const uint32_t ring = smem_u32(smem) + kTmaBarBytes + warp * S * ta.stage_stride;
-  const SlotMap<MODE, VPL> m(a, 32, lane);
+  const SlotMap<MODE, VPL, 32> m(a, lane);
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
@@ -486,7 +499,7 @@ rows_tma_kernel(const TmaArgs ta) {
     const uint32_t buf = ring + s * ta.stage_stride;
 #pragma unroll
     for (int k = 0; k < VPL; ++k)
-      v[k] = m.valid[k] ? ld_shared16(buf + m.off[k] * 2) : make_uint4(0u, 0u, 0u, 0u);
+      v[k] = m.valid(k) ? ld_shared16(buf + m.off(k) * 2) : make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     if (lane == 0) {
       const int64_t next = row + S * nwarps;
@@ -498,7 +511,7 @@ rows_tma_kernel(const TmaArgs ta) {
       }
     }
     const float ss = warp_sum(slots_sumsq(v));
-    row_epilogue<MODE, VPL>(a, row, v, m, inv_rms_of(ss, a));
+    row_epilogue<MODE, VPL, 32>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 
