@@ -46,15 +46,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(),
+          out_dir: str | None = None) -> str:
+    """Compile (only what is stale) and link libltxk.so.  ``extra_flags`` are
+    added to every nvcc compile; ``out_dir`` puts the objects and the library
+    in another directory (for building variants side by side)."""
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj_dir = OBJ_DIR if out_dir is None else os.path.join(out_dir, "_build")
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libltxk.so")
+    os.makedirs(obj_dir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "ltxk.h")]
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(obj_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
             cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
@@ -72,13 +78,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with ThreadPoolExecutor(max_workers=len(jobs) or 1) as ex:
         list(ex.map(run, jobs))
 
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
         run(cmd)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

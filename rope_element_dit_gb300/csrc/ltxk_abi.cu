@@ -31,7 +31,10 @@ constexpr int kMaxVplSlots = 16;
 constexpr int kGroupChoices[] = {1, 2, 4, 8, 16, 32};
 // Dynamic shared memory a TMA-ring CTA aims for: two CTAs per SM share the
 // 228 KB of an SM, so each keeps about 100 KB of rows in flight.
-constexpr uint32_t kTmaSmemTarget = 100u * 1024u;
+#ifndef LTXK_TMA_SMEM_TARGET
+#define LTXK_TMA_SMEM_TARGET (100u * 1024u)
+#endif
+constexpr uint32_t kTmaSmemTarget = LTXK_TMA_SMEM_TARGET;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per mbarrier wait
 
 bool aligned_to(const void* p, uintptr_t a) {

@@ -105,6 +105,18 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
                : "memory");
 }
 
+// Bring `bytes` at p (16-byte aligned, a multiple of 16) into L2 with one
+// bulk-copy-engine request; nothing is written to shared memory or registers.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// Rows ahead that the register kernel asks the bulk-copy engine to bring
+// into L2 (0 = off).
+#ifndef LTXK_L2_PREFETCH_ROWS
+#define LTXK_L2_PREFETCH_ROWS 0
+#endif
+
 // Read-only 16-byte loads for the weight and the tables (reused by every
 // row, so they stay in L1/L2).  They are volatile so that they stay in
 // program order between the stores: hoisting all of them ahead of the
@@ -345,6 +357,10 @@ rows_vec_kernel(const RowArgs a) {
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
        row < a.rows; row += row_step) {
     const uint16_t* xr = a.x + row * a.hidden;
+    if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
+      const int64_t ahead = row + LTXK_L2_PREFETCH_ROWS * row_step;
+      if (ahead < a.rows) prefetch_l2(a.x + ahead * a.hidden, static_cast<uint32_t>(a.hidden) * 2u);
+    }
     uint4 v[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k)
