@@ -56,7 +56,13 @@ int bucket_vpl(int need) {
   return 16;
 }
 
-int block_for_group(int g) { return g <= 8 ? 256 : 32 * g; }
+int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC_BLOCK; }
+
+// 1: grids of at most (resident CTAs) that stride over the rows; 0: one CTA
+// per row group and let the hardware schedule them.
+#ifndef LTXK_PERSISTENT
+#define LTXK_PERSISTENT 0
+#endif
 
 int kernel_mode(int op, int mode) {
   if (op == LTXK_OP_RMS_NORM) return ltxk::kPlain;
@@ -225,7 +231,9 @@ int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStre
   e = resident_ctas(dev, fn, p.block_threads, p.smem_bytes, &per_sm);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
-  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  const int64_t cap = (LTXK_PERSISTENT || p.kernel == LTXK_KERNEL_ROWS_TMA)
+                          ? static_cast<int64_t>(sms) * per_sm
+                          : int64_t{2147483647};
   const unsigned grid = static_cast<unsigned>(needed < cap ? needed : cap);
   if (p.kernel == LTXK_KERNEL_ROWS_TMA) {
     ltxk::TmaArgs ta{args, p.stages, tma_stride(args.hidden), wait_limit_ns, skip_first_copy,

@@ -181,48 +181,75 @@ constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
 
 template <int MODE, int VPL, int GT>
 struct SlotMap {
-  // plain / interleaved: slot k is vector k*GT + t, computed on the fly so
-  // the offsets fold into immediate address offsets (no per-slot registers)
-  int t, nv;
-  // split-half: per-slot offsets and validity, computed once per thread
-  int off_[MODE == kSplitHalf ? VPL : 1];
-  bool valid_[MODE == kSplitHalf ? VPL : 1];
-  // fused modes: first rotation-pair column of each slot
-  int pair_[MODE == kPlain ? 1 : VPL];
+  // Offsets are generated slot by slot: plain / interleaved slot k is vector
+  // k*GT + t; the rotation-pair column (interleaved) and the (head, vector in
+  // head) position (split-half) advance by fixed steps with one conditional
+  // subtraction, so no division happens inside the row loop and no per-slot
+  // registers are kept.
+  int t, nv, D, P, QPH;
+  int a0, a1, b0, b1;   // interleaved: (t*8)%D, (GT*8)%D; split: t/QPH, GT/QPH, t%QPH, GT%QPH
 
-  __device__ __forceinline__ SlotMap(const RowArgs& a, int t_) : t(t_), nv(a.hidden >> 3) {
-    if constexpr (MODE == kSplitHalf) {
-      const int P = a.head_dim >> 1;
-      const int QPH = P >> 3;
-#pragma unroll
-      for (int j = 0; j < VPL / 2; ++j) {
-        const int q = j * GT + t;
-        const bool ok = q < (nv >> 1);
-        const int head = ok ? q / QPH : 0;
-        const int jv = ok ? q - head * QPH : 0;
-        off_[2 * j] = head * a.head_dim + jv * 8;
-        off_[2 * j + 1] = off_[2 * j] + P;
-        valid_[2 * j] = valid_[2 * j + 1] = ok;
-        pair_[2 * j] = pair_[2 * j + 1] = jv * 8;
-      }
-    } else if constexpr (MODE == kInterleaved) {
-#pragma unroll
-      for (int k = 0; k < VPL; ++k) pair_[k] = valid(k) ? (off(k) % a.head_dim) >> 1 : 0;
+  __device__ __forceinline__ SlotMap(const RowArgs& a, int t_)
+      : t(t_), nv(a.hidden >> 3), D(a.head_dim), P(a.head_dim >> 1), QPH(a.head_dim >> 4),
+        a0(0), a1(0), b0(0), b1(0) {
+    if constexpr (MODE == kInterleaved) {
+      a0 = (t * 8) % D;
+      a1 = (GT * 8) % D;
+    } else if constexpr (MODE == kSplitHalf) {
+      a0 = t / QPH;
+      a1 = GT / QPH;
+      b0 = t - a0 * QPH;
+      b1 = GT - a1 * QPH;
     }
   }
-  // element offset of slot k's vector inside the row
-  __device__ __forceinline__ int off(int k) const {
-    if constexpr (MODE == kSplitHalf) return off_[k];
-    else return (k * GT + t) * 8;
+
+  // f(k, element offset, first pair column, slot exists) for every slot k.
+  template <class F>
+  __device__ __forceinline__ void each_slot(F&& f) const {
+    static_assert(MODE != kSplitHalf, "split-half slots come in pairs");
+    int r = a0;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int v = k * GT + t;
+      f(k, v * 8, r >> 1, v < nv);
+      if constexpr (MODE == kInterleaved) {
+        r += a1;
+        if (r >= D) r -= D;
+      }
+    }
   }
-  // slot k exists (rows need not fill every slot)
-  __device__ __forceinline__ bool valid(int k) const {
-    if constexpr (MODE == kSplitHalf) return valid_[k];
-    else return k * GT + t < nv;
+
+  // Split-half: f(j, offset of the lo vector, offset of the hi vector,
+  // first pair column, pair exists) for every slot pair j (slots 2j, 2j+1).
+  template <class F>
+  __device__ __forceinline__ void each_pair(F&& f) const {
+    int head = a0, jv = b0;
+#pragma unroll
+    for (int j = 0; j < VPL / 2; ++j) {
+      const int lo = head * D + jv * 8;
+      f(j, lo, lo + P, jv * 8, j * GT + t < (nv >> 1));
+      head += a1;
+      jv += b1;
+      if (jv >= QPH) {
+        jv -= QPH;
+        ++head;
+      }
+    }
   }
-  __device__ __forceinline__ int pair0(int k) const {
-    if constexpr (MODE == kPlain) return 0;
-    else return pair_[k];
+
+  // Load this thread's slots of one row (fetch(off) returns 16 bytes).
+  template <class Fetch>
+  __device__ __forceinline__ void load(uint4 (&v)[VPL], Fetch&& fetch) const {
+    if constexpr (MODE == kSplitHalf) {
+      each_pair([&](int j, int lo, int hi, int, bool ok) {
+        v[2 * j] = ok ? fetch(lo) : make_uint4(0u, 0u, 0u, 0u);
+        v[2 * j + 1] = ok ? fetch(hi) : make_uint4(0u, 0u, 0u, 0u);
+      });
+    } else {
+      each_slot([&](int k, int off, int, bool ok) {
+        v[k] = ok ? fetch(off) : make_uint4(0u, 0u, 0u, 0u);
+      });
+    }
   }
 };
 
@@ -248,11 +275,10 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   const bool has_w = a.w != nullptr;
   uint16_t* yr = a.out + row * a.hidden;
   const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
-  if (MODE == kPlain) {
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      if (!m.valid(k)) continue;
-      const uint4 wv = has_w ? ld_ro16(a.w + m.off(k)) : ones;
+  if constexpr (MODE == kPlain) {
+    m.each_slot([&](int k, int off, int, bool ok) {
+      if (!ok) return;
+      const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
       const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
       const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
       uint32_t o[4];
@@ -262,83 +288,101 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
         o[i] = pack_bf2(lo, hi);
       }
-      st16(yr + m.off(k), make_uint4(o[0], o[1], o[2], o[3]));
-    }
+      st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+    });
     return;
-  }
-  const int P = a.head_dim >> 1;
-  const int64_t pos = row % a.table_rows;
-  const float* ct = a.cos_t + pos * P;
-  const float* st = a.sin_t + pos * P;
-  if (MODE == kInterleaved) {
+  } else {
+    const int64_t pos = row % a.table_rows;
+    const float* ct = a.cos_t + pos * m.P;
+    const float* st = a.sin_t + pos * m.P;
+    if constexpr (MODE == kInterleaved) {
+      m.each_slot([&](int k, int off, int pair0, bool ok) {
+        if (!ok) return;
+        const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
+        const float4 c4 = ld_ro16f(ct + pair0);
+        const float4 s4 = ld_ro16f(st + pair0);
+        const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+        const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+        const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      if (!m.valid(k)) continue;
-      const uint4 wv = has_w ? ld_ro16(a.w + m.off(k)) : ones;
-      const float4 c4 = ld_ro16f(ct + m.pair0(k));
-      const float4 s4 = ld_ro16f(st + m.pair0(k));
-      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-      const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-      uint32_t o[4];
+        for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
+          const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
+          const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
+          const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
+          const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
+          o[i] = pack_bf2(ra, rb);
+        }
+        st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+      });
+    } else {
+      m.each_pair([&](int j, int lo_off, int hi_off, int pair0, bool ok) {
+        if (!ok) return;
+        const int kl = 2 * j, kh = 2 * j + 1;
+        const uint4 wl = has_w ? ld_ro16(a.w + lo_off) : ones;
+        const uint4 wh = has_w ? ld_ro16(a.w + hi_off) : ones;
+        const float4 c0 = ld_ro16f(ct + pair0), c1 = ld_ro16f(ct + pair0 + 4);
+        const float4 s0 = ld_ro16f(st + pair0), s1 = ld_ro16f(st + pair0 + 4);
+        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
+        const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
+        const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
+        const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
+        uint32_t ol[4], oh[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
-        const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
-        const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
-        const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
-        const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
-        o[i] = pack_bf2(ra, rb);
-      }
-      st16(yr + m.off(k), make_uint4(o[0], o[1], o[2], o[3]));
+        for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
+          const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
+          const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
+          const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
+          const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
+          const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
+          const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
+          const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
+          const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
+          const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
+          ol[i] = pack_bf2(la, lb);
+          oh[i] = pack_bf2(ha, hb);
+        }
+        st16(yr + lo_off, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+        st16(yr + hi_off, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+      });
     }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < VPL / 2; ++j) {
-    const int kl = 2 * j, kh = 2 * j + 1;
-    if (!m.valid(kl)) continue;
-    const uint4 wl = has_w ? ld_ro16(a.w + m.off(kl)) : ones;
-    const uint4 wh = has_w ? ld_ro16(a.w + m.off(kh)) : ones;
-    const float4 c0 = ld_ro16f(ct + m.pair0(kl)), c1 = ld_ro16f(ct + m.pair0(kl) + 4);
-    const float4 s0 = ld_ro16f(st + m.pair0(kl)), s1 = ld_ro16f(st + m.pair0(kl) + 4);
-    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
-    const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
-    const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
-    const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
-    uint32_t ol[4], oh[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
-      const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
-      const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
-      const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
-      const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
-      const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
-      const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
-      const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
-      const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
-      const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
-      ol[i] = pack_bf2(la, lb);
-      oh[i] = pack_bf2(ha, hb);
-    }
-    st16(yr + m.off(kl), make_uint4(ol[0], ol[1], ol[2], ol[3]));
-    st16(yr + m.off(kh), make_uint4(oh[0], oh[1], oh[2], oh[3]));
   }
 }
 
 // ---- register kernel: G warps per row, row loaded straight into registers -
 
+// Threads per CTA of the register kernel when a row group is smaller.
+#ifndef LTXK_VEC_BLOCK
+#define LTXK_VEC_BLOCK 128
+#endif
+
 template <int G>
 struct GroupShape {
   static constexpr int kThreadsPerGroup = 32 * G;
-  static constexpr int kBlock = G <= 8 ? 256 : 32 * G;
+  static constexpr int kBlock = 32 * G >= LTXK_VEC_BLOCK ? 32 * G : LTXK_VEC_BLOCK;
   static constexpr int kGroupsPerCta = kBlock / kThreadsPerGroup;
 };
 
+// Register budget per thread of the register kernel: the row's 4*VPL words
+// plus what the epilogue needs (weights, and for RoPE the cos/sin vectors).
+// Capping it lets more warps, hence more bytes of x, be in flight per SM.
+template <int MODE, int VPL>
+struct RegBudget {
+  static constexpr int kRegs = 4 * VPL + (MODE == kPlain ? 32 : (MODE == kInterleaved ? 48 : 96));
+};
 template <int MODE, int G, int VPL>
-__global__ void __launch_bounds__(GroupShape<G>::kBlock)
+struct VecLaunch {
+  static constexpr int kBlock = GroupShape<G>::kBlock;
+  static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, VPL>::kRegs);
+  static constexpr int kMinBlocks = kMin < 1 ? 1 : kMin;
+};
+
+template <int MODE, int G, int VPL>
+__global__ void __launch_bounds__(VecLaunch<MODE, G, VPL>::kBlock,
+                                  VecLaunch<MODE, G, VPL>::kMinBlocks)
 rows_vec_kernel(const RowArgs a) {
   using S = GroupShape<G>;
   constexpr int GT = S::kThreadsPerGroup;
@@ -362,9 +406,7 @@ rows_vec_kernel(const RowArgs a) {
       if (ahead < a.rows) prefetch_l2(a.x + ahead * a.hidden, static_cast<uint32_t>(a.hidden) * 2u);
     }
     uint4 v[VPL];
-#pragma unroll
-    for (int k = 0; k < VPL; ++k)
-      v[k] = m.valid(k) ? ld_stream16(xr + m.off(k)) : make_uint4(0u, 0u, 0u, 0u);
+    m.load(v, [&](int off) { return ld_stream16(xr + off); });
 
     float ss = warp_sum(slots_sumsq(v));
     if (G > 1) {
@@ -513,9 +555,7 @@ rows_tma_kernel(const TmaArgs ta) {
     }
     uint4 v[VPL];
     const uint32_t buf = ring + s * ta.stage_stride;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k)
-      v[k] = m.valid(k) ? ld_shared16(buf + m.off(k) * 2) : make_uint4(0u, 0u, 0u, 0u);
+    m.load(v, [&](int off) { return ld_shared16(buf + off * 2); });
     __syncwarp();
     if (lane == 0) {
       const int64_t next = row + S * nwarps;

@@ -134,7 +134,7 @@ def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
         nv = hidden // 8
         assert 32 * G * vpl >= nv
     if kernel == L.KERNEL_ROWS_VEC:
-        assert p.block_threads == max(256, 32 * G)
+        assert p.block_threads == max(128, 32 * G)
         assert p.rows_per_cta == p.block_threads // (32 * G)
         assert p.stages == 0 and p.smem_bytes == 0
     if kernel == L.KERNEL_ROWS_TMA:
