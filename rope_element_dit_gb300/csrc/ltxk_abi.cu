@@ -63,6 +63,9 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 #ifndef LTXK_PERSISTENT
 #define LTXK_PERSISTENT 0
 #endif
+#ifndef LTXK_PERSISTENT_ROPE
+#define LTXK_PERSISTENT_ROPE 0
+#endif
 
 int kernel_mode(int op, int mode) {
   if (op == LTXK_OP_RMS_NORM) return ltxk::kPlain;
@@ -173,7 +176,9 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
       if (need > kMaxVplSlots) continue;
       p->group_warps = g;
       p->vec_per_lane = bucket_vpl(static_cast<int>(need));
-      if (g == 1 && path != LTXK_PATH_REGISTERS) {
+      // The TMA ring is used only on request: measured on GB300 it trails
+      // the register kernel on every workload here.
+      if (g == 1 && path == LTXK_PATH_TMA) {
         const uint32_t stride = tma_stride(hidden);
         int stages = static_cast<int>((kTmaSmemTarget - ltxk::kTmaBarBytes) /
                                       (ltxk::kTmaWarps * stride));
@@ -231,7 +236,8 @@ int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStre
   e = resident_ctas(dev, fn, p.block_threads, p.smem_bytes, &per_sm);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
-  const int64_t cap = (LTXK_PERSISTENT || p.kernel == LTXK_KERNEL_ROWS_TMA)
+  const bool persistent = km == ltxk::kPlain ? LTXK_PERSISTENT : LTXK_PERSISTENT_ROPE;
+  const int64_t cap = (persistent || p.kernel == LTXK_KERNEL_ROWS_TMA)
                           ? static_cast<int64_t>(sms) * per_sm
                           : int64_t{2147483647};
   const unsigned grid = static_cast<unsigned>(needed < cap ? needed : cap);

@@ -296,11 +296,19 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
     const float* ct = a.cos_t + pos * m.P;
     const float* st = a.sin_t + pos * m.P;
     if constexpr (MODE == kInterleaved) {
+      // When the slot stride is a multiple of head_dim (a1 == 0), every slot
+      // of this thread uses the same four rotation columns: load them once.
+      const bool same_cols = m.a1 == 0;
+      float4 c4h = make_float4(0.f, 0.f, 0.f, 0.f), s4h = c4h;
+      if (same_cols) {
+        c4h = ld_ro16f(ct + (m.a0 >> 1));
+        s4h = ld_ro16f(st + (m.a0 >> 1));
+      }
       m.each_slot([&](int k, int off, int pair0, bool ok) {
         if (!ok) return;
         const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
-        const float4 c4 = ld_ro16f(ct + pair0);
-        const float4 s4 = ld_ro16f(st + pair0);
+        const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
+        const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
         const float c[4] = {c4.x, c4.y, c4.z, c4.w};
         const float s[4] = {s4.x, s4.y, s4.z, s4.w};
         const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
@@ -317,13 +325,25 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
       });
     } else {
+      // Same idea: when the pair-vector stride is a multiple of the vectors
+      // per half-head (b1 == 0), the columns are the same for every pair.
+      const bool same_cols = m.b1 == 0;
+      float4 c0h = make_float4(0.f, 0.f, 0.f, 0.f), c1h = c0h, s0h = c0h, s1h = c0h;
+      if (same_cols) {
+        c0h = ld_ro16f(ct + m.b0 * 8);
+        c1h = ld_ro16f(ct + m.b0 * 8 + 4);
+        s0h = ld_ro16f(st + m.b0 * 8);
+        s1h = ld_ro16f(st + m.b0 * 8 + 4);
+      }
       m.each_pair([&](int j, int lo_off, int hi_off, int pair0, bool ok) {
         if (!ok) return;
         const int kl = 2 * j, kh = 2 * j + 1;
         const uint4 wl = has_w ? ld_ro16(a.w + lo_off) : ones;
         const uint4 wh = has_w ? ld_ro16(a.w + hi_off) : ones;
-        const float4 c0 = ld_ro16f(ct + pair0), c1 = ld_ro16f(ct + pair0 + 4);
-        const float4 s0 = ld_ro16f(st + pair0), s1 = ld_ro16f(st + pair0 + 4);
+        const float4 c0 = same_cols ? c0h : ld_ro16f(ct + pair0);
+        const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
+        const float4 s0 = same_cols ? s0h : ld_ro16f(st + pair0);
+        const float4 s1 = same_cols ? s1h : ld_ro16f(st + pair0 + 4);
         const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
         const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};

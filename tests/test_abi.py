@@ -105,21 +105,21 @@ def test_rope_validation(L):
 
 
 @pytest.mark.parametrize("op,rows,hidden,D,mode,vec,kernel,G,vpl", [
-    # plain RMSNorm: one warp per row (TMA ring) up to 4096, then warp groups
-    (0, 16384, 2048, 0, 0, True, 3, 1, 8),
-    (0, 16384, 3072, 0, 0, True, 3, 1, 12),
-    (0, 65536, 4096, 0, 0, True, 3, 1, 16),
-    (0, 262143, 2560, 0, 0, True, 3, 1, 12),
+    # plain RMSNorm: one warp per row up to 4096, then warp groups
+    (0, 16384, 2048, 0, 0, True, 1, 1, 8),
+    (0, 16384, 3072, 0, 0, True, 1, 1, 12),
+    (0, 65536, 4096, 0, 0, True, 1, 1, 16),
+    (0, 262143, 2560, 0, 0, True, 1, 1, 12),
     (0, 65536, 5120, 0, 0, True, 1, 2, 12),
     (0, 7, 131072, 0, 0, True, 1, 32, 16),
     (0, 7, 131080, 0, 0, True, 2, 8, 0),     # beyond the register path
-    (0, 7, 264, 0, 0, True, 3, 1, 4),
+    (0, 7, 264, 0, 0, True, 1, 1, 4),
     (0, 7, 4, 0, 0, True, 2, 8, 0),          # hidden % 8 != 0
     (0, 7, 3072, 0, 0, False, 2, 8, 0),      # unaligned pointers
     # fused
-    (1, 8192, 4096, 128, 0, True, 3, 1, 16),
-    (1, 6144, 2048, 64, 1, True, 3, 1, 8),
-    (1, 9, 48, 24, 0, True, 3, 1, 4),
+    (1, 8192, 4096, 128, 0, True, 1, 1, 16),
+    (1, 6144, 2048, 64, 1, True, 1, 1, 8),
+    (1, 9, 48, 24, 0, True, 1, 1, 4),
     (1, 9, 48, 24, 1, True, 2, 8, 0),        # split needs head_dim % 16
     (1, 9, 40, 20, 0, True, 2, 8, 0),        # interleaved needs head_dim % 8
     (1, 9, 4096, 128, 1, False, 2, 8, 0),
@@ -153,6 +153,7 @@ def test_plan_follows_path_setting(L):
         assert L.ltxk_set_path(L.PATH_TMA) == L.PATH_REGISTERS
         st, p = L.ltxk_plan_launch(0, 16384, 3072, 0, 0, True)
         assert p.kernel == L.KERNEL_ROWS_TMA
+        assert p.stages >= 1 and p.smem_bytes > 0
         # beyond one warp per row the register kernel stays
         st, p = L.ltxk_plan_launch(0, 16384, 5120, 0, 0, True)
         assert p.kernel == L.KERNEL_ROWS_VEC
