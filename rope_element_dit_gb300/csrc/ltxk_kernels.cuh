@@ -87,6 +87,24 @@ __device__ __forceinline__ float sum_of_products(float a, float b, float c, floa
   return diff_of_products(a, b, -c, d);
 }
 
+// ---- two-wide fp32 (Blackwell f32x2: two independently rounded IEEE
+// operations per instruction, bit-identical to the scalar forms) -----------
+
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+// The two bf16 halves of a word as (lo, hi), exactly.
+__device__ __forceinline__ float2 bf2_of(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+
+__device__ __forceinline__ uint32_t pack_f2(float2 v) { return pack_bf2(v.x, v.y); }
+
+// Kahan's a*b - c*d on both lanes.
+__device__ __forceinline__ float2 diff_of_products2(float2 a, float2 b, float2 c, float2 d) {
+  const float2 cd = __fmul2_rn(c, d);
+  const float2 err = __ffma2_rn(neg2(c), d, cd);
+  const float2 dop = __ffma2_rn(a, b, neg2(cd));
+  return __fadd2_rn(dop, err);
+}
+
 // ---- memory helpers ------------------------------------------------------
 
 // Streaming 16-byte load: x is read once, so it should not displace L1 lines.
@@ -153,14 +171,13 @@ __device__ __forceinline__ void group_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ float sumsq8(uint4 v) {
-  float s = 0.f;
+// Sum of squares of 8 bf16 values, as two fp32 partial sums (even, odd).
+__device__ __forceinline__ float2 sumsq8(uint4 v, float2 s) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = bf_lo(u[i]), b = bf_hi(u[i]);
-    s = __fmaf_rn(a, a, s);
-    s = __fmaf_rn(b, b, s);
+    const float2 p = bf2_of(u[i]);
+    s = __ffma2_rn(p, p, s);
   }
   return s;
 }
@@ -255,10 +272,10 @@ struct SlotMap {
 
 template <int VPL>
 __device__ __forceinline__ float slots_sumsq(const uint4 (&v)[VPL]) {
-  float ss = 0.f;
+  float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < VPL; ++k) ss += sumsq8(v[k]);
-  return ss;
+  for (int k = 0; k < VPL; ++k) ss = sumsq8(v[k], ss);
+  return ss.x + ss.y;
 }
 
 __device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
@@ -275,6 +292,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   const bool has_w = a.w != nullptr;
   uint16_t* yr = a.out + row * a.hidden;
   const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
+  const float2 inv2 = make_float2(inv_rms, inv_rms);
   if constexpr (MODE == kPlain) {
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
@@ -283,11 +301,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
       uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __fmul_rn(__fmul_rn(bf_lo(xu[i]), bf_lo(wu[i])), inv_rms);
-        const float hi = __fmul_rn(__fmul_rn(bf_hi(xu[i]), bf_hi(wu[i])), inv_rms);
-        o[i] = pack_bf2(lo, hi);
-      }
+      for (int i = 0; i < 4; ++i)   // (x * w) is exact; one rounding by inv_rms
+        o[i] = pack_f2(__fmul2_rn(__fmul2_rn(bf2_of(xu[i]), bf2_of(wu[i])), inv2));
       st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
     });
     return;
@@ -309,18 +324,25 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
         const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
         const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
-        const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-        const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float2 c[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
+        const float2 s[2] = {make_float2(s4.x, s4.y), make_float2(s4.z, s4.w)};
         const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
         const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // word i holds pair (2i, 2i+1)
-          const float u = __fmul_rn(bf_lo(xu[i]), bf_lo(wu[i]));
-          const float w2 = __fmul_rn(bf_hi(xu[i]), bf_hi(wu[i]));
-          const float ra = __fmul_rn(diff_of_products(u, c[i], w2, s[i]), inv_rms);
-          const float rb = __fmul_rn(sum_of_products(u, s[i], w2, c[i]), inv_rms);
-          o[i] = pack_bf2(ra, rb);
+        for (int h = 0; h < 2; ++h) {
+          // words 2h and 2h+1 hold pairs 2h and 2h+1: lane x of each float2
+          // is the first pair, lane y the second
+          const uint32_t x0 = xu[2 * h], x1 = xu[2 * h + 1];
+          const uint32_t w0 = wu[2 * h], w1 = wu[2 * h + 1];
+          const float2 u = __fmul2_rn(make_float2(bf_lo(x0), bf_lo(x1)),
+                                      make_float2(bf_lo(w0), bf_lo(w1)));   // a * w, exact
+          const float2 q = __fmul2_rn(make_float2(bf_hi(x0), bf_hi(x1)),
+                                      make_float2(bf_hi(w0), bf_hi(w1)));   // b * w, exact
+          const float2 ra = __fmul2_rn(diff_of_products2(u, c[h], q, s[h]), inv2);
+          const float2 rb = __fmul2_rn(diff_of_products2(u, s[h], neg2(q), c[h]), inv2);
+          o[2 * h] = pack_bf2(ra.x, rb.x);
+          o[2 * h + 1] = pack_bf2(ra.y, rb.y);
         }
         st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
       });
@@ -344,26 +366,21 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
         const float4 s0 = same_cols ? s0h : ld_ro16f(st + pair0);
         const float4 s1 = same_cols ? s1h : ld_ro16f(st + pair0 + 4);
-        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const float2 c[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w),
+                             make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
+        const float2 s[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
+                             make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
         const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
         const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
         const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
         const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
         uint32_t ol[4], oh[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // elements 2i, 2i+1 of each half
-          const float ua = __fmul_rn(bf_lo(xl[i]), bf_lo(wlu[i]));
-          const float va = __fmul_rn(bf_lo(xh[i]), bf_lo(whu[i]));
-          const float ub = __fmul_rn(bf_hi(xl[i]), bf_hi(wlu[i]));
-          const float vb = __fmul_rn(bf_hi(xh[i]), bf_hi(whu[i]));
-          const float ca = c[2 * i], sa = s[2 * i], cb = c[2 * i + 1], sb = s[2 * i + 1];
-          const float la = __fmul_rn(diff_of_products(ua, ca, va, sa), inv_rms);
-          const float ha = __fmul_rn(sum_of_products(ua, sa, va, ca), inv_rms);
-          const float lb = __fmul_rn(diff_of_products(ub, cb, vb, sb), inv_rms);
-          const float hb = __fmul_rn(sum_of_products(ub, sb, vb, cb), inv_rms);
-          ol[i] = pack_bf2(la, lb);
-          oh[i] = pack_bf2(ha, hb);
+        for (int i = 0; i < 4; ++i) {   // pairs 2i, 2i+1: (lo word i, hi word i)
+          const float2 u = __fmul2_rn(bf2_of(xl[i]), bf2_of(wlu[i]));   // exact
+          const float2 q = __fmul2_rn(bf2_of(xh[i]), bf2_of(whu[i]));   // exact
+          ol[i] = pack_f2(__fmul2_rn(diff_of_products2(u, c[i], q, s[i]), inv2));
+          oh[i] = pack_f2(__fmul2_rn(diff_of_products2(u, s[i], neg2(q), c[i]), inv2));
         }
         st16(yr + lo_off, make_uint4(ol[0], ol[1], ol[2], ol[3]));
         st16(yr + hi_off, make_uint4(oh[0], oh[1], oh[2], oh[3]));
@@ -389,9 +406,21 @@ struct GroupShape {
 // Register budget per thread of the register kernel: the row's 4*VPL words
 // plus what the epilogue needs (weights, and for RoPE the cos/sin vectors).
 // Capping it lets more warps, hence more bytes of x, be in flight per SM.
+#ifndef LTXK_REG_EXTRA_PLAIN
+#define LTXK_REG_EXTRA_PLAIN 32
+#endif
+#ifndef LTXK_REG_EXTRA_INTERLEAVED
+#define LTXK_REG_EXTRA_INTERLEAVED 48
+#endif
+#ifndef LTXK_REG_EXTRA_SPLIT
+#define LTXK_REG_EXTRA_SPLIT 96
+#endif
 template <int MODE, int VPL>
 struct RegBudget {
-  static constexpr int kRegs = 4 * VPL + (MODE == kPlain ? 32 : (MODE == kInterleaved ? 48 : 96));
+  static constexpr int kRegs =
+      4 * VPL + (MODE == kPlain ? LTXK_REG_EXTRA_PLAIN
+                                : (MODE == kInterleaved ? LTXK_REG_EXTRA_INTERLEAVED
+                                                        : LTXK_REG_EXTRA_SPLIT));
 };
 template <int MODE, int G, int VPL>
 struct VecLaunch {
