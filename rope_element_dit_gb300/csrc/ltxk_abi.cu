@@ -58,13 +58,27 @@ int bucket_vpl(int need) {
 
 int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC_BLOCK; }
 
-// 1: grids of at most (resident CTAs) that stride over the rows; 0: one CTA
-// per row group and let the hardware schedule them.
+// Grid shape.  1: at most the resident CTAs, striding over the rows
+// (persistent); 0: one CTA per row group, scheduled by the hardware.
+// Measured on GB300: plain RMSNorm is faster with one CTA per row group
+// (no rounding of the last pass over the rows), the fused kernels with
+// persistent CTAs (their per-CTA set-up is amortised).
 #ifndef LTXK_PERSISTENT
 #define LTXK_PERSISTENT 0
 #endif
+// Most vector slots per lane for the fused kernels before a row is split
+// over more warps.  The rotation makes these kernels issue-heavy, so more
+// warps with fewer registers each hide memory latency better; measured on
+// GB300 for [2 x 4096 x 32 x 128] interleaved and [6144 x 32 x 64]
+// split-half.
+#ifndef LTXK_ROPE_MAX_SLOTS_INTERLEAVED
+#define LTXK_ROPE_MAX_SLOTS_INTERLEAVED 4
+#endif
+#ifndef LTXK_ROPE_MAX_SLOTS_SPLIT
+#define LTXK_ROPE_MAX_SLOTS_SPLIT 8
+#endif
 #ifndef LTXK_PERSISTENT_ROPE
-#define LTXK_PERSISTENT_ROPE 0
+#define LTXK_PERSISTENT_ROPE 1
 #endif
 
 int kernel_mode(int op, int mode) {
@@ -171,8 +185,12 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
     // split-half slots are (lo, hi) pairs: nv/2 units of two slots each
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
+    const int max_slots = km == ltxk::kPlain         ? kMaxVplSlots
+                          : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
+                                                     : LTXK_ROPE_MAX_SLOTS_SPLIT;
     for (int g : kGroupChoices) {
       const int64_t need = (units + 32 * g - 1) / (32 * g) * slots_per_unit;
+      if (need > max_slots && g < 32) continue;
       if (need > kMaxVplSlots) continue;
       p->group_warps = g;
       p->vec_per_lane = bucket_vpl(static_cast<int>(need));

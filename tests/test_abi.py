@@ -117,13 +117,13 @@ def test_rope_validation(L):
     (0, 7, 4, 0, 0, True, 2, 8, 0),          # hidden % 8 != 0
     (0, 7, 3072, 0, 0, False, 2, 8, 0),      # unaligned pointers
     # fused
-    (1, 8192, 4096, 128, 0, True, 1, 1, 16),
+    (1, 8192, 4096, 128, 0, True, 1, 4, 4),  # fused rows split over 4 warps
     (1, 6144, 2048, 64, 1, True, 1, 1, 8),
     (1, 9, 48, 24, 0, True, 1, 1, 4),
     (1, 9, 48, 24, 1, True, 2, 8, 0),        # split needs head_dim % 16
     (1, 9, 40, 20, 0, True, 2, 8, 0),        # interleaved needs head_dim % 8
     (1, 9, 4096, 128, 1, False, 2, 8, 0),
-    (1, 9, 10240, 128, 1, True, 1, 4, 12),
+    (1, 9, 10240, 128, 1, True, 1, 8, 8),
 ])
 def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
     st, p = L.ltxk_plan_launch(op, rows, hidden, D, mode, vec)
