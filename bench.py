@@ -82,6 +82,30 @@ def dist_env():
     return world, rank, local
 
 
+def shard_rows(rows, world, rank):
+    """Rows [r0, r1) of a batch that rank `rank` of `world` normalises: rows
+    are independent, so a contiguous split needs no exchange."""
+    base, extra = divmod(rows, world)
+    r0 = rank * base + min(rank, extra)
+    return r0, r0 + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(seconds, world, device=None):
+    """The slowest rank's time (the job's time) via an all-reduce MAX."""
+    if world == 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbps(bytes_per_rank_step, steps, world, job_seconds):
+    """Whole-job throughput: bytes all ranks moved / the job's time."""
+    return world * bytes_per_rank_step * steps / job_seconds / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -324,11 +348,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                      "tma": L.PATH_TMA}[args.path])
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    flush_r = torch.zeros(2 * l2, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=dev)
 
     def flush_l2(i):
-        # write 2x L2 (evicts everything), then read another 2x L2 so that the
-        # written lines are written back here and L2 is left clean and cold
+        # write 2x L2 (evicts everything), then read another 2x L2 (a float32
+        # sum reads it in place) so that the written lines are written back
+        # here and L2 is left clean and cold
         flush_w.fill_(i & 0xFF)
         flush_r.sum()
 
@@ -390,12 +415,8 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     per_launch = np.array([[ev[i][j][0].elapsed_time(ev[i][j][1]) for j in range(n)]
                            for i in range(args.steps)], dtype=np.float64)   # ms
     step_ms = per_launch.sum(axis=1)
-    total_s = step_ms.sum() / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = world * bytes_per_step * args.steps / total_s / 1e9
+    total_s = max_over_ranks(step_ms.sum() / 1e3, world, dev)
+    value = aggregate_gbps(bytes_per_step, args.steps, world, total_s)
 
     # dominant kernel: the kernel instance with the largest share of time
     by_kernel = {}
@@ -447,12 +468,8 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             torch.cuda.synchronize()
             if i >= 3:
                 e_ms.append(e0.elapsed_time(e1))
-        e2e_s = sum(e_ms) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": round(world * bytes_per_step * len(e_ms) / e2e_s / 1e9, 2),
+        e2e_s = max_over_ranks(sum(e_ms) / 1e3, world, dev)
+        e2e = {"value": round(aggregate_gbps(bytes_per_step, len(e_ms), world, e2e_s), 2),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_s / len(e_ms) * 1e3, 4),
                "note": "pinned host x -> HBM, ltxk call, HBM y -> pinned host, per "
