@@ -159,6 +159,36 @@ LTXK_API int ltxk_diag_missing_copy(void* out, const void* x, int64_t rows,
                                     int64_t hidden, uint64_t wait_limit_ns,
                                     ltxk_stream_t stream);
 
+/*
+ * ltxk_rms_norm_noalloc -- the same RMSNorm as ltxk_rms_norm, for callers
+ * that cannot allocate device memory: for example an engine whose device
+ * memory all comes from its own pre-sized pool, or a latency-critical loop
+ * where an allocation's implicit device synchronisation is not acceptable.
+ * The pages have no counterpart to it.
+ *
+ * It runs the TMA-ring kernel, whose only device memory beyond x, w and out
+ * is one fault word for its bounded waits.  That word lives in a file-scope
+ * static device array of LTXK_NOALLOC_SCRATCH_WORDS 32-bit words (256 bytes)
+ * that every GPU loading the library holds until the process exits; the call
+ * allocates nothing and calls no cudaMalloc or cudaFree.
+ *   out, x, w : as for ltxk_rms_norm, but 16-byte aligned (w may be NULL).
+ *   hidden    : a multiple of 8 and at most LTXK_NOALLOC_MAX_HIDDEN (one warp
+ *               per row); larger or ragged rows return LTXK_ERR_SHAPE.
+ * The first call on a device resolves the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Each call clears the fault word on `stream`
+ * before its kernel.  A wait that runs out sets the word and leaves that
+ * warp's remaining rows unwritten; no entry point reads this word back
+ * (ltxk_fault_status reads the other entry points' word).  All calls share
+ * the array, which keeps the last call's contents, so calls that overlap on
+ * the GPU (other streams, other threads) race on it.
+ */
+#define LTXK_NOALLOC_SCRATCH_WORDS 64
+#define LTXK_NOALLOC_MAX_HIDDEN 4096
+LTXK_API int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w,
+                                   int64_t rows, int64_t hidden, float eps,
+                                   ltxk_stream_t stream);
+
 /* Human-readable name of an ltxk_status (static string, never NULL). */
 LTXK_API const char* ltxk_status_string(int status);
 

@@ -43,6 +43,7 @@ KERNEL_ROWS_TMA = 3
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
+           "ltxk_rms_norm_noalloc",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -77,6 +78,8 @@ def _load():
     lib.ltxk_rms_norm_rope_seq.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, P]
     for f in ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq"):
         getattr(lib, f).restype = I32
+    lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
+    lib.ltxk_rms_norm_noalloc.restype = I32
     lib.ltxk_fault_status.argtypes = []
     lib.ltxk_fault_status.restype = I32
     lib.ltxk_set_path.argtypes = [I32]
@@ -111,6 +114,10 @@ def ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads, head_dim, mode,
                            eps, seq_len, stream) -> int:
     return _lib.ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads,
                                        head_dim, mode, eps, seq_len, stream)
+
+
+def ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream) -> int:
+    return _lib.ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream)
 
 
 def ltxk_fault_status() -> int:

@@ -314,6 +314,10 @@ int norm_checks(void* out, const void* x, const void* w, int64_t rows, int64_t h
 
 }  // namespace
 
+namespace ltxk {
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+}  // namespace ltxk
+
 extern "C" {
 
 int ltxk_rms_norm(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,

@@ -15,6 +15,9 @@ const void* rows_tma_plain_ptr(int vec_per_lane);
 const void* rows_tma_interleaved_ptr(int vec_per_lane);
 const void* rows_tma_split_ptr(int vec_per_lane);
 
+// Record a cudaError_t for ltxk_last_cuda_error() (calling thread).
+void record_cuda_error(int e);
+
 // Element-wise kernel for a mode (0 plain, 1 interleaved, 2 split-half).
 const void* rows_elem_kernel_ptr(int mode);
 
