@@ -71,6 +71,16 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 // warps with fewer registers each hide memory latency better; measured on
 // GB300 for [2 x 4096 x 32 x 128] interleaved and [6144 x 32 x 64]
 // split-half.
+// Plain RMSNorm: 0 = fewest warps per row; 1 = four warps when a row is
+// exactly 3 or 4 vectors per lane; 2 = any g >= 4 with such an exact fit
+// (measured on GB300: copy speed or better for hidden 3072, 4096, 6144 and
+// 8192, at 16384-65536 rows).
+#ifndef LTXK_PLAIN_SPLIT_RULE
+#define LTXK_PLAIN_SPLIT_RULE 2
+#endif
+#ifndef LTXK_PLAIN_MAX_SLOTS
+#define LTXK_PLAIN_MAX_SLOTS 16
+#endif
 #ifndef LTXK_ROPE_MAX_SLOTS_INTERLEAVED
 #define LTXK_ROPE_MAX_SLOTS_INTERLEAVED 4
 #endif
@@ -180,12 +190,31 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
   bool vec = vector_ok && hidden % 8 == 0;
   if (km == ltxk::kInterleaved) vec = vec && head_dim % 8 == 0;
   if (km == ltxk::kSplitHalf) vec = vec && head_dim % 16 == 0;
+  if (vec && km == ltxk::kPlain && LTXK_PLAIN_SPLIT_RULE > 0) {
+    // Split the row over g >= 4 warps when it divides into exactly 3 or 4
+    // vectors per lane: a light per-warp share (about 45 registers) lets far
+    // more warps be resident.
+    const int64_t nv = hidden / 8;
+    for (int g : kGroupChoices) {
+      if (g < 4 || (LTXK_PLAIN_SPLIT_RULE == 1 && g != 4)) continue;
+      if (nv % (32 * g) != 0) continue;
+      const int64_t s = nv / (32 * g);
+      if (s == 3 || s == 4) {
+        p->kernel = LTXK_KERNEL_ROWS_VEC;
+        p->group_warps = g;
+        p->vec_per_lane = 4;
+        p->block_threads = block_for_group(g);
+        p->rows_per_cta = p->block_threads / (32 * g);
+        return LTXK_OK;
+      }
+    }
+  }
   if (vec) {
     const int64_t nv = hidden / 8;
     // split-half slots are (lo, hi) pairs: nv/2 units of two slots each
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
-    const int max_slots = km == ltxk::kPlain         ? kMaxVplSlots
+    const int max_slots = km == ltxk::kPlain         ? LTXK_PLAIN_MAX_SLOTS
                           : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
                                                      : LTXK_ROPE_MAX_SLOTS_SPLIT;
     for (int g : kGroupChoices) {

@@ -105,10 +105,15 @@ def test_rope_validation(L):
 
 
 @pytest.mark.parametrize("op,rows,hidden,D,mode,vec,kernel,G,vpl", [
-    # plain RMSNorm: one warp per row up to 4096, then warp groups
+    # plain RMSNorm: rows that split exactly into 3-4 vectors per lane over
+    # g >= 4 warps take that split; others the fewest warps per row
     (0, 16384, 2048, 0, 0, True, 1, 1, 8),
-    (0, 16384, 3072, 0, 0, True, 1, 1, 12),
-    (0, 65536, 4096, 0, 0, True, 1, 1, 16),
+    (0, 16384, 3072, 0, 0, True, 1, 4, 4),
+    (0, 65536, 4096, 0, 0, True, 1, 4, 4),
+    (0, 16384, 6144, 0, 0, True, 1, 8, 4),
+    (0, 16384, 8192, 0, 0, True, 1, 8, 4),
+    (0, 4, 16384, 0, 0, True, 1, 16, 4),
+    (0, 4, 32768, 0, 0, True, 1, 32, 4),
     (0, 262143, 2560, 0, 0, True, 1, 1, 12),
     (0, 65536, 5120, 0, 0, True, 1, 2, 12),
     (0, 7, 131072, 0, 0, True, 1, 32, 16),
@@ -148,10 +153,10 @@ def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
 def test_plan_follows_path_setting(L):
     try:
         assert L.ltxk_set_path(L.PATH_REGISTERS) == L.PATH_AUTO
-        st, p = L.ltxk_plan_launch(0, 16384, 3072, 0, 0, True)
+        st, p = L.ltxk_plan_launch(0, 16384, 2560, 0, 0, True)
         assert (p.kernel, p.group_warps, p.vec_per_lane) == (L.KERNEL_ROWS_VEC, 1, 12)
         assert L.ltxk_set_path(L.PATH_TMA) == L.PATH_REGISTERS
-        st, p = L.ltxk_plan_launch(0, 16384, 3072, 0, 0, True)
+        st, p = L.ltxk_plan_launch(0, 16384, 2560, 0, 0, True)
         assert p.kernel == L.KERNEL_ROWS_TMA
         assert p.stages >= 1 and p.smem_bytes > 0
         # beyond one warp per row the register kernel stays

@@ -166,7 +166,8 @@ def test_workload_full_size(case, path):
 
 NORM_SHAPES = [(1, 4), (3, 8), (37, 24), (9, 40), (1000, 264), (17, 2056),
                (1001, 3072), (33, 5120), (19, 8200), (3, 131072), (2, 131080),
-               (2049, 2048), (5, 7), (4, 1)]
+               (2049, 2048), (5, 7), (4, 1), (9, 4096), (7, 6144), (5, 8192),
+               (3, 12288), (3, 16384), (2, 24576), (2, 32768), (11, 2560)]
 
 
 @pytest.mark.parametrize("rows,hidden", NORM_SHAPES)
