@@ -70,6 +70,9 @@ def _load():
                 P, P, P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_float,
                 I64, I64, P]
             lib.oracle_rms_norm_rope.restype = ctypes.c_int
+            lib.oracle_rms_norm_adaln.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                                  ctypes.c_float, P]
+            lib.oracle_rms_norm_adaln.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -172,6 +175,45 @@ def rms_norm_rope(x, w, cos, sin, heads, head_dim, mode, eps, *,
             r0, None if ye is None else _ptr(ye[r0:r1]))
         if rc != 0:
             raise RuntimeError(f"oracle_rms_norm_rope failed ({rc})")
+
+    _run_blocks(run, rows, threads)
+    y = y.reshape(x.shape)
+    return (y, ye.reshape(x.shape)) if exact else y
+
+
+def rms_norm_adaln(x, w, scale, shift, eps, *, rows_per_cond=None,
+                   threads: int = 1, exact: bool = False):
+    """Oracle AdaLN-modulated RMSNorm: norm(x) * w * (1 + scale) + shift.
+
+    ``x``: uint16 [rows, H]; ``scale``/``shift``: uint16 [n_cond, H]; row r
+    uses conditioning row ``r // rows_per_cond`` (default: rows / n_cond).
+    """
+    x = _u16(x, "x")
+    H = x.shape[-1]
+    rows = x.size // H
+    x2 = x.reshape(rows, H)
+    w = None if w is None else _u16(w, "w")
+    scale = _u16(scale, "scale").reshape(-1, H)
+    shift = _u16(shift, "shift").reshape(-1, H)
+    if scale.shape != shift.shape:
+        raise ValueError("scale and shift must have the same shape")
+    n_cond = scale.shape[0]
+    if rows_per_cond is None:
+        rows_per_cond = max(1, -(-rows // n_cond))
+    if rows and (rows - 1) // rows_per_cond >= n_cond:
+        raise ValueError("not enough conditioning rows")
+    y = np.empty_like(x2)
+    ye = np.empty(x2.shape, np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        rc = lib.oracle_rms_norm_adaln(
+            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(scale), _ptr(shift),
+            r1 - r0, H, rows_per_cond, r0, ctypes.c_float(eps),
+            None if ye is None else _ptr(ye[r0:r1]))
+        if rc != 0:
+            raise RuntimeError(f"oracle_rms_norm_adaln failed ({rc})")
 
     _run_blocks(run, rows, threads)
     y = y.reshape(x.shape)

@@ -32,6 +32,11 @@
  * no blocking, fusion or reordering.  The build compiles this file with
  * -ffp-contract=off so that no multiply-add is fused on any host.
  *
+ *   - same page, "Kernel-Specific Guidelines / AdaLN": the DiT conditioning
+ *     norm(x) * weight * (1 + scale) + shift, with norm the RMSNorm above;
+ *     scale and shift are one hidden-sized vector per conditioning row (one
+ *     per batch item), shared by the rows_per_cond consecutive rows of x.
+ *
  * Every exported function is re-entrant (no global state), so callers may run
  * disjoint row ranges on several threads at once.
  *
@@ -183,5 +188,34 @@ int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
     }
     free(n);
     free(o);
+    return 0;
+}
+
+/* AdaLN-modulated RMSNorm:
+ *   y[r, j] = bf16( n[r, j] * (1 + scale[c, j]) + shift[c, j] ),
+ *   n = the RMSNorm above (with w, or ones when w == NULL),
+ *   c = r / rows_per_cond (x is [n_cond, rows_per_cond, H]).
+ * scale, shift: bfloat16 [n_cond, H].  first_row is the global index of the
+ * first row passed, so that row blocks keep their conditioning row.
+ * Returns 0; -1 on allocation failure; -2 on an invalid argument. */
+int oracle_rms_norm_adaln(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                          const uint16_t* scale, const uint16_t* shift,
+                          int64_t rows, int64_t H, int64_t rows_per_cond,
+                          int64_t first_row, float eps, double* y_exact) {
+    if (H <= 0 || rows_per_cond <= 0 || first_row < 0) return -2;
+    double* n = (double*)malloc((size_t)H * sizeof(double));
+    if (!n) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        normalise_row(x + r * H, w, H, eps, n);
+        const int64_t c = (first_row + r) / rows_per_cond;
+        for (int64_t j = 0; j < H; ++j) {
+            const double sc = widen_bf16(scale[c * H + j]);
+            const double sh = widen_bf16(shift[c * H + j]);
+            const double v = n[j] * (1.0 + sc) + sh;
+            if (y_exact) y_exact[r * H + j] = v;
+            y[r * H + j] = round_to_bf16(v);
+        }
+    }
+    free(n);
     return 0;
 }

@@ -342,3 +342,86 @@ def test_rope_rejects_bad_arguments(oracle_mod):
     c, s = _const_tables(1, 4, 1.0, 0.0)
     with pytest.raises(RuntimeError):
         oracle_mod.rms_norm_rope(x, None, c, s, 1, 8, 2, 1e-6)
+
+
+# ------------------------------------------------------------ AdaLN pins --
+
+ADALN_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "adaln_hand_cases_h4.txt")
+
+
+def _parse_adaln():
+    cases = []
+    for line in open(ADALN_GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, eps, xs, ws, sc, sh, rpc, exact, bits = [s.strip() for s in line.split(" | ")]
+        rows = lambda t: np.array([list(map(float, r.split())) for r in t.split(";")])
+        x = rows(xs)
+        cases.append(dict(
+            name=name, eps=float(eps), x=x,
+            w=None if ws == "-" else np.array(list(map(float, ws.split()))),
+            scale=rows(sc), shift=rows(sh), rows_per_cond=int(rpc),
+            exact=np.array(list(map(float, exact.split()))).reshape(x.shape),
+            bits=np.array([int(b, 16) for b in bits.split()], np.uint16).reshape(x.shape)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _parse_adaln(), ids=lambda c: c["name"])
+def test_adaln_hand_cases(oracle_mod, case):
+    y, ye = oracle_mod.rms_norm_adaln(
+        bits_of(case["x"]), None if case["w"] is None else bits_of(case["w"]),
+        bits_of(case["scale"]), bits_of(case["shift"]), case["eps"],
+        rows_per_cond=case["rows_per_cond"], exact=True)
+    assert np.array_equal(y, case["bits"]), [hex(v) for v in y.ravel()]
+    np.testing.assert_allclose(ye, case["exact"], rtol=4e-16, atol=1e-300)
+
+
+def _cond(seed, n, H, lo, hi):
+    return synth.uniform_bf16(seed, 3, n * H, lo, hi).reshape(n, H)
+
+
+def test_adaln_zero_modulation_is_rms_norm(oracle_mod):
+    x = _rows(41, 12, 96)
+    w = synth.normal_bf16(41, 2, 96, 1.0, 0.1)
+    zero = np.zeros((3, 96), np.uint16)
+    y, ye = oracle_mod.rms_norm_adaln(x, w, zero, zero, 1e-6, rows_per_cond=4, exact=True)
+    yn, yne = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    assert np.array_equal(y, yn) and np.array_equal(ye, yne)
+
+
+def test_adaln_scale_minus_one_gives_shift(oracle_mod):
+    x = _rows(42, 6, 40)
+    shift = _cond(42, 2, 40, -3, 3)
+    minus1 = bits_of(-np.ones((2, 40)))
+    y = oracle_mod.rms_norm_adaln(x, None, minus1, shift, 1e-6, rows_per_cond=3)
+    assert np.array_equal(y, np.repeat(shift, 3, axis=0))
+
+
+def test_adaln_is_affine_in_scale_and_shift(oracle_mod):
+    x = _rows(43, 8, 64)
+    w = synth.normal_bf16(43, 2, 64, 1.0, 0.1)
+    s = _cond(43, 2, 64, -0.5, 0.5)
+    t = _cond(44, 2, 64, -2, 2)
+    zero = np.zeros_like(s)
+    _, n = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    _, ys = oracle_mod.rms_norm_adaln(x, w, s, zero, 1e-6, rows_per_cond=4, exact=True)
+    _, yst = oracle_mod.rms_norm_adaln(x, w, s, t, 1e-6, rows_per_cond=4, exact=True)
+    sw = np.repeat(oracle_mod.widen_bf16(s), 4, axis=0)
+    tw = np.repeat(oracle_mod.widen_bf16(t), 4, axis=0)
+    np.testing.assert_allclose(ys, n * (1 + sw), rtol=1e-15, atol=1e-300)
+    np.testing.assert_allclose(yst - ys, tw, rtol=0, atol=1e-14)
+
+
+def test_adaln_conditioning_rows(oracle_mod):
+    # rows_per_cond consecutive rows share one conditioning row; a ragged last
+    # group uses the next conditioning row
+    x = _rows(45, 7, 32)
+    s = _cond(45, 3, 32, -1, 1)
+    t = _cond(46, 3, 32, -1, 1)
+    y = oracle_mod.rms_norm_adaln(x, None, s, t, 1e-6, rows_per_cond=3)
+    parts = [oracle_mod.rms_norm_adaln(x[c * 3:(c + 1) * 3], None, s[c:c + 1], t[c:c + 1],
+                                       1e-6, rows_per_cond=3) for c in range(3)]
+    assert np.array_equal(y, np.concatenate(parts))
+    assert np.array_equal(oracle_mod.rms_norm_adaln(x, None, s, t, 1e-6, rows_per_cond=3,
+                                                    threads=3), y)

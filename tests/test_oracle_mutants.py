@@ -37,6 +37,11 @@ MUTANTS = [
      ""),
     ("subnormal_spacing", "if (e < -125) e = -125;", "if (e < -126) e = -126;"),
     ("precision_9_bits", "ldexp(1.0, e - 8)", "ldexp(1.0, e - 9)"),
+    ("adaln_scale_not_plus_one", "n[j] * (1.0 + sc) + sh", "n[j] * sc + sh"),
+    ("adaln_shift_subtracted", "n[j] * (1.0 + sc) + sh", "n[j] * (1.0 + sc) - sh"),
+    ("adaln_scale_shift_swapped", "n[j] * (1.0 + sc) + sh", "n[j] * (1.0 + sh) + sc"),
+    ("adaln_cond_ignores_first_row", "(first_row + r) / rows_per_cond", "r / rows_per_cond"),
+    ("adaln_cond_modulo", "(first_row + r) / rows_per_cond", "(first_row + r) % rows_per_cond"),
 ]
 
 
@@ -63,6 +68,14 @@ def _pin_calls():
     ]
     for name, case in hand.items():
         calls.append(("hand_" + name, pins.test_hand_cases, (case,)))
+    for case in pins._parse_adaln():
+        calls.append(("adaln_hand_" + case["name"], pins.test_adaln_hand_cases, (case,)))
+    calls += [
+        ("adaln_zero", pins.test_adaln_zero_modulation_is_rms_norm, ()),
+        ("adaln_minus1", pins.test_adaln_scale_minus_one_gives_shift, ()),
+        ("adaln_affine", pins.test_adaln_is_affine_in_scale_and_shift, ()),
+        ("adaln_cond", pins.test_adaln_conditioning_rows, ()),
+    ]
     return calls
 
 
