@@ -52,6 +52,8 @@ WORKLOAD_TITLES = {
                   "positions 8x24x32, fp32 cos/sin [6144, 32], seed 6",
     "stress": "bf16 RMSNorm [4x16384x4096], [262143x2560], [65536x5120], "
               "U(-4,4), eps 1e-5, seeds 7-9",
+    "adaln": "AdaLN-modulated RMSNorm norm(x)*(1+scale)+shift, x [2, 6144, 2048], "
+             "no weight, scale/shift [2, 2048] ~ N(0, 0.5), seed 10",
 }
 
 
@@ -222,14 +224,18 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         r = max(1, math.ceil(c.rows * row_frac))
         x = inp["x"][:r]
         t0 = time.perf_counter()
-        if c.mode is None:
+        if c.kind == "adaln":
+            oracle.rms_norm_adaln(x, inp["w"], inp["scale"], inp["shift"], c.eps,
+                                  rows_per_cond=c.rows_per_cond, threads=threads)
+        elif c.mode is None:
             oracle.rms_norm(x, inp["w"], c.eps, threads=threads)
         else:
             oracle.rms_norm_rope(x, inp["w"], inp["cos"], inp["sin"], c.heads, c.head_dim,
                                  c.mode, c.eps, table_rows=c.seq_len, threads=threads)
         t += time.perf_counter() - t0
-        b += 4 * r * c.hidden + 2 * c.hidden + (
-            8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0)
+        b += 4 * r * c.hidden + (2 * c.hidden if inp["w"] is not None else 0) + (
+            8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0) + (
+            4 * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0)
     return t, b
 
 
@@ -292,8 +298,10 @@ def run_reference(args, cases, inputs, world, rank):
 # ------------------------------------------------------------- GPU timing --
 
 def kernel_name(plan, mode):
+    """Kernel instance name as ncu prints it; mode None = plain, 0/1 = RoPE
+    pairing, 3 = AdaLN."""
     import rope_element_dit_gb300 as L
-    km = 0 if mode is None else (1 if mode == 0 else 2)
+    km = 0 if mode is None else {0: 1, 1: 2, 3: 3}[mode]
     if plan.kernel == L.KERNEL_ROWS_VEC:
         return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
     if plan.kernel == L.KERNEL_ROWS_TMA:
@@ -318,8 +326,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     dev_bufs = []
     for c, inp in zip(cases, inputs):
         d = {"x": torch.from_numpy(inp["x"].view(np.int16)).to(dev),
-             "w": torch.from_numpy(inp["w"].view(np.int16)).to(dev),
+             "w": (None if inp["w"] is None
+                   else torch.from_numpy(inp["w"].view(np.int16)).to(dev)),
              "y": torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)}
+        if c.kind == "adaln":
+            d["scale"] = torch.from_numpy(inp["scale"].view(np.int16)).to(dev)
+            d["shift"] = torch.from_numpy(inp["shift"].view(np.int16)).to(dev)
         if c.mode is not None:
             d["cos"] = torch.from_numpy(inp["cos"]).to(dev)
             d["sin"] = torch.from_numpy(inp["sin"]).to(dev)
@@ -328,11 +340,16 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     def call_args(i, x=None):
         c, d = cases[i], dev_bufs[i]
         x = d["x"] if x is None else x
+        wp = None if d["w"] is None else d["w"].data_ptr()
+        if c.kind == "adaln":
+            return L.ltxk_rms_norm_adaln, (
+                d["y"].data_ptr(), x.data_ptr(), wp, d["scale"].data_ptr(),
+                d["shift"].data_ptr(), c.rows, c.hidden, c.rows_per_cond, c.eps, sptr)
         if c.mode is None:
-            return L.ltxk_rms_norm, (d["y"].data_ptr(), x.data_ptr(), d["w"].data_ptr(),
+            return L.ltxk_rms_norm, (d["y"].data_ptr(), x.data_ptr(), wp,
                                      c.rows, c.hidden, c.eps, sptr)
         return L.ltxk_rms_norm_rope_seq, (
-            d["y"].data_ptr(), x.data_ptr(), d["w"].data_ptr(), d["cos"].data_ptr(),
+            d["y"].data_ptr(), x.data_ptr(), wp, d["cos"].data_ptr(),
             d["sin"].data_ptr(), c.rows, c.heads, c.head_dim, c.mode, c.eps, c.seq_len, sptr)
 
     # prebuilt calls keep the host side of a launch to one ctypes call
@@ -362,9 +379,10 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     bytes_per_step = sum(bytes_per_launch)
     plans = []
     for c in cases:
-        op = L.OP_RMS_NORM if c.mode is None else L.OP_RMS_NORM_ROPE
+        op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
+              "adaln": L.OP_RMS_NORM_ADALN}[c.kind]
         st, p = L.ltxk_plan_launch(op, c.rows, c.hidden, c.head_dim, c.mode or 0, True)
-        plans.append(kernel_name(p, c.mode))
+        plans.append(kernel_name(p, 3 if c.kind == "adaln" else c.mode))
 
     for i in range(args.warmup):
         flush_l2(i)

@@ -123,6 +123,26 @@ LTXK_API int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w,
                            int64_t seq_len, ltxk_stream_t stream);
 
 /*
+ * ltxk_rms_norm_adaln -- AdaLN-modulated RMSNorm, the DiT conditioning of
+ * the "cuda-kernels" page ("Kernel-Specific Guidelines / AdaLN"):
+ *     y[r, j] = bf16_rne( n[r, j] * (1 + scale[c, j]) + shift[c, j] ),
+ *     n = x * w / sqrt(mean(x^2) + eps) (the RMSNorm above, fp32),
+ *     c = r / rows_per_cond.
+ *   out, x        [rows, hidden] bf16.   w [hidden] bf16 or NULL (ones: the
+ *                 pages' weightless LTX-Video block norm).
+ *   scale, shift  [ceil(rows / rows_per_cond), hidden] bf16: one vector per
+ *                 conditioning row (per batch item for x [B, S, hidden] with
+ *                 rows_per_cond = S), shared by rows_per_cond rows.
+ *   rows_per_cond >= 1.
+ * out may equal x; it must not overlap w, scale or shift.
+ */
+LTXK_API int ltxk_rms_norm_adaln(void* out, const void* x, const void* w,
+                                 const void* scale, const void* shift,
+                                 int64_t rows, int64_t hidden,
+                                 int64_t rows_per_cond, float eps,
+                                 ltxk_stream_t stream);
+
+/*
  * ltxk_fault_status -- did any kernel on the current device give up waiting
  * since the last call?  The TMA-ring kernel bounds each wait for a bulk copy
  * of a row (about two seconds); a wait that runs out sets a device fault
@@ -206,7 +226,7 @@ enum {
                                    copies through a shared-memory ring */
 };
 
-enum { LTXK_OP_RMS_NORM = 0, LTXK_OP_RMS_NORM_ROPE = 1 };
+enum { LTXK_OP_RMS_NORM = 0, LTXK_OP_RMS_NORM_ROPE = 1, LTXK_OP_RMS_NORM_ADALN = 2 };
 
 typedef struct {
     int kernel;          /* LTXK_KERNEL_* */

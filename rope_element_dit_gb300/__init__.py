@@ -34,6 +34,7 @@ ROPE_SPLIT_HALF = 1
 
 OP_RMS_NORM = 0
 OP_RMS_NORM_ROPE = 1
+OP_RMS_NORM_ADALN = 2
 
 KERNEL_NONE = 0
 KERNEL_ROWS_VEC = 1
@@ -42,6 +43,7 @@ KERNEL_ROWS_TMA = 3
 
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
+           "ltxk_rms_norm_adaln",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_rms_norm_noalloc",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
@@ -78,6 +80,8 @@ def _load():
     lib.ltxk_rms_norm_rope_seq.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, P]
     for f in ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq"):
         getattr(lib, f).restype = I32
+    lib.ltxk_rms_norm_adaln.argtypes = [P, P, P, P, P, I64, I64, I64, F32, P]
+    lib.ltxk_rms_norm_adaln.restype = I32
     lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
     lib.ltxk_rms_norm_noalloc.restype = I32
     lib.ltxk_fault_status.argtypes = []
@@ -114,6 +118,12 @@ def ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads, head_dim, mode,
                            eps, seq_len, stream) -> int:
     return _lib.ltxk_rms_norm_rope_seq(out, x, w, cos, sin, rows, heads,
                                        head_dim, mode, eps, seq_len, stream)
+
+
+def ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond, eps,
+                        stream) -> int:
+    return _lib.ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond,
+                                    eps, stream)
 
 
 def ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream) -> int:
@@ -218,4 +228,30 @@ def rms_norm_rope(x, weight, cos, sin, heads: int, head_dim: int,
     else:
         st = ltxk_rms_norm_rope_seq(*args, table_rows, _stream_handle(x, stream))
         _check(st, "ltxk_rms_norm_rope_seq")
+    return out
+
+
+def rms_norm_adaln(x, weight, scale, shift, eps: float = 1e-6, rows_per_cond=None,
+                   out=None, stream=None):
+    """norm(x) * weight * (1 + scale) + shift over the last axis (bf16).
+
+    ``scale``/``shift`` are ``[n_cond, hidden]``; row r of x uses conditioning
+    row ``r // rows_per_cond`` (default: rows / n_cond, e.g. the sequence
+    length for x ``[B, S, hidden]`` and conditioning ``[B, hidden]``).
+    """
+    import torch
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    n_cond = scale.numel() // hidden if hidden else 0
+    if rows_per_cond is None:
+        rows_per_cond = max(1, -(-rows // max(1, n_cond)))
+    if out is None:
+        out = torch.empty_like(x)
+    st = ltxk_rms_norm_adaln(_dev_ptr(out, "out", torch.bfloat16),
+                             _dev_ptr(x, "x", torch.bfloat16),
+                             _dev_ptr(weight, "weight", torch.bfloat16),
+                             _dev_ptr(scale, "scale", torch.bfloat16),
+                             _dev_ptr(shift, "shift", torch.bfloat16),
+                             rows, hidden, rows_per_cond, eps, _stream_handle(x, stream))
+    _check(st, "ltxk_rms_norm_adaln")
     return out

@@ -93,6 +93,7 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 
 int kernel_mode(int op, int mode) {
   if (op == LTXK_OP_RMS_NORM) return ltxk::kPlain;
+  if (op == LTXK_OP_RMS_NORM_ADALN) return ltxk::kAdaLN;
   return mode == LTXK_ROPE_INTERLEAVED ? ltxk::kInterleaved : ltxk::kSplitHalf;
 }
 
@@ -174,7 +175,7 @@ int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
   if (op == LTXK_OP_RMS_NORM_ROPE) {
     if (head_dim < 2 || head_dim % 2 != 0 || hidden % head_dim != 0) return LTXK_ERR_SHAPE;
     if (mode != LTXK_ROPE_INTERLEAVED && mode != LTXK_ROPE_SPLIT_HALF) return LTXK_ERR_MODE;
-  } else if (op != LTXK_OP_RMS_NORM) {
+  } else if (op != LTXK_OP_RMS_NORM && op != LTXK_OP_RMS_NORM_ADALN) {
     return LTXK_ERR_MODE;
   }
   return LTXK_OK;
@@ -190,7 +191,8 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
   bool vec = vector_ok && hidden % 8 == 0;
   if (km == ltxk::kInterleaved) vec = vec && head_dim % 8 == 0;
   if (km == ltxk::kSplitHalf) vec = vec && head_dim % 16 == 0;
-  if (vec && km == ltxk::kPlain && LTXK_PLAIN_SPLIT_RULE > 0) {
+  const bool row_only = km == ltxk::kPlain || km == ltxk::kAdaLN;   // no rotation
+  if (vec && row_only && LTXK_PLAIN_SPLIT_RULE > 0) {
     // Split the row over g >= 4 warps when it divides into exactly 3 or 4
     // vectors per lane: a light per-warp share (about 45 registers) lets far
     // more warps be resident.
@@ -214,7 +216,7 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
     // split-half slots are (lo, hi) pairs: nv/2 units of two slots each
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
-    const int max_slots = km == ltxk::kPlain         ? LTXK_PLAIN_MAX_SLOTS
+    const int max_slots = row_only                   ? LTXK_PLAIN_MAX_SLOTS
                           : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
                                                      : LTXK_ROPE_MAX_SLOTS_SPLIT;
     for (int g : kGroupChoices) {
@@ -225,7 +227,7 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
       p->vec_per_lane = bucket_vpl(static_cast<int>(need));
       // The TMA ring is used only on request: measured on GB300 it trails
       // the register kernel on every workload here.
-      if (g == 1 && path == LTXK_PATH_TMA) {
+      if (g == 1 && path == LTXK_PATH_TMA && km != ltxk::kAdaLN) {
         const uint32_t stride = tma_stride(hidden);
         int stages = static_cast<int>((kTmaSmemTarget - ltxk::kTmaBarBytes) /
                                       (ltxk::kTmaWarps * stride));
@@ -256,6 +258,7 @@ const void* kernel_fn(const ltxk_plan& p, int km) {
       if (km == ltxk::kPlain) return ltxk::rows_vec_plain_ptr(p.group_warps, p.vec_per_lane);
       if (km == ltxk::kInterleaved)
         return ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
+      if (km == ltxk::kAdaLN) return ltxk::rows_vec_adaln_ptr(p.group_warps, p.vec_per_lane);
       return ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane);
     case LTXK_KERNEL_ROWS_TMA:
       if (km == ltxk::kPlain) return ltxk::rows_tma_plain_ptr(p.vec_per_lane);
@@ -283,7 +286,8 @@ int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStre
   e = resident_ctas(dev, fn, p.block_threads, p.smem_bytes, &per_sm);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
-  const bool persistent = km == ltxk::kPlain ? LTXK_PERSISTENT : LTXK_PERSISTENT_ROPE;
+  const bool persistent =
+      (km == ltxk::kPlain || km == ltxk::kAdaLN) ? LTXK_PERSISTENT : LTXK_PERSISTENT_ROPE;
   const int64_t cap = (persistent || p.kernel == LTXK_KERNEL_ROWS_TMA)
                           ? static_cast<int64_t>(sms) * per_sm
                           : int64_t{2147483647};
@@ -373,6 +377,29 @@ int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w, const float*
                            const float* sin, int64_t rows, int heads, int head_dim, int mode,
                            float eps, int64_t seq_len, ltxk_stream_t stream) {
   return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len, stream);
+}
+
+int ltxk_rms_norm_adaln(void* out, const void* x, const void* w, const void* scale,
+                        const void* shift, int64_t rows, int64_t hidden, int64_t rows_per_cond,
+                        float eps, ltxk_stream_t stream) {
+  if (scale == nullptr || shift == nullptr) return LTXK_ERR_NULL;
+  int st = norm_checks(out, x, w, rows, hidden);
+  if (st != LTXK_OK) return st;
+  if (rows_per_cond < 1) return LTXK_ERR_SHAPE;
+  if (!aligned_to(scale, 2) || !aligned_to(shift, 2)) return LTXK_ERR_ALIGN;
+  const int64_t n_cond = rows == 0 ? 0 : (rows - 1) / rows_per_cond + 1;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  const uint64_t cbytes = static_cast<uint64_t>(n_cond) * hidden * 2;
+  if (overlaps(out, xbytes, scale, cbytes) || overlaps(out, xbytes, shift, cbytes))
+    return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
+                         aligned_to(scale, 16) && aligned_to(shift, 16);
+  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
+                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
+                  static_cast<int>(hidden), 0, eps, static_cast<const uint16_t*>(scale),
+                  static_cast<const uint16_t*>(shift), rows_per_cond};
+  return launch(LTXK_OP_RMS_NORM_ADALN, 0, a, vector_ok, stream, g_path.load());
 }
 
 int ltxk_fault_status(void) {

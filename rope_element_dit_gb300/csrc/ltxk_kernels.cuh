@@ -38,7 +38,7 @@
 
 namespace ltxk {
 
-enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2 };
+enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2, kAdaLN = 3 };
 
 struct RowArgs {
   uint16_t* out;            // [rows, hidden] bf16
@@ -51,6 +51,9 @@ struct RowArgs {
   int hidden;
   int head_dim;
   float eps;
+  const uint16_t* scale;    // AdaLN: [n_cond, hidden] bf16
+  const uint16_t* shift;    // AdaLN: [n_cond, hidden] bf16
+  int64_t rows_per_cond;    // AdaLN: row r uses conditioning row r / rows_per_cond
 };
 
 // ---- element helpers -----------------------------------------------------
@@ -306,6 +309,31 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
     });
     return;
+  } else if constexpr (MODE == kAdaLN) {
+    // y = n * (1 + scale) + shift with n = (x * w) * inv_rms; one conditioning
+    // row serves rows_per_cond rows, so its vectors come from L1/L2
+    const int64_t c = row / a.rows_per_cond;
+    const uint16_t* scr = a.scale + c * a.hidden;
+    const uint16_t* shr = a.shift + c * a.hidden;
+    const float2 one2 = make_float2(1.f, 1.f);
+    m.each_slot([&](int k, int off, int, bool ok) {
+      if (!ok) return;
+      const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
+      const uint4 sv = ld_ro16(scr + off);
+      const uint4 tv = ld_ro16(shr + off);
+      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
+      const uint32_t su[4] = {sv.x, sv.y, sv.z, sv.w};
+      const uint32_t tu[4] = {tv.x, tv.y, tv.z, tv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 n = __fmul2_rn(__fmul2_rn(bf2_of(xu[i]), bf2_of(wu[i])), inv2);
+        o[i] = pack_f2(__ffma2_rn(n, __fadd2_rn(one2, bf2_of(su[i])), bf2_of(tu[i])));
+      }
+      st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+    });
+    return;
   } else {
     const int64_t pos = row % a.table_rows;
     const float* ct = a.cos_t + pos * m.P;
@@ -418,9 +446,10 @@ struct GroupShape {
 template <int MODE, int VPL>
 struct RegBudget {
   static constexpr int kRegs =
-      4 * VPL + (MODE == kPlain ? LTXK_REG_EXTRA_PLAIN
-                                : (MODE == kInterleaved ? LTXK_REG_EXTRA_INTERLEAVED
-                                                        : LTXK_REG_EXTRA_SPLIT));
+      4 * VPL + (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
+                 : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
+                 : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
+                                         : LTXK_REG_EXTRA_PLAIN + 16);
 };
 template <int MODE, int G, int VPL>
 struct VecLaunch {
@@ -663,6 +692,14 @@ rows_elem_kernel(const RowArgs a) {
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
         const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
         yr[j] = f_to_bf(__fmul_rn(__fmul_rn(bf_to_f(xr[j]), wj), inv_rms));
+      }
+    } else if (MODE == kAdaLN) {
+      const int64_t c = row / a.rows_per_cond;
+      for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+        const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
+        const float n = __fmul_rn(__fmul_rn(bf_to_f(xr[j]), wj), inv_rms);
+        const float sc = __fadd_rn(1.f, bf_to_f(a.scale[c * H + j]));
+        yr[j] = f_to_bf(__fmaf_rn(n, sc, bf_to_f(a.shift[c * H + j])));
       }
     } else {
       const int64_t D = a.head_dim, P = D >> 1;

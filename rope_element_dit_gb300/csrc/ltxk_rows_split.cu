@@ -12,6 +12,7 @@ const void* rows_elem_kernel_ptr(int mode) {
     case kPlain: return reinterpret_cast<const void*>(&rows_elem_kernel<kPlain>);
     case kInterleaved: return reinterpret_cast<const void*>(&rows_elem_kernel<kInterleaved>);
     case kSplitHalf: return reinterpret_cast<const void*>(&rows_elem_kernel<kSplitHalf>);
+    case kAdaLN: return reinterpret_cast<const void*>(&rows_elem_kernel<kAdaLN>);
     default: return nullptr;
   }
 }

@@ -215,10 +215,23 @@ class Case:
     seq_len: int = 0               # positions per batch item (table rows)
     table: str = ""                # "1d" or "3axis"
     meta: dict = field(default_factory=dict)
+    op: str = ""                   # "adaln" for the AdaLN-modulated norm
+    weight: bool = True            # False: no weight (ones)
+    rows_per_cond: int = 0         # AdaLN: rows sharing one conditioning row
 
     @property
     def elements(self) -> int:
         return self.rows * self.hidden
+
+    @property
+    def kind(self) -> str:
+        if self.op:
+            return self.op
+        return "norm" if self.mode is None else "rope"
+
+    @property
+    def n_cond(self) -> int:
+        return -(-self.rows // self.rows_per_cond) if self.rows_per_cond else 0
 
 
 def _norm(name, b, s, h, seed, dist, eps):
@@ -260,13 +273,25 @@ STRESS = [
     _norm("rms_norm_65536x5120", 1, 65536, 5120, 9, "uniform4", 1e-5),
 ]
 
+# AdaLN-modulated RMSNorm, x [2, 6144, 2048] with no weight (the pages'
+# weightless LTX-Video block norm); scale, shift [2, 2048] ~ N(0, 0.5).
+ADALN = [Case(
+    name="rms_norm_adaln_2x6144x2048", rows=2 * 6144, hidden=2048, seed=10,
+    x_dist="normal", eps=1e-6, op="adaln", weight=False, rows_per_cond=6144,
+    meta={"shape": [2, 6144, 2048], "cond": [2, 2048], "scale_std": 0.5,
+          "shift_std": 0.5})]
+
 WORKLOADS = {
     "small": SMALL,
     "sweep": SWEEP,
     "rope_interleaved": ROPE_INTERLEAVED,
     "rope_split": ROPE_SPLIT,
     "stress": STRESS,
+    "adaln": ADALN,
 }
+
+STREAM_SCALE = 3
+STREAM_SHIFT = 4
 
 
 def make_x(case: Case, threads: int | None = None) -> np.ndarray:
@@ -301,16 +326,30 @@ def make_tables(case: Case):
     raise ValueError(case.table)
 
 
+def make_cond(case: Case):
+    """AdaLN scale and shift, bfloat16 [n_cond, hidden]."""
+    if case.kind != "adaln":
+        return None, None
+    n = case.n_cond * case.hidden
+    sc = normal_bf16(case.seed, STREAM_SCALE, n, 0.0, case.meta.get("scale_std", 0.5))
+    sh = normal_bf16(case.seed, STREAM_SHIFT, n, 0.0, case.meta.get("shift_std", 0.5))
+    return sc.reshape(case.n_cond, case.hidden), sh.reshape(case.n_cond, case.hidden)
+
+
 def make_inputs(case: Case, threads: int | None = None) -> dict:
     cos, sin = make_tables(case)
-    return {"x": make_x(case, threads), "w": make_w(case), "cos": cos,
-            "sin": sin}
+    scale, shift = make_cond(case)
+    return {"x": make_x(case, threads), "w": make_w(case) if case.weight else None,
+            "cos": cos, "sin": sin, "scale": scale, "shift": shift}
 
 
 def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
     """Bytes one call must move: read x, write y, read w (all bf16), plus the
-    fp32 cos/sin tables at their literal size for the fused form."""
-    b = 4 * case.rows * case.hidden + 2 * case.hidden
+    fp32 cos/sin tables at their literal size for the fused form, or the
+    bf16 scale and shift for the AdaLN form."""
+    b = 4 * case.rows * case.hidden + (2 * case.hidden if case.weight else 0)
+    if case.kind == "adaln":
+        b += 2 * 2 * case.n_cond * case.hidden
     if case.mode is not None:
         P = case.head_dim // 2
         table_rows = case.rows if per_row_tables else case.seq_len

@@ -213,3 +213,30 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_adaln_validation(L):
+    f = L.ltxk_rms_norm_adaln
+    assert f(A, B, W, None, S, 4, 8, 2, 1e-6, None) == L.ERR_NULL
+    assert f(A, B, W, C, None, 4, 8, 2, 1e-6, None) == L.ERR_NULL
+    assert f(A, B, W, C, S, 4, 8, 0, 1e-6, None) == L.ERR_SHAPE        # rows_per_cond
+    assert f(A, B, W, C + 1, S, 4, 8, 2, 1e-6, None) == L.ERR_ALIGN
+    # out (4 rows x 8 x 2 B = 64 B) overlaps the scale
+    assert f(A, B, W, A + 32, S, 4, 8, 2, 1e-6, None) == L.ERR_OVERLAP
+    assert f(A, B, W, C, A, 4, 8, 2, 1e-6, None) == L.ERR_OVERLAP
+    assert f(A, B, W, C, S, 0, 8, 2, 1e-6, None) == L.OK
+
+
+def test_adaln_plan(L):
+    st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 2048, 0, 0, True)
+    assert st == L.OK and (p.kernel, p.group_warps, p.vec_per_lane) == (1, 1, 8)
+    st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 3072, 0, 0, True)
+    assert (p.kernel, p.group_warps, p.vec_per_lane) == (1, 4, 4)
+    st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 3072, 0, 0, False)
+    assert p.kernel == L.KERNEL_ROWS_ELEM
+    try:   # the TMA ring has no AdaLN form: the register kernel stays
+        L.ltxk_set_path(L.PATH_TMA)
+        st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 2048, 0, 0, True)
+        assert p.kernel == L.KERNEL_ROWS_VEC
+    finally:
+        L.ltxk_set_path(L.PATH_AUTO)

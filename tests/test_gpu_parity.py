@@ -23,7 +23,7 @@ import torch
 import oracle
 import rope_element_dit_gb300 as L
 import synth
-from oracle.compare import compare_bf16
+from oracle.compare import compare_bf16, compare_bf16_bounded
 
 pytestmark = pytest.mark.gpu
 
@@ -128,13 +128,56 @@ def gpu_rope(x_dev, w_dev, c_dev, s_dev, rows, heads, D, mode, eps, seq_len=None
 ALL_CASES = [c for cases in synth.WORKLOADS.values() for c in cases]
 
 
+def adaln_bound(hidden, y_exact, shift_rows):
+    """Bound on the GPU's fp32 error in n*(1+scale)+shift before rounding.
+
+    n = (x*w)*inv_rms carries a relative error delta(H) from the fp32 sum of
+    squares (at most H/64 + 40 chained additions), the mean, eps, rsqrtf
+    (2 ulp) and the product; the shift can cancel n*(1+scale), so the bound
+    is absolute: 2*delta*|n(1+s)| plus the roundings of 1+s and of the FMA."""
+    delta = (hidden / 128 + 26) * 2.0 ** -24
+    ns = np.abs(y_exact - shift_rows)
+    return 2 * delta * ns + 2.0 ** -22 * (ns + np.abs(shift_rows))
+
+
+def gpu_adaln(x_dev, w_dev, sc_dev, sh_dev, rows, hidden, rows_per_cond, eps, out=None):
+    if out is None:
+        out = torch.empty(rows * hidden, dtype=torch.int16, device="cuda")
+    st = L.ltxk_rms_norm_adaln(dptr(out), dptr(x_dev), dptr(w_dev), dptr(sc_dev),
+                               dptr(sh_dev), rows, hidden, rows_per_cond, eps, stream_ptr())
+    assert st == L.OK, L.ltxk_status_string(st)
+    return out
+
+
+def check_adaln(got_bits, x, w, scale, shift, rows_per_cond, eps, what, threads=1):
+    rows, H = x.shape
+    _, ye = oracle.rms_norm_adaln(x, w, scale, shift, eps, rows_per_cond=rows_per_cond,
+                                  threads=threads, exact=True)
+    t = np.repeat(oracle.widen_bf16(shift), rows_per_cond, axis=0)[:rows]
+    got = got_bits.reshape(rows, H)
+    step = max(1, (1 << 24) // H)
+    for r0 in range(0, rows, step):
+        r = compare_bf16_bounded(got[r0:r0 + step], ye[r0:r0 + step],
+                                 adaln_bound(H, ye[r0:r0 + step], t[r0:r0 + step]))
+        assert r["ok"], f"{what} rows {r0}+: {r}"
+
+
 @pytest.mark.parametrize("case", ALL_CASES, ids=[c.name for c in ALL_CASES])
 def test_workload_full_size(case, path):
     inp = synth.make_inputs(case)
     x, w = inp["x"], inp["w"]
     n = case.rows * case.hidden
     whole, out = guarded(n)
-    xd, wd = to_dev(x), to_dev(w)
+    xd, wd = to_dev(x), (None if w is None else to_dev(w))
+    if case.kind == "adaln":
+        gpu_adaln(xd, wd, to_dev(inp["scale"]), to_dev(inp["shift"]), case.rows,
+                  case.hidden, case.rows_per_cond, case.eps, out=out)
+        torch.cuda.synchronize()
+        check_guard(whole, n)
+        check_adaln(to_host(out), x, w, inp["scale"], inp["shift"], case.rows_per_cond,
+                    case.eps, case.name, threads=THREADS)
+        assert L.ltxk_fault_status() == L.OK
+        return
     if case.mode is None:
         gpu_rms_norm(xd, wd, case.rows, case.hidden, case.eps, out=out)
         ref = oracle.rms_norm(x, w, case.eps, threads=THREADS)
@@ -398,3 +441,67 @@ def test_tma_wait_runs_out_and_context_survives():
     torch.cuda.synchronize()
     assert_parity(to_host(y), oracle.rms_norm(x, None, 1e-6), "after timeout")
     assert L.ltxk_fault_status() == L.OK
+
+
+# ------------------------------------------------------------------ AdaLN --
+
+ADALN_SHAPES = [  # (rows, hidden, rows_per_cond, with_w)
+    (6, 4, 3, False), (7, 24, 3, True), (33, 264, 11, False), (100, 2048, 25, True),
+    (1001, 3072, 1000, False), (64, 5120, 64, True), (9, 4096, 1, False),
+    (5, 7, 2, True), (3, 131080, 2, False), (37, 2056, 10, True)]
+
+
+@pytest.mark.parametrize("rows,hidden,rpc,with_w", ADALN_SHAPES)
+def test_adaln_shapes(rows, hidden, rpc, with_w):
+    seed = 3000 + rows + hidden
+    n_cond = -(-rows // rpc)
+    x = synth.normal_bf16(seed, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(seed, 2, hidden, 1.0, 0.1) if with_w else None
+    sc = synth.normal_bf16(seed, 3, n_cond * hidden, 0.0, 0.5).reshape(n_cond, hidden)
+    sh = synth.normal_bf16(seed, 4, n_cond * hidden, 0.0, 0.5).reshape(n_cond, hidden)
+    whole, out = guarded(rows * hidden)
+    gpu_adaln(to_dev(x), None if w is None else to_dev(w), to_dev(sc), to_dev(sh), rows,
+              hidden, rpc, 1e-6, out=out)
+    torch.cuda.synchronize()
+    check_guard(whole, rows * hidden)
+    check_adaln(to_host(out), x, w, sc, sh, rpc, 1e-6, f"adaln {rows}x{hidden}/{rpc}")
+
+
+def test_adaln_unaligned_and_in_place():
+    rows, hidden, rpc = 40, 3072, 20
+    x = synth.normal_bf16(51, 0, rows * hidden).reshape(rows, hidden)
+    sc = synth.normal_bf16(51, 3, 2 * hidden, 0.0, 0.5).reshape(2, hidden)
+    sh = synth.normal_bf16(51, 4, 2 * hidden, 0.0, 0.5).reshape(2, hidden)
+    # scale 2 bytes off a 16-byte boundary: element-wise kernel
+    scb = to_dev(np.concatenate([np.zeros(1, np.uint16), sc.ravel()]))
+    out = gpu_adaln(to_dev(x), None, scb[1:], to_dev(sh), rows, hidden, rpc, 1e-6)
+    torch.cuda.synchronize()
+    check_adaln(to_host(out), x, None, sc, sh, rpc, 1e-6, "adaln unaligned")
+    xd = to_dev(x)
+    gpu_adaln(xd, None, to_dev(sc), to_dev(sh), rows, hidden, rpc, 1e-6, out=xd)
+    torch.cuda.synchronize()
+    check_adaln(to_host(xd), x, None, sc, sh, rpc, 1e-6, "adaln in place")
+
+
+def test_adaln_zero_modulation_equals_rms_norm():
+    rows, hidden = 257, 3072
+    x = synth.normal_bf16(52, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(52, 2, hidden, 1.0, 0.1)
+    zero = torch.zeros(hidden, dtype=torch.int16, device="cuda")
+    xd, wd = to_dev(x), to_dev(w)
+    a = gpu_adaln(xd, wd, zero, zero, rows, hidden, rows, 1e-6)
+    b = gpu_rms_norm(xd, wd, rows, hidden, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_adaln_binding_helper():
+    B, S, H = 2, 48, 2048
+    x = synth.normal_bf16(53, 0, B * S * H).reshape(B * S, H)
+    sc = synth.normal_bf16(53, 3, B * H, 0.0, 0.5).reshape(B, H)
+    sh = synth.normal_bf16(53, 4, B * H, 0.0, 0.5).reshape(B, H)
+    y = L.rms_norm_adaln(to_dev(x).view(torch.bfloat16).reshape(B, S, H), None,
+                         to_dev(sc).view(torch.bfloat16), to_dev(sh).view(torch.bfloat16))
+    torch.cuda.synchronize()
+    check_adaln(y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * S, H), x,
+                None, sc, sh, S, 1e-6, "adaln helper")
