@@ -72,7 +72,8 @@ def compare_bf16_bounded(got: np.ndarray, exact: np.ndarray, bound: np.ndarray) 
     before that rounding)."""
     got = np.asarray(got, dtype=np.uint16).reshape(-1)
     exact = np.asarray(exact, dtype=np.float64).reshape(-1)
-    bound = np.broadcast_to(np.asarray(bound, dtype=np.float64), exact.shape).reshape(-1)
+    bound = np.asarray(bound, dtype=np.float64)
+    bound = bound.reshape(-1) if bound.size == exact.size else np.broadcast_to(bound, exact.shape)
     g = widen(got)
     ref_bits = _round_bits(exact)
     d = ulp_distance(got, ref_bits)
