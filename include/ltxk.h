@@ -143,6 +143,28 @@ LTXK_API int ltxk_rms_norm_adaln(void* out, const void* x, const void* w,
                                  ltxk_stream_t stream);
 
 /*
+ * ltxk_rms_norm_host -- ltxk_rms_norm for x and y in HOST memory, pipelined.
+ * The rows are cut into chunks; chunk i is copied in on streams[i % n],
+ * normalised in place in staging slot i % n, and copied out, so the copy-in,
+ * kernel and copy-out of consecutive chunks overlap.  Asynchronous: the
+ * results are in out_host once every stream in `streams` has finished.
+ *   out_host, x_host [rows, hidden] bf16 in host memory; page-locked memory
+ *                 (cudaHostAlloc / torch pin_memory) lets the copies overlap.
+ *   w             [hidden] bf16 on the device, or NULL (ones).
+ *   staging       device memory of staging_bytes, 256-byte aligned, owned by
+ *                 the caller; split into n_streams slots of at least one row.
+ *   streams       n_streams (1 .. LTXK_HOST_MAX_STREAMS) streams, ideally
+ *                 distinct non-default streams.
+ * The library allocates nothing.  Returns an ltxk_status; argument errors
+ * are reported before any copy is queued.
+ */
+#define LTXK_HOST_MAX_STREAMS 8
+LTXK_API int ltxk_rms_norm_host(void* out_host, const void* x_host, const void* w,
+                                int64_t rows, int64_t hidden, float eps,
+                                void* staging, int64_t staging_bytes,
+                                const ltxk_stream_t* streams, int n_streams);
+
+/*
  * ltxk_fault_status -- did any kernel on the current device give up waiting
  * since the last call?  The TMA-ring kernel bounds each wait for a bulk copy
  * of a row (about two seconds); a wait that runs out sets a device fault

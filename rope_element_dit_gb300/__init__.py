@@ -43,7 +43,7 @@ KERNEL_ROWS_TMA = 3
 
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
-           "ltxk_rms_norm_adaln",
+           "ltxk_rms_norm_adaln", "ltxk_rms_norm_host",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_rms_norm_noalloc",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
@@ -82,6 +82,9 @@ def _load():
         getattr(lib, f).restype = I32
     lib.ltxk_rms_norm_adaln.argtypes = [P, P, P, P, P, I64, I64, I64, F32, P]
     lib.ltxk_rms_norm_adaln.restype = I32
+    lib.ltxk_rms_norm_host.argtypes = [P, P, P, I64, I64, F32, P, I64,
+                                       ctypes.POINTER(ctypes.c_void_p), I32]
+    lib.ltxk_rms_norm_host.restype = I32
     lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
     lib.ltxk_rms_norm_noalloc.restype = I32
     lib.ltxk_fault_status.argtypes = []
@@ -124,6 +127,14 @@ def ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond, ep
                         stream) -> int:
     return _lib.ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond,
                                     eps, stream)
+
+
+def ltxk_rms_norm_host(out_host, x_host, w, rows, hidden, eps, staging, staging_bytes,
+                       streams, n_streams) -> int:
+    """``streams``: a sequence of stream handles (ints), marshalled to an array."""
+    arr = (ctypes.c_void_p * max(1, len(streams)))(*streams)
+    return _lib.ltxk_rms_norm_host(out_host, x_host, w, rows, hidden, eps, staging,
+                                   staging_bytes, arr, n_streams)
 
 
 def ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream) -> int:
@@ -254,4 +265,34 @@ def rms_norm_adaln(x, weight, scale, shift, eps: float = 1e-6, rows_per_cond=Non
                              _dev_ptr(shift, "shift", torch.bfloat16),
                              rows, hidden, rows_per_cond, eps, _stream_handle(x, stream))
     _check(st, "ltxk_rms_norm_adaln")
+    return out
+
+
+def rms_norm_host(x, weight=None, eps: float = 1e-6, out=None, staging=None,
+                  streams=None):
+    """RMSNorm of a HOST tensor ``x`` (bf16, ideally pinned) into a host
+    tensor, pipelined over ``streams`` (default: three new streams on the
+    current device) and a device ``staging`` buffer (default: 3 x 16 MiB).
+    Waits for the result before returning."""
+    import torch
+    if x.is_cuda:
+        raise TypeError("x must be a host tensor (use rms_norm for device tensors)")
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous bfloat16 tensor")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    if out is None:
+        out = torch.empty_like(x, pin_memory=x.is_pinned())
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if streams is None:
+        streams = [torch.cuda.Stream(dev) for _ in range(3)]
+    if staging is None:
+        staging = torch.empty(len(streams) * (16 << 20), dtype=torch.uint8, device=dev)
+    w = _dev_ptr(weight, "weight", torch.bfloat16)
+    st = ltxk_rms_norm_host(out.data_ptr(), x.data_ptr(), w, rows, hidden, eps,
+                            staging.data_ptr(), staging.numel() * staging.element_size(),
+                            [s.cuda_stream for s in streams], len(streams))
+    _check(st, "ltxk_rms_norm_host")
+    for s in streams:
+        s.synchronize()
     return out

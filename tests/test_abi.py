@@ -240,3 +240,17 @@ def test_adaln_plan(L):
         assert p.kernel == L.KERNEL_ROWS_VEC
     finally:
         L.ltxk_set_path(L.PATH_AUTO)
+
+
+def test_host_pipeline_validation(L):
+    f = L.ltxk_rms_norm_host
+    st = [0, 0]
+    assert f(None, B, W, 4, 8, 1e-6, C, 1 << 20, st, 2) == L.ERR_NULL
+    assert f(A, B, W, 4, 8, 1e-6, None, 1 << 20, st, 2) == L.ERR_NULL
+    assert f(A, B, W, 4, 8, 1e-6, C, 1 << 20, st, 0) == L.ERR_SHAPE       # no stream
+    assert f(A, B, W, 4, 8, 1e-6, C, 1 << 20, st * 5, 10) == L.ERR_SHAPE  # too many
+    assert f(A, B, W, 4, 8, 1e-6, C, 16, st, 2) == L.ERR_SHAPE            # < 1 row/slot
+    assert f(A, B, W, 4, 8, 1e-6, C + 16, 1 << 20, st, 2) == L.ERR_ALIGN  # staging 256 B
+    assert f(A + 1, B, W, 4, 8, 1e-6, C, 1 << 20, st, 2) == L.ERR_ALIGN
+    assert f(A, B, C + 64, 4, 8, 1e-6, C, 1 << 20, st, 2) == L.ERR_OVERLAP  # w in staging
+    assert f(A, B, W, 0, 8, 1e-6, C, 1 << 20, st, 2) == L.OK

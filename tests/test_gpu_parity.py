@@ -505,3 +505,39 @@ def test_adaln_binding_helper():
     torch.cuda.synchronize()
     check_adaln(y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(B * S, H), x,
                 None, sc, sh, S, 1e-6, "adaln helper")
+
+
+# --------------------------------------------------------- host pipeline --
+
+@pytest.mark.parametrize("rows,hidden,slot_rows,n_streams,pinned", [
+    (4099, 3072, 512, 3, True), (1000, 2048, 1, 2, True), (37, 264, 5, 3, False),
+    (16384, 3072, 4096, 3, True), (9, 24, 100, 1, True)])
+def test_host_pipeline_matches_device_call(rows, hidden, slot_rows, n_streams, pinned):
+    x = synth.normal_bf16(61, 0, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(61, 2, hidden, 1.0, 0.1)
+    xh = torch.from_numpy(x.view(np.int16).copy())
+    yh = torch.full_like(xh, 0x7FC1)
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
+    wd = to_dev(w)
+    slot = (slot_rows * hidden * 2 + 255) // 256 * 256
+    staging = torch.empty(n_streams * slot, dtype=torch.uint8, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    st = L.ltxk_rms_norm_host(yh.data_ptr(), xh.data_ptr(), wd.data_ptr(), rows, hidden,
+                              1e-6, staging.data_ptr(), staging.numel(),
+                              [s.cuda_stream for s in streams], n_streams)
+    assert st == L.OK
+    for s in streams:
+        s.synchronize()
+    ref = gpu_rms_norm(to_dev(x), wd, rows, hidden, 1e-6)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh.numpy().view(np.uint16), to_host(ref))
+
+
+def test_host_pipeline_helper():
+    rows, hidden = 3000, 2048
+    x = synth.normal_bf16(62, 0, rows * hidden).reshape(rows, hidden)
+    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    y = L.rms_norm_host(xh, None, 1e-6)
+    assert_parity(y.view(torch.int16).numpy().view(np.uint16), oracle.rms_norm(x, None, 1e-6),
+                  "host helper")
