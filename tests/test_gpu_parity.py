@@ -531,7 +531,7 @@ def test_host_pipeline_matches_device_call(rows, hidden, slot_rows, n_streams, p
         s.synchronize()
     ref = gpu_rms_norm(to_dev(x), wd, rows, hidden, 1e-6)
     torch.cuda.synchronize()
-    assert np.array_equal(yh.numpy().view(np.uint16), to_host(ref))
+    assert np.array_equal(yh.numpy().view(np.uint16).ravel(), to_host(ref))
 
 
 def test_host_pipeline_helper():
