@@ -73,6 +73,8 @@ def _load():
             lib.oracle_rms_norm_adaln.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                                   ctypes.c_float, P]
             lib.oracle_rms_norm_adaln.restype = ctypes.c_int
+            lib.oracle_add_rms_norm.argtypes = [P, P, P, P, P, I64, I64, ctypes.c_float, P]
+            lib.oracle_add_rms_norm.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -218,6 +220,38 @@ def rms_norm_adaln(x, w, scale, shift, eps, *, rows_per_cond=None,
     _run_blocks(run, rows, threads)
     y = y.reshape(x.shape)
     return (y, ye.reshape(x.shape)) if exact else y
+
+
+def add_rms_norm(x, res, w, eps, *, threads: int = 1, exact: bool = False):
+    """Oracle fused residual add + RMSNorm.
+
+    Returns ``(y, h)`` bf16 bit patterns (``h = bf16(x + res)``, ``y`` the
+    RMSNorm of ``h``), or ``(y, h, y_exact)`` when ``exact``.
+    """
+    x = _u16(x, "x")
+    res = _u16(res, "res")
+    if x.shape != res.shape:
+        raise ValueError("x and res must have the same shape")
+    H = x.shape[-1]
+    rows = x.size // H if H else 0
+    x2, r2 = x.reshape(rows, H), res.reshape(rows, H)
+    w = None if w is None else _u16(w, "w")
+    y = np.empty_like(x2)
+    h = np.empty_like(x2)
+    ye = np.empty(x2.shape, np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        rc = lib.oracle_add_rms_norm(
+            _ptr(y[r0:r1]), _ptr(h[r0:r1]), _ptr(x2[r0:r1]), _ptr(r2[r0:r1]), _ptr(w),
+            r1 - r0, H, ctypes.c_float(eps), None if ye is None else _ptr(ye[r0:r1]))
+        if rc != 0:
+            raise MemoryError("oracle_add_rms_norm failed")
+
+    _run_blocks(run, rows, threads)
+    y, h = y.reshape(x.shape), h.reshape(x.shape)
+    return (y, h, ye.reshape(x.shape)) if exact else (y, h)
 
 
 def _run_blocks(fn, rows, threads):

@@ -32,6 +32,11 @@
  * no blocking, fusion or reordering.  The build compiles this file with
  * -ffp-contract=off so that no multiply-add is fused on any host.
  *
+ *   - same page, "Supported Data Types" / "Kernel-Specific Guidelines /
+ *     RMSNorm" in the block context of "Diffusers Critical Pitfalls": the
+ *     residual add that precedes each block norm, fused here as
+ *     h = bf16(x + residual), y = RMSNorm(h) -- the norm reads the rounded
+ *     residual stream h, exactly as the unfused add-then-norm does.
  *   - same page, "Kernel-Specific Guidelines / AdaLN": the DiT conditioning
  *     norm(x) * weight * (1 + scale) + shift, with norm the RMSNorm above;
  *     scale and shift are one hidden-sized vector per conditioning row (one
@@ -214,6 +219,29 @@ int oracle_rms_norm_adaln(uint16_t* y, const uint16_t* x, const uint16_t* w,
             const double v = n[j] * (1.0 + sc) + sh;
             if (y_exact) y_exact[r * H + j] = v;
             y[r * H + j] = round_to_bf16(v);
+        }
+    }
+    free(n);
+    return 0;
+}
+
+/* Fused residual add + RMSNorm:
+ *   h[r, j] = bf16( x[r, j] + res[r, j] )        (the new residual stream)
+ *   y[r, j] = bf16( h[r, j] * w[j] / sqrt(mean_j h[r, j]^2 + eps) )
+ * x, res, h, y: row-major [rows, H] bf16.  w: [H] or NULL.
+ * Returns 0, or -1 on allocation failure. */
+int oracle_add_rms_norm(uint16_t* y, uint16_t* h, const uint16_t* x,
+                        const uint16_t* res, const uint16_t* w, int64_t rows,
+                        int64_t H, float eps, double* y_exact) {
+    double* n = (double*)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+    if (!n) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < H; ++j)
+            h[r * H + j] = round_to_bf16(widen_bf16(x[r * H + j]) + widen_bf16(res[r * H + j]));
+        normalise_row(h + r * H, w, H, eps, n);
+        for (int64_t j = 0; j < H; ++j) {
+            if (y_exact) y_exact[r * H + j] = n[j];
+            y[r * H + j] = round_to_bf16(n[j]);
         }
     }
     free(n);

@@ -425,3 +425,57 @@ def test_adaln_conditioning_rows(oracle_mod):
     assert np.array_equal(y, np.concatenate(parts))
     assert np.array_equal(oracle_mod.rms_norm_adaln(x, None, s, t, 1e-6, rows_per_cond=3,
                                                     threads=3), y)
+
+
+# ------------------------------------------------------ residual-add pins --
+
+def test_add_norm_hand_cases(oracle_mod):
+    # h = x + res = (3, 4, 0, 0) exactly -> y = (1.2, 1.6, 0, 0) (see
+    # hand_cases_h4.txt for the bf16 bits 0x3F9A, 0x3FCD)
+    x = bits_of([[1, 1, -1, 2]])
+    r = bits_of([[2, 3, 1, -2]])
+    y, h, ye = oracle_mod.add_rms_norm(x, r, None, 0.0, exact=True)
+    assert h.ravel().tolist() == [0x4040, 0x4080, 0x0000, 0x0000]     # 3, 4, 0, 0
+    assert y.ravel().tolist() == [0x3F9A, 0x3FCD, 0x0000, 0x0000]
+    np.testing.assert_allclose(ye.ravel(), [1.2, 1.6, 0, 0], rtol=4e-16)
+    # rounding of h, round to nearest even: 1 + 2^-8 is a tie -> 1.0 (even);
+    # 1 + 3*2^-8 is a tie between 1 + 2^-7 (odd) and 1 + 2^-6 (even)
+    x = bits_of([[1, 1, 1, 1]])
+    r = bits_of([[2.0 ** -8, 3 * 2.0 ** -8, 0, 0]])
+    y, h, ye = oracle_mod.add_rms_norm(x, r, None, 0.0, exact=True)
+    assert h.ravel().tolist() == [0x3F80, 0x3F82, 0x3F80, 0x3F80]
+    # the norm reads the ROUNDED h: mean = (1 + (1 + 2^-6)^2 + 1 + 1) / 4
+    hv = np.array([1.0, 1 + 2.0 ** -6, 1.0, 1.0])
+    np.testing.assert_allclose(ye.ravel(), hv / np.sqrt(np.mean(hv ** 2)), rtol=4e-16)
+
+
+def test_add_norm_zero_residual_is_rms_norm(oracle_mod):
+    x = _rows(61, 9, 96)
+    w = synth.normal_bf16(61, 2, 96, 1.0, 0.1)
+    zero = np.zeros_like(x)
+    y, h, ye = oracle_mod.add_rms_norm(x, zero, w, 1e-6, exact=True)
+    yn, yne = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    assert np.array_equal(h, x) and np.array_equal(y, yn) and np.array_equal(ye, yne)
+
+
+def test_add_norm_commutes_and_cancels(oracle_mod):
+    x = _rows(62, 7, 40)
+    r = _rows(63, 7, 40)
+    a = oracle_mod.add_rms_norm(x, r, None, 1e-6)
+    b = oracle_mod.add_rms_norm(r, x, None, 1e-6)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # x + (-x) = 0 exactly: h is all zero, and with eps > 0 so is y
+    neg = (x ^ np.uint16(0x8000)).astype(np.uint16)
+    y, h = oracle_mod.add_rms_norm(x, neg, None, 1e-6)
+    assert np.all(oracle_mod.widen_bf16(h) == 0) and np.all(oracle_mod.widen_bf16(y) == 0)
+
+
+def test_add_norm_h_is_the_rounded_sum(oracle_mod):
+    x = _rows(64, 16, 128)
+    r = _rows(65, 16, 128, "uniform")
+    _, h = oracle_mod.add_rms_norm(x, r, None, 1e-6, threads=3)
+    s = oracle_mod.widen_bf16(x) + oracle_mod.widen_bf16(r)   # exact in binary64
+    assert np.array_equal(h, oracle_mod.round_bf16(s))
+    # and y is the RMSNorm of that h
+    y, _ = oracle_mod.add_rms_norm(x, r, None, 1e-6)
+    assert np.array_equal(y, oracle_mod.rms_norm(h, None, 1e-6))

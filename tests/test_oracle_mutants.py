@@ -42,6 +42,10 @@ MUTANTS = [
     ("adaln_scale_shift_swapped", "n[j] * (1.0 + sc) + sh", "n[j] * (1.0 + sh) + sc"),
     ("adaln_cond_ignores_first_row", "(first_row + r) / rows_per_cond", "r / rows_per_cond"),
     ("adaln_cond_modulo", "(first_row + r) / rows_per_cond", "(first_row + r) % rows_per_cond"),
+    ("add_norm_of_x", "normalise_row(h + r * H, w, H, eps, n);",
+     "normalise_row(x + r * H, w, H, eps, n);"),
+    ("add_subtracts", "widen_bf16(x[r * H + j]) + widen_bf16(res[r * H + j])",
+     "widen_bf16(x[r * H + j]) - widen_bf16(res[r * H + j])"),
 ]
 
 
@@ -75,6 +79,10 @@ def _pin_calls():
         ("adaln_minus1", pins.test_adaln_scale_minus_one_gives_shift, ()),
         ("adaln_affine", pins.test_adaln_is_affine_in_scale_and_shift, ()),
         ("adaln_cond", pins.test_adaln_conditioning_rows, ()),
+        ("add_hand", pins.test_add_norm_hand_cases, ()),
+        ("add_zero", pins.test_add_norm_zero_residual_is_rms_norm, ()),
+        ("add_commute", pins.test_add_norm_commutes_and_cancels, ()),
+        ("add_rounded", pins.test_add_norm_h_is_the_rounded_sum, ()),
     ]
     return calls
 
