@@ -54,6 +54,8 @@ WORKLOAD_TITLES = {
               "U(-4,4), eps 1e-5, seeds 7-9",
     "adaln": "AdaLN-modulated RMSNorm norm(x)*(1+scale)+shift, x [2, 6144, 2048], "
              "no weight, scale/shift [2, 2048] ~ N(0, 0.5), seed 10",
+    "add_norm": "fused residual add + RMSNorm, h = x + residual, y = RMSNorm(h), "
+                "[4, 4096, 3072], x, residual ~ N(0,1), w ~ N(1,0.1), seed 11",
 }
 
 
@@ -122,7 +124,7 @@ def measured_peak():
 # traffic recorded by ncu stays valid while none of them changes.
 KERNEL_SOURCES = ("ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h", "ltxk_abi.cu",
                   "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",
-                  "ltxk_rows_adaln.cu")
+                  "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu")
 
 
 def source_digest():
@@ -231,7 +233,9 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         r = max(1, math.ceil(c.rows * row_frac))
         x = inp["x"][:r]
         t0 = time.perf_counter()
-        if c.kind == "adaln":
+        if c.kind == "add_norm":
+            oracle.add_rms_norm(x, inp["res"][:r], inp["w"], c.eps, threads=threads)
+        elif c.kind == "adaln":
             oracle.rms_norm_adaln(x, inp["w"], inp["scale"], inp["shift"], c.eps,
                                   rows_per_cond=c.rows_per_cond, threads=threads)
         elif c.mode is None:
@@ -242,7 +246,8 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         t += time.perf_counter() - t0
         b += 4 * r * c.hidden + (2 * c.hidden if inp["w"] is not None else 0) + (
             8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0) + (
-            4 * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0)
+            4 * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0) + (
+            4 * r * c.hidden if c.kind == "add_norm" else 0)
     return t, b
 
 
@@ -306,9 +311,9 @@ def run_reference(args, cases, inputs, world, rank):
 
 def kernel_name(plan, mode):
     """Kernel instance name as ncu prints it; mode None = plain, 0/1 = RoPE
-    pairing, 3 = AdaLN."""
+    pairing, 3 = AdaLN, 4 = residual add + RMSNorm."""
     import rope_element_dit_gb300 as L
-    km = 0 if mode is None else {0: 1, 1: 2, 3: 3}[mode]
+    km = 0 if mode is None else {0: 1, 1: 2, 3: 3, 4: 4}[mode]
     if plan.kernel == L.KERNEL_ROWS_VEC:
         return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
     if plan.kernel == L.KERNEL_ROWS_TMA:
@@ -336,6 +341,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
              "w": (None if inp["w"] is None
                    else torch.from_numpy(inp["w"].view(np.int16)).to(dev)),
              "y": torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)}
+        if c.kind == "add_norm":
+            d["res"] = torch.from_numpy(inp["res"].view(np.int16)).to(dev)
+            d["h"] = torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)
         if c.kind == "adaln":
             d["scale"] = torch.from_numpy(inp["scale"].view(np.int16)).to(dev)
             d["shift"] = torch.from_numpy(inp["shift"].view(np.int16)).to(dev)
@@ -348,6 +356,10 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         c, d = cases[i], dev_bufs[i]
         x = d["x"] if x is None else x
         wp = None if d["w"] is None else d["w"].data_ptr()
+        if c.kind == "add_norm":
+            return L.ltxk_add_rms_norm, (d["y"].data_ptr(), d["h"].data_ptr(), x.data_ptr(),
+                                         d["res"].data_ptr(), wp, c.rows, c.hidden, c.eps,
+                                         sptr)
         if c.kind == "adaln":
             return L.ltxk_rms_norm_adaln, (
                 d["y"].data_ptr(), x.data_ptr(), wp, d["scale"].data_ptr(),
@@ -387,9 +399,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     plans = []
     for c in cases:
         op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
-              "adaln": L.OP_RMS_NORM_ADALN}[c.kind]
+              "adaln": L.OP_RMS_NORM_ADALN, "add_norm": L.OP_ADD_RMS_NORM}[c.kind]
         st, p = L.ltxk_plan_launch(op, c.rows, c.hidden, c.head_dim, c.mode or 0, True)
-        plans.append(kernel_name(p, 3 if c.kind == "adaln" else c.mode))
+        plans.append(kernel_name(p, {"adaln": 3, "add_norm": 4}.get(c.kind, c.mode)))
 
     for i in range(args.warmup):
         flush_l2(i)

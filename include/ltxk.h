@@ -143,6 +143,23 @@ LTXK_API int ltxk_rms_norm_adaln(void* out, const void* x, const void* w,
                                  ltxk_stream_t stream);
 
 /*
+ * ltxk_add_rms_norm -- fused residual add + RMSNorm, the add-then-norm that
+ * precedes each block norm:
+ *     h[r, j] = bf16_rne( x[r, j] + residual[r, j] )     -> residual_out
+ *     y[r, j] = bf16_rne( h[r, j] * w[j] / sqrt(mean_j h[r, j]^2 + eps) ) -> out
+ * The norm reads the rounded h, exactly as the unfused add then norm would.
+ *   out, residual_out, x, residual  [rows, hidden] bf16.  w [hidden] or NULL.
+ * out and residual_out must be disjoint.  Either may be exactly one of the
+ * inputs (in place, e.g. residual_out == residual to update the residual
+ * stream); partial overlaps are rejected.  Reads 4 and writes 4 bytes per
+ * element.
+ */
+LTXK_API int ltxk_add_rms_norm(void* out, void* residual_out, const void* x,
+                               const void* residual, const void* w,
+                               int64_t rows, int64_t hidden, float eps,
+                               ltxk_stream_t stream);
+
+/*
  * ltxk_rms_norm_host -- ltxk_rms_norm for x and y in HOST memory, pipelined.
  * The rows are cut into chunks; chunk i is copied in on streams[i % n],
  * normalised in place in staging slot i % n, and copied out, so the copy-in,
@@ -248,7 +265,12 @@ enum {
                                    copies through a shared-memory ring */
 };
 
-enum { LTXK_OP_RMS_NORM = 0, LTXK_OP_RMS_NORM_ROPE = 1, LTXK_OP_RMS_NORM_ADALN = 2 };
+enum {
+    LTXK_OP_RMS_NORM = 0,
+    LTXK_OP_RMS_NORM_ROPE = 1,
+    LTXK_OP_RMS_NORM_ADALN = 2,
+    LTXK_OP_ADD_RMS_NORM = 3
+};
 
 typedef struct {
     int kernel;          /* LTXK_KERNEL_* */

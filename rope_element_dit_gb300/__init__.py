@@ -35,6 +35,7 @@ ROPE_SPLIT_HALF = 1
 OP_RMS_NORM = 0
 OP_RMS_NORM_ROPE = 1
 OP_RMS_NORM_ADALN = 2
+OP_ADD_RMS_NORM = 3
 
 KERNEL_NONE = 0
 KERNEL_ROWS_VEC = 1
@@ -43,7 +44,7 @@ KERNEL_ROWS_TMA = 3
 
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
-           "ltxk_rms_norm_adaln", "ltxk_rms_norm_host",
+           "ltxk_rms_norm_adaln", "ltxk_rms_norm_host", "ltxk_add_rms_norm",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_rms_norm_noalloc",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
@@ -82,6 +83,8 @@ def _load():
         getattr(lib, f).restype = I32
     lib.ltxk_rms_norm_adaln.argtypes = [P, P, P, P, P, I64, I64, I64, F32, P]
     lib.ltxk_rms_norm_adaln.restype = I32
+    lib.ltxk_add_rms_norm.argtypes = [P, P, P, P, P, I64, I64, F32, P]
+    lib.ltxk_add_rms_norm.restype = I32
     lib.ltxk_rms_norm_host.argtypes = [P, P, P, I64, I64, F32, P, I64,
                                        ctypes.POINTER(ctypes.c_void_p), I32]
     lib.ltxk_rms_norm_host.restype = I32
@@ -127,6 +130,10 @@ def ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond, ep
                         stream) -> int:
     return _lib.ltxk_rms_norm_adaln(out, x, w, scale, shift, rows, hidden, rows_per_cond,
                                     eps, stream)
+
+
+def ltxk_add_rms_norm(out, residual_out, x, residual, w, rows, hidden, eps, stream) -> int:
+    return _lib.ltxk_add_rms_norm(out, residual_out, x, residual, w, rows, hidden, eps, stream)
 
 
 def ltxk_rms_norm_host(out_host, x_host, w, rows, hidden, eps, staging, staging_bytes,
@@ -296,3 +303,24 @@ def rms_norm_host(x, weight=None, eps: float = 1e-6, out=None, staging=None,
     for s in streams:
         s.synchronize()
     return out
+
+
+def add_rms_norm(x, residual, weight=None, eps: float = 1e-6, out=None, residual_out=None,
+                 stream=None):
+    """h = x + residual (bf16), y = RMSNorm(h); returns ``(y, h)``.  Pass
+    ``residual_out=residual`` to update the residual stream in place."""
+    import torch
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    if out is None:
+        out = torch.empty_like(x)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    st = ltxk_add_rms_norm(_dev_ptr(out, "out", torch.bfloat16),
+                           _dev_ptr(residual_out, "residual_out", torch.bfloat16),
+                           _dev_ptr(x, "x", torch.bfloat16),
+                           _dev_ptr(residual, "residual", torch.bfloat16),
+                           _dev_ptr(weight, "weight", torch.bfloat16),
+                           rows, hidden, eps, _stream_handle(x, stream))
+    _check(st, "ltxk_add_rms_norm")
+    return out, residual_out

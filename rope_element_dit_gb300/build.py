@@ -20,7 +20,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libltxk.so")
 
 SOURCES = ["ltxk_abi.cu", "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu",
-           "ltxk_rows_split.cu", "ltxk_rows_adaln.cu", "ltxk_noalloc.cu",
+           "ltxk_rows_split.cu", "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu", "ltxk_noalloc.cu",
            "ltxk_pipeline.cu"]
 HEADERS = ["ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h"]
 

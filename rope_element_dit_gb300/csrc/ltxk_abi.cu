@@ -94,6 +94,7 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 int kernel_mode(int op, int mode) {
   if (op == LTXK_OP_RMS_NORM) return ltxk::kPlain;
   if (op == LTXK_OP_RMS_NORM_ADALN) return ltxk::kAdaLN;
+  if (op == LTXK_OP_ADD_RMS_NORM) return ltxk::kAddNorm;
   return mode == LTXK_ROPE_INTERLEAVED ? ltxk::kInterleaved : ltxk::kSplitHalf;
 }
 
@@ -175,7 +176,8 @@ int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
   if (op == LTXK_OP_RMS_NORM_ROPE) {
     if (head_dim < 2 || head_dim % 2 != 0 || hidden % head_dim != 0) return LTXK_ERR_SHAPE;
     if (mode != LTXK_ROPE_INTERLEAVED && mode != LTXK_ROPE_SPLIT_HALF) return LTXK_ERR_MODE;
-  } else if (op != LTXK_OP_RMS_NORM && op != LTXK_OP_RMS_NORM_ADALN) {
+  } else if (op != LTXK_OP_RMS_NORM && op != LTXK_OP_RMS_NORM_ADALN &&
+             op != LTXK_OP_ADD_RMS_NORM) {
     return LTXK_ERR_MODE;
   }
   return LTXK_OK;
@@ -191,7 +193,7 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
   bool vec = vector_ok && hidden % 8 == 0;
   if (km == ltxk::kInterleaved) vec = vec && head_dim % 8 == 0;
   if (km == ltxk::kSplitHalf) vec = vec && head_dim % 16 == 0;
-  const bool row_only = km == ltxk::kPlain || km == ltxk::kAdaLN;   // no rotation
+  const bool row_only = km == ltxk::kPlain || km == ltxk::kAdaLN || km == ltxk::kAddNorm;
   if (vec && row_only && LTXK_PLAIN_SPLIT_RULE > 0) {
     // Split the row over g >= 4 warps when it divides into exactly 3 or 4
     // vectors per lane: a light per-warp share (about 45 registers) lets far
@@ -227,7 +229,7 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
       p->vec_per_lane = bucket_vpl(static_cast<int>(need));
       // The TMA ring is used only on request: measured on GB300 it trails
       // the register kernel on every workload here.
-      if (g == 1 && path == LTXK_PATH_TMA && km != ltxk::kAdaLN) {
+      if (g == 1 && path == LTXK_PATH_TMA && km != ltxk::kAdaLN && km != ltxk::kAddNorm) {
         const uint32_t stride = tma_stride(hidden);
         int stages = static_cast<int>((kTmaSmemTarget - ltxk::kTmaBarBytes) /
                                       (ltxk::kTmaWarps * stride));
@@ -259,6 +261,8 @@ const void* kernel_fn(const ltxk_plan& p, int km) {
       if (km == ltxk::kInterleaved)
         return ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
       if (km == ltxk::kAdaLN) return ltxk::rows_vec_adaln_ptr(p.group_warps, p.vec_per_lane);
+      if (km == ltxk::kAddNorm)
+        return ltxk::rows_vec_addnorm_ptr(p.group_warps, p.vec_per_lane);
       return ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane);
     case LTXK_KERNEL_ROWS_TMA:
       if (km == ltxk::kPlain) return ltxk::rows_tma_plain_ptr(p.vec_per_lane);
@@ -287,7 +291,8 @@ int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStre
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
   const bool persistent =
-      (km == ltxk::kPlain || km == ltxk::kAdaLN) ? LTXK_PERSISTENT : LTXK_PERSISTENT_ROPE;
+      (km == ltxk::kPlain || km == ltxk::kAdaLN || km == ltxk::kAddNorm) ? LTXK_PERSISTENT
+                                                                         : LTXK_PERSISTENT_ROPE;
   const int64_t cap = (persistent || p.kernel == LTXK_KERNEL_ROWS_TMA)
                           ? static_cast<int64_t>(sms) * per_sm
                           : int64_t{2147483647};
@@ -400,6 +405,33 @@ int ltxk_rms_norm_adaln(void* out, const void* x, const void* w, const void* sca
                   static_cast<int>(hidden), 0, eps, static_cast<const uint16_t*>(scale),
                   static_cast<const uint16_t*>(shift), rows_per_cond};
   return launch(LTXK_OP_RMS_NORM_ADALN, 0, a, vector_ok, stream, g_path.load());
+}
+
+int ltxk_add_rms_norm(void* out, void* residual_out, const void* x, const void* residual,
+                      const void* w, int64_t rows, int64_t hidden, float eps,
+                      ltxk_stream_t stream) {
+  if (residual_out == nullptr || residual == nullptr) return LTXK_ERR_NULL;
+  int st = norm_checks(out, x, w, rows, hidden);
+  if (st != LTXK_OK) return st;
+  if (!aligned_to(residual_out, 2) || !aligned_to(residual, 2)) return LTXK_ERR_ALIGN;
+  const uint64_t bytes = static_cast<uint64_t>(rows) * hidden * 2;
+  const uint64_t wbytes = static_cast<uint64_t>(hidden) * 2;
+  // the two outputs must be disjoint; an output may coincide exactly with an
+  // input (every row is read before it is written) but not partly overlap one
+  if (overlaps(out, bytes, residual_out, bytes)) return LTXK_ERR_OVERLAP;
+  if (residual_out != x && overlaps(residual_out, bytes, x, bytes)) return LTXK_ERR_OVERLAP;
+  if (residual_out != residual && overlaps(residual_out, bytes, residual, bytes))
+    return LTXK_ERR_OVERLAP;
+  if (out != residual && overlaps(out, bytes, residual, bytes)) return LTXK_ERR_OVERLAP;
+  if (overlaps(residual_out, bytes, w, wbytes)) return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
+                         aligned_to(residual, 16) && aligned_to(residual_out, 16);
+  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
+                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
+                  static_cast<int>(hidden), 0, eps, nullptr, nullptr, 0,
+                  static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(residual_out)};
+  return launch(LTXK_OP_ADD_RMS_NORM, 0, a, vector_ok, stream, g_path.load());
 }
 
 int ltxk_fault_status(void) {

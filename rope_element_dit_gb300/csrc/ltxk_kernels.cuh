@@ -38,7 +38,7 @@
 
 namespace ltxk {
 
-enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2, kAdaLN = 3 };
+enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2, kAdaLN = 3, kAddNorm = 4 };
 
 struct RowArgs {
   uint16_t* out;            // [rows, hidden] bf16
@@ -54,6 +54,8 @@ struct RowArgs {
   const uint16_t* scale;    // AdaLN: [n_cond, hidden] bf16
   const uint16_t* shift;    // AdaLN: [n_cond, hidden] bf16
   int64_t rows_per_cond;    // AdaLN: row r uses conditioning row r / rows_per_cond
+  const uint16_t* res;      // residual add: [rows, hidden] bf16 residual in
+  uint16_t* h_out;          // residual add: [rows, hidden] bf16 h = x + res out
 };
 
 // ---- element helpers -----------------------------------------------------
@@ -99,6 +101,17 @@ __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y
 __device__ __forceinline__ float2 bf2_of(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
 
 __device__ __forceinline__ uint32_t pack_f2(float2 v) { return pack_bf2(v.x, v.y); }
+
+// bf16(a + b) for the 8 bf16 lanes of two vectors.  The fp32 sum of two
+// bf16 values is exact unless their exponents differ by 16 or more, and then
+// the smaller one is far below half a bf16 spacing of the larger, so the one
+// RNE conversion gives the correctly rounded bf16 sum.
+__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
+  return make_uint4(pack_f2(__fadd2_rn(bf2_of(a.x), bf2_of(b.x))),
+                    pack_f2(__fadd2_rn(bf2_of(a.y), bf2_of(b.y))),
+                    pack_f2(__fadd2_rn(bf2_of(a.z), bf2_of(b.z))),
+                    pack_f2(__fadd2_rn(bf2_of(a.w), bf2_of(b.w))));
+}
 
 // Kahan's a*b - c*d on both lanes.
 __device__ __forceinline__ float2 diff_of_products2(float2 a, float2 b, float2 c, float2 d) {
@@ -296,7 +309,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   uint16_t* yr = a.out + row * a.hidden;
   const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
   const float2 inv2 = make_float2(inv_rms, inv_rms);
-  if constexpr (MODE == kPlain) {
+  if constexpr (MODE == kPlain || MODE == kAddNorm) {
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
       const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
@@ -449,6 +462,7 @@ struct RegBudget {
       4 * VPL + (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
                  : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
                  : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
+                 : MODE == kAddNorm      ? 4 * VPL + LTXK_REG_EXTRA_PLAIN  // x and res in flight
                                          : LTXK_REG_EXTRA_PLAIN + 16);
 };
 template <int MODE, int G, int VPL>
@@ -485,6 +499,18 @@ rows_vec_kernel(const RowArgs a) {
     }
     uint4 v[VPL];
     m.load(v, [&](int off) { return ld_stream16(xr + off); });
+    if constexpr (MODE == kAddNorm) {
+      // h = bf16(x + res): stored as the new residual stream, then normalised
+      const uint16_t* rr = a.res + row * a.hidden;
+      uint16_t* hr = a.h_out + row * a.hidden;
+      uint4 rv[VPL];
+      m.load(rv, [&](int off) { return ld_stream16(rr + off); });
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) v[k] = add_bf16x8(v[k], rv[k]);
+      m.each_slot([&](int k, int off, int, bool ok) {
+        if (ok) st16(hr + off, v[k]);
+      });
+    }
 
     float ss = warp_sum(slots_sumsq(v));
     if (G > 1) {
@@ -679,19 +705,33 @@ rows_elem_kernel(const RowArgs a) {
     const uint16_t* xr = a.x + row * H;
     uint16_t* yr = a.out + row * H;
     float ss = 0.f;
-    for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-      const float v = bf_to_f(xr[j]);
-      ss = __fmaf_rn(v, v, ss);
+    if (MODE == kAddNorm) {
+      // h = bf16(x + res), stored as the new residual stream; each thread
+      // reads back only the elements it wrote itself
+      const uint16_t* rr = a.res + row * H;
+      uint16_t* hr = a.h_out + row * H;
+      for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+        const uint16_t hb = f_to_bf(__fadd_rn(bf_to_f(xr[j]), bf_to_f(rr[j])));
+        hr[j] = hb;
+        const float v = bf_to_f(hb);
+        ss = __fmaf_rn(v, v, ss);
+      }
+    } else {
+      for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+        const float v = bf_to_f(xr[j]);
+        ss = __fmaf_rn(v, v, ss);
+      }
     }
     // block_sum ends with a barrier, so every read of this row is done
     // before any thread writes it (in-place safe), and scratch is free for
     // the next row.
     ss = block_sum(ss, scratch);
     const float inv_rms = rsqrtf(__fdiv_rn(ss, static_cast<float>(H)) + a.eps);
-    if (MODE == kPlain) {
+    if (MODE == kPlain || MODE == kAddNorm) {
+      const uint16_t* src = MODE == kAddNorm ? a.h_out + row * H : xr;
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
         const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
-        yr[j] = f_to_bf(__fmul_rn(__fmul_rn(bf_to_f(xr[j]), wj), inv_rms));
+        yr[j] = f_to_bf(__fmul_rn(__fmul_rn(bf_to_f(src[j]), wj), inv_rms));
       }
     } else if (MODE == kAdaLN) {
       const int64_t c = row / a.rows_per_cond;

@@ -10,6 +10,7 @@ const void* rows_vec_plain_ptr(int group_warps, int vec_per_lane);
 const void* rows_vec_interleaved_ptr(int group_warps, int vec_per_lane);
 const void* rows_vec_split_ptr(int group_warps, int vec_per_lane);
 const void* rows_vec_adaln_ptr(int group_warps, int vec_per_lane);
+const void* rows_vec_addnorm_ptr(int group_warps, int vec_per_lane);
 
 // TMA ring kernel for vector slots per lane, or nullptr.
 const void* rows_tma_plain_ptr(int vec_per_lane);
@@ -20,7 +21,7 @@ const void* rows_tma_split_ptr(int vec_per_lane);
 void record_cuda_error(int e);
 
 // Element-wise kernel for a mode (0 plain, 1 interleaved, 2 split-half,
-// 3 AdaLN).
+// 3 AdaLN, 4 residual add + RMSNorm).
 const void* rows_elem_kernel_ptr(int mode);
 
 }  // namespace ltxk

@@ -13,6 +13,7 @@ const void* rows_elem_kernel_ptr(int mode) {
     case kInterleaved: return reinterpret_cast<const void*>(&rows_elem_kernel<kInterleaved>);
     case kSplitHalf: return reinterpret_cast<const void*>(&rows_elem_kernel<kSplitHalf>);
     case kAdaLN: return reinterpret_cast<const void*>(&rows_elem_kernel<kAdaLN>);
+    case kAddNorm: return reinterpret_cast<const void*>(&rows_elem_kernel<kAddNorm>);
     default: return nullptr;
   }
 }

@@ -281,6 +281,12 @@ ADALN = [Case(
     meta={"shape": [2, 6144, 2048], "cond": [2, 2048], "scale_std": 0.5,
           "shift_std": 0.5})]
 
+# Fused residual add + RMSNorm on the largest sweep shape [4, 4096, 3072]:
+# x, residual ~ N(0, 1), weight ~ N(1, 0.1).
+ADD_NORM = [Case(
+    name="add_rms_norm_4x4096x3072", rows=4 * 4096, hidden=3072, seed=11,
+    x_dist="normal", eps=1e-6, op="add_norm", meta={"shape": [4, 4096, 3072]})]
+
 WORKLOADS = {
     "small": SMALL,
     "sweep": SWEEP,
@@ -288,10 +294,12 @@ WORKLOADS = {
     "rope_split": ROPE_SPLIT,
     "stress": STRESS,
     "adaln": ADALN,
+    "add_norm": ADD_NORM,
 }
 
 STREAM_SCALE = 3
 STREAM_SHIFT = 4
+STREAM_RESIDUAL = 5
 
 
 def make_x(case: Case, threads: int | None = None) -> np.ndarray:
@@ -339,8 +347,12 @@ def make_cond(case: Case):
 def make_inputs(case: Case, threads: int | None = None) -> dict:
     cos, sin = make_tables(case)
     scale, shift = make_cond(case)
+    res = None
+    if case.kind == "add_norm":
+        res = normal_bf16(case.seed, STREAM_RESIDUAL, case.elements,
+                          threads=threads).reshape(case.rows, case.hidden)
     return {"x": make_x(case, threads), "w": make_w(case) if case.weight else None,
-            "cos": cos, "sin": sin, "scale": scale, "shift": shift}
+            "cos": cos, "sin": sin, "scale": scale, "shift": shift, "res": res}
 
 
 def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
@@ -348,6 +360,8 @@ def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
     fp32 cos/sin tables at their literal size for the fused form, or the
     bf16 scale and shift for the AdaLN form."""
     b = 4 * case.rows * case.hidden + (2 * case.hidden if case.weight else 0)
+    if case.kind == "add_norm":
+        b += 4 * case.rows * case.hidden          # read the residual, write h
     if case.kind == "adaln":
         b += 2 * 2 * case.n_cond * case.hidden
     if case.mode is not None:

@@ -254,3 +254,19 @@ def test_host_pipeline_validation(L):
     assert f(A + 1, B, W, 4, 8, 1e-6, C, 1 << 20, st, 2) == L.ERR_ALIGN
     assert f(A, B, C + 64, 4, 8, 1e-6, C, 1 << 20, st, 2) == L.ERR_OVERLAP  # w in staging
     assert f(A, B, W, 0, 8, 1e-6, C, 1 << 20, st, 2) == L.OK
+
+
+def test_add_norm_validation(L):
+    f = L.ltxk_add_rms_norm
+    D = 0x7F0500000000
+    E = 0x7F0600000000
+    assert f(A, None, B, C, W, 4, 8, 1e-6, None) == L.ERR_NULL
+    assert f(A, D, B, None, W, 4, 8, 1e-6, None) == L.ERR_NULL
+    assert f(A, D + 1, B, C, W, 4, 8, 1e-6, None) == L.ERR_ALIGN
+    assert f(A, A + 16, B, C, W, 4, 8, 1e-6, None) == L.ERR_OVERLAP      # outputs overlap
+    assert f(A, D, B, D + 2, W, 4, 8, 1e-6, None) == L.ERR_OVERLAP       # partial alias
+    # exact aliases are allowed (rows == 0: nothing is launched)
+    assert f(A, D, A, D, W, 0, 8, 1e-6, None) == L.OK
+    assert f(A, D, E, C, D + 8, 4, 8, 1e-6, None) == L.ERR_OVERLAP       # w in residual_out
+    st, p = L.ltxk_plan_launch(L.OP_ADD_RMS_NORM, 16384, 3072, 0, 0, True)
+    assert st == L.OK and (p.kernel, p.group_warps, p.vec_per_lane) == (1, 4, 4)

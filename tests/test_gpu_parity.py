@@ -169,6 +169,18 @@ def test_workload_full_size(case, path):
     n = case.rows * case.hidden
     whole, out = guarded(n)
     xd, wd = to_dev(x), (None if w is None else to_dev(w))
+    if case.kind == "add_norm":
+        hwhole, hout = guarded(n)
+        st = L.ltxk_add_rms_norm(dptr(out), dptr(hout), dptr(xd), dptr(to_dev(inp["res"])),
+                                 dptr(wd), case.rows, case.hidden, case.eps, stream_ptr())
+        assert st == L.OK
+        torch.cuda.synchronize()
+        check_guard(whole, n)
+        check_guard(hwhole, n)
+        y_ref, h_ref = oracle.add_rms_norm(x, inp["res"], w, case.eps, threads=THREADS)
+        assert np.array_equal(to_host(hout), h_ref.ravel()), "h must be bit-exact"
+        compare_chunked(to_host(out), y_ref, case.name)
+        return
     if case.kind == "adaln":
         gpu_adaln(xd, wd, to_dev(inp["scale"]), to_dev(inp["shift"]), case.rows,
                   case.hidden, case.rows_per_cond, case.eps, out=out)
@@ -541,3 +553,66 @@ def test_host_pipeline_helper():
     y = L.rms_norm_host(xh, None, 1e-6)
     assert_parity(y.view(torch.int16).numpy().view(np.uint16), oracle.rms_norm(x, None, 1e-6),
                   "host helper")
+
+
+# ------------------------------------------------------------ residual add --
+
+ADD_SHAPES = [(1, 4), (3, 24), (37, 264), (1000, 2048), (1001, 3072), (33, 5120),
+              (9, 4096), (5, 7), (2, 131080), (4, 8192)]
+
+
+@pytest.mark.parametrize("rows,hidden", ADD_SHAPES)
+@pytest.mark.parametrize("with_w", [True, False])
+def test_add_rms_norm_shapes(rows, hidden, with_w):
+    seed = 5000 + rows + hidden
+    x = synth.normal_bf16(seed, 0, rows * hidden).reshape(rows, hidden)
+    r = synth.normal_bf16(seed, 5, rows * hidden).reshape(rows, hidden)
+    w = synth.normal_bf16(seed, 2, hidden, 1.0, 0.1) if with_w else None
+    yw, y = guarded(rows * hidden)
+    hw, h = guarded(rows * hidden)
+    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), to_dev(x).data_ptr(),
+                             to_dev(r).data_ptr(), None if w is None else to_dev(w).data_ptr(),
+                             rows, hidden, 1e-6, stream_ptr())
+    assert st == L.OK
+    torch.cuda.synchronize()
+    check_guard(yw, rows * hidden)
+    check_guard(hw, rows * hidden)
+    y_ref, h_ref = oracle.add_rms_norm(x, r, w, 1e-6)
+    assert np.array_equal(to_host(h), h_ref.ravel())
+    assert_parity(to_host(y), y_ref, f"add norm {rows}x{hidden}")
+
+
+def test_add_rms_norm_in_place_residual_stream():
+    """residual_out == residual (update the stream) and out == x."""
+    rows, hidden = 515, 3072
+    x = synth.normal_bf16(71, 0, rows * hidden).reshape(rows, hidden)
+    r = synth.normal_bf16(71, 5, rows * hidden).reshape(rows, hidden)
+    xd, rd = to_dev(x), to_dev(r)
+    st = L.ltxk_add_rms_norm(xd.data_ptr(), rd.data_ptr(), xd.data_ptr(), rd.data_ptr(), None,
+                             rows, hidden, 1e-6, stream_ptr())
+    assert st == L.OK
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.add_rms_norm(x, r, None, 1e-6)
+    assert np.array_equal(to_host(rd), h_ref.ravel())
+    assert_parity(to_host(xd), y_ref, "add norm in place")
+
+
+def test_add_rms_norm_unaligned_and_helper():
+    rows, hidden = 40, 2048
+    x = synth.normal_bf16(72, 0, rows * hidden).reshape(rows, hidden)
+    r = synth.normal_bf16(72, 5, rows * hidden).reshape(rows, hidden)
+    rb = to_dev(np.concatenate([np.zeros(1, np.uint16), r.ravel()]))
+    y = torch.empty(rows * hidden, dtype=torch.int16, device="cuda")
+    h = torch.empty_like(y)
+    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), to_dev(x).data_ptr(),
+                             rb[1:].data_ptr(), None, rows, hidden, 1e-6, stream_ptr())
+    assert st == L.OK
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.add_rms_norm(x, r, None, 1e-6)
+    assert np.array_equal(to_host(h), h_ref.ravel())
+    assert_parity(to_host(y), y_ref, "add norm unaligned")
+    yt, ht = L.add_rms_norm(to_dev(x).view(torch.bfloat16), to_dev(r).view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert np.array_equal(ht.view(torch.int16).cpu().numpy().view(np.uint16).ravel(),
+                          h_ref.ravel())
+    assert_parity(yt.view(torch.int16).cpu().numpy().view(np.uint16), y_ref, "add norm helper")
