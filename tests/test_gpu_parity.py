@@ -171,7 +171,8 @@ def test_workload_full_size(case, path):
     xd, wd = to_dev(x), (None if w is None else to_dev(w))
     if case.kind == "add_norm":
         hwhole, hout = guarded(n)
-        st = L.ltxk_add_rms_norm(dptr(out), dptr(hout), dptr(xd), dptr(to_dev(inp["res"])),
+        rd = to_dev(inp["res"])
+        st = L.ltxk_add_rms_norm(dptr(out), dptr(hout), dptr(xd), dptr(rd),
                                  dptr(wd), case.rows, case.hidden, case.eps, stream_ptr())
         assert st == L.OK
         torch.cuda.synchronize()
@@ -570,9 +571,12 @@ def test_add_rms_norm_shapes(rows, hidden, with_w):
     w = synth.normal_bf16(seed, 2, hidden, 1.0, 0.1) if with_w else None
     yw, y = guarded(rows * hidden)
     hw, h = guarded(rows * hidden)
-    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), to_dev(x).data_ptr(),
-                             to_dev(r).data_ptr(), None if w is None else to_dev(w).data_ptr(),
-                             rows, hidden, 1e-6, stream_ptr())
+    # keep every input tensor referenced until the kernel has run: a freed
+    # temporary's block would be handed to the next allocation
+    xd, rd = to_dev(x), to_dev(r)
+    wd = None if w is None else to_dev(w)
+    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), xd.data_ptr(), rd.data_ptr(),
+                             dptr(wd), rows, hidden, 1e-6, stream_ptr())
     assert st == L.OK
     torch.cuda.synchronize()
     check_guard(yw, rows * hidden)
@@ -604,7 +608,8 @@ def test_add_rms_norm_unaligned_and_helper():
     rb = to_dev(np.concatenate([np.zeros(1, np.uint16), r.ravel()]))
     y = torch.empty(rows * hidden, dtype=torch.int16, device="cuda")
     h = torch.empty_like(y)
-    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), to_dev(x).data_ptr(),
+    xd = to_dev(x)
+    st = L.ltxk_add_rms_norm(y.data_ptr(), h.data_ptr(), xd.data_ptr(),
                              rb[1:].data_ptr(), None, rows, hidden, 1e-6, stream_ptr())
     assert st == L.OK
     torch.cuda.synchronize()
