@@ -597,7 +597,7 @@ def test_add_rms_norm_in_place_residual_stream():
     assert st == L.OK
     torch.cuda.synchronize()
     y_ref, h_ref = oracle.add_rms_norm(x, r, None, 1e-6)
-    assert np.array_equal(to_host(rd), h_ref.ravel())
+    assert np.array_equal(to_host(rd).ravel(), h_ref.ravel())
     assert_parity(to_host(xd), y_ref, "add norm in place")
 
 
