@@ -75,6 +75,10 @@ def _load():
             lib.oracle_rms_norm_adaln.restype = ctypes.c_int
             lib.oracle_add_rms_norm.argtypes = [P, P, P, P, P, I64, I64, ctypes.c_float, P]
             lib.oracle_add_rms_norm.restype = ctypes.c_int
+            lib.oracle_gelu_tanh.argtypes = [P, P, I64, P]
+            lib.oracle_gelu_tanh.restype = None
+            lib.oracle_geglu.argtypes = [P, P, I64, I64, P]
+            lib.oracle_geglu.restype = None
             _lib = lib
     return _lib
 
@@ -252,6 +256,48 @@ def add_rms_norm(x, res, w, eps, *, threads: int = 1, exact: bool = False):
     _run_blocks(run, rows, threads)
     y, h = y.reshape(x.shape), h.reshape(x.shape)
     return (y, h, ye.reshape(x.shape)) if exact else (y, h)
+
+
+def gelu_tanh(x, *, threads: int = 1, exact: bool = False):
+    """Oracle tanh-approximated GELU, elementwise (uint16 bf16 bits)."""
+    x = _u16(x, "x")
+    flat = x.reshape(-1)
+    y = np.empty_like(flat)
+    ye = np.empty(flat.shape, np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        lib.oracle_gelu_tanh(_ptr(y[r0:r1]), _ptr(flat[r0:r1]), r1 - r0,
+                             None if ye is None else _ptr(ye[r0:r1]))
+
+    _run_blocks(run, flat.size, threads)
+    y = y.reshape(x.shape)
+    return (y, ye.reshape(x.shape)) if exact else y
+
+
+def geglu(x, *, threads: int = 1, exact: bool = False):
+    """Oracle GEGLU: x [..., 2h] -> [..., h], value * gelu(gate) with the
+    value in the first half of the last axis and the gate in the second."""
+    x = _u16(x, "x")
+    h2 = x.shape[-1]
+    if h2 % 2:
+        raise ValueError("last axis must be even")
+    h = h2 // 2
+    rows = x.size // h2 if h2 else 0
+    x2 = x.reshape(rows, h2)
+    y = np.empty((rows, h), np.uint16)
+    ye = np.empty((rows, h), np.float64) if exact else None
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        lib.oracle_geglu(_ptr(y[r0:r1]), _ptr(x2[r0:r1]), r1 - r0, h,
+                         None if ye is None else _ptr(ye[r0:r1]))
+
+    _run_blocks(run, rows, threads)
+    shape = x.shape[:-1] + (h,)
+    return (y.reshape(shape), ye.reshape(shape)) if exact else y.reshape(shape)
 
 
 def _run_blocks(fn, rows, threads):

@@ -37,6 +37,14 @@
  *     residual add that precedes each block norm, fused here as
  *     h = bf16(x + residual), y = RMSNorm(h) -- the norm reads the rounded
  *     residual stream h, exactly as the unfused add-then-norm does.
+ *   - same page, "Kernel-Specific Guidelines / GEGLU vs GELU": LTX-Video's
+ *     tanh-approximated GELU ("gelu-approximate"),
+ *       gelu(x) = x/2 * (1 + tanh(z)),  z = sqrt(2/pi) * (x + 0.044715 x^3),
+ *     evaluated through the identity (1 + tanh(z))/2 = 1/(1 + exp(-2z)),
+ *     which stays accurate where 1 + tanh(z) cancels (z < about -18); and
+ *     GEGLU [.., 2h] -> [.., h]: the first half of the last axis is the
+ *     value, the second half the gate, y = value * gelu(gate) (the diffusers
+ *     GEGLU convention the page's LTX-Video discussion refers to).
  *   - same page, "Kernel-Specific Guidelines / AdaLN": the DiT conditioning
  *     norm(x) * weight * (1 + scale) + shift, with norm the RMSNorm above;
  *     scale and shift are one hidden-sized vector per conditioning row (one
@@ -52,6 +60,7 @@
  * pair-norm preservation and the permutation that maps split-half pairing to
  * interleaved pairing.  No function here is left unpinned.
  */
+#define _DEFAULT_SOURCE 1
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -246,4 +255,33 @@ int oracle_add_rms_norm(uint16_t* y, uint16_t* h, const uint16_t* x,
     }
     free(n);
     return 0;
+}
+
+/* tanh-approximated GELU of one value, binary64. */
+static double gelu_tanh(double x) {
+    const double z = sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x);
+    /* x/2 (1 + tanh z) = x / (1 + exp(-2z)) */
+    if (z >= 0.0) return x / (1.0 + exp(-2.0 * z));
+    const double e = exp(2.0 * z);
+    return x * e / (1.0 + e);
+}
+
+/* y = bf16(gelu(x)) elementwise over n values; y_exact optional. */
+void oracle_gelu_tanh(uint16_t* y, const uint16_t* x, int64_t n, double* y_exact) {
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = gelu_tanh(widen_bf16(x[i]));
+        if (y_exact) y_exact[i] = v;
+        y[i] = round_to_bf16(v);
+    }
+}
+
+/* GEGLU: x [rows, 2h] -> y [rows, h], y[r, j] = bf16(x[r, j] * gelu(x[r, h + j])). */
+void oracle_geglu(uint16_t* y, const uint16_t* x, int64_t rows, int64_t h, double* y_exact) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < h; ++j) {
+            const double v = widen_bf16(x[r * 2 * h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + h + j]));
+            if (y_exact) y_exact[r * h + j] = v;
+            y[r * h + j] = round_to_bf16(v);
+        }
+    }
 }

@@ -479,3 +479,65 @@ def test_add_norm_h_is_the_rounded_sum(oracle_mod):
     # and y is the RMSNorm of that h
     y, _ = oracle_mod.add_rms_norm(x, r, None, 1e-6)
     assert np.array_equal(y, oracle_mod.rms_norm(h, None, 1e-6))
+
+
+# ------------------------------------------------------- GELU / GEGLU pins --
+
+def _bf16_grid(lo, hi, n):
+    v = np.linspace(lo, hi, n).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)    # truncate to bf16
+
+
+def test_gelu_is_x_sigma_identity(oracle_mod):
+    # z is odd in x and sigma(2z) + sigma(-2z) = 1, so gelu(x) - gelu(-x) = x
+    x = _bf16_grid(0.01, 12, 3001)
+    neg = (x | np.uint16(0x8000)).astype(np.uint16)
+    _, gp = oracle_mod.gelu_tanh(x, exact=True)
+    _, gn = oracle_mod.gelu_tanh(neg, exact=True)
+    xv = oracle_mod.widen_bf16(x)
+    np.testing.assert_allclose(gp - gn, xv, rtol=1e-15, atol=0)
+
+
+def test_gelu_matches_tanh_form_and_torch(oracle_mod):
+    # on [-2, 4] the literal tanh form is itself accurate (1 + tanh(z) >= 0.04,
+    # so its cancellation costs under 3e-15); further left it is not, which is
+    # why the oracle uses the sigmoid identity
+    x = _bf16_grid(-2, 4, 8001)
+    _, g = oracle_mod.gelu_tanh(x, exact=True)
+    xv = oracle_mod.widen_bf16(x)
+    z = np.sqrt(2 / np.pi) * (xv + 0.044715 * xv ** 3)
+    np.testing.assert_allclose(g, 0.5 * xv * (1 + np.tanh(z)), rtol=1e-14, atol=1e-300)
+    torch = pytest.importorskip("torch")
+    ref = torch.nn.functional.gelu(torch.from_numpy(xv), approximate="tanh").numpy()
+    np.testing.assert_allclose(g, ref, rtol=1e-14, atol=1e-300)
+
+
+def test_gelu_tails(oracle_mod):
+    # large x: gelu(x) = x to far below bf16 resolution
+    x = _bf16_grid(6, 100, 500)
+    assert np.array_equal(oracle_mod.gelu_tanh(x), x)
+    # very negative x: gelu(x) = x e^{2z} / (1 + e^{2z}), so
+    # log(gelu/x) = 2z - log1p(e^{2z}) -- accurate where 1 + tanh(z) cancels
+    x = _bf16_grid(-11, -6, 500)
+    _, g = oracle_mod.gelu_tanh(x, exact=True)
+    xv = oracle_mod.widen_bf16(x)
+    z = np.sqrt(2 / np.pi) * (xv + 0.044715 * xv ** 3)
+    np.testing.assert_allclose(np.log(g / xv), 2 * z - np.log1p(np.exp(2 * z)), rtol=1e-13)
+    assert np.all(g < 0) and np.all(g > -1e-8)
+    assert int(oracle_mod.gelu_tanh(np.array([0x0000], np.uint16))[0]) == 0
+
+
+def test_geglu_value_times_gelu_of_gate(oracle_mod):
+    rows, h = 6, 40
+    x = _rows(81, rows, 2 * h)
+    y, ye = oracle_mod.geglu(x, exact=True)
+    _, gate = oracle_mod.gelu_tanh(x[:, h:], exact=True)
+    np.testing.assert_allclose(ye, oracle_mod.widen_bf16(x[:, :h]) * gate, rtol=1e-15,
+                               atol=1e-300)
+    # the halves are not interchangeable
+    swapped = np.concatenate([x[:, h:], x[:, :h]], axis=1)
+    assert not np.array_equal(oracle_mod.geglu(swapped), y)
+    # gate -> +inf side: gelu(gate) = gate, so y = round(value * gate)
+    big = np.concatenate([x[:, :h], bits_of(np.full((rows, h), 16.0))], axis=1)
+    np.testing.assert_array_equal(oracle_mod.geglu(big),
+                                  oracle_mod.round_bf16(oracle_mod.widen_bf16(x[:, :h]) * 16))

@@ -46,6 +46,12 @@ MUTANTS = [
      "normalise_row(x + r * H, w, H, eps, n);"),
     ("add_subtracts", "widen_bf16(x[r * H + j]) + widen_bf16(res[r * H + j])",
      "widen_bf16(x[r * H + j]) - widen_bf16(res[r * H + j])"),
+    ("gelu_cubic_coefficient", "0.044715 * x * x * x", "0.0447 * x * x * x"),
+    ("gelu_exp_sign", "x / (1.0 + exp(-2.0 * z))", "x / (1.0 + exp(2.0 * z))"),
+    ("gelu_half_scale", "sqrt(2.0 / M_PI)", "sqrt(1.0 / M_PI)"),
+    ("geglu_halves_swapped",
+     "widen_bf16(x[r * 2 * h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + h + j]))",
+     "widen_bf16(x[r * 2 * h + h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + j]))"),
 ]
 
 
@@ -83,6 +89,10 @@ def _pin_calls():
         ("add_zero", pins.test_add_norm_zero_residual_is_rms_norm, ()),
         ("add_commute", pins.test_add_norm_commutes_and_cancels, ()),
         ("add_rounded", pins.test_add_norm_h_is_the_rounded_sum, ()),
+        ("gelu_odd", pins.test_gelu_is_x_sigma_identity, ()),
+        ("gelu_torch", pins.test_gelu_matches_tanh_form_and_torch, ()),
+        ("gelu_tails", pins.test_gelu_tails, ()),
+        ("geglu", pins.test_geglu_value_times_gelu_of_gate, ()),
     ]
     return calls
 
