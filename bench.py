@@ -56,6 +56,10 @@ WORKLOAD_TITLES = {
              "no weight, scale/shift [2, 2048] ~ N(0, 0.5), seed 10",
     "add_norm": "fused residual add + RMSNorm, h = x + residual, y = RMSNorm(h), "
                 "[4, 4096, 3072], x, residual ~ N(0,1), w ~ N(1,0.1), seed 11",
+    "gelu": "tanh-approximated GELU, x [2, 6144, 8192] (LTX-Video feed-forward inner "
+            "width), N(0,1) with 1% x50 outliers, seed 12",
+    "geglu": "GEGLU value * gelu_tanh(gate), x [2, 6144, 2x8192] -> [2, 6144, 8192], "
+             "N(0,1) with 1% x50 outliers, seed 13",
 }
 
 
@@ -120,16 +124,23 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-# The files that define the timed kernels and their launch configuration;
-# traffic recorded by ncu stays valid while none of them changes.
-KERNEL_SOURCES = ("ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h", "ltxk_abi.cu",
-                  "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",
-                  "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu")
+# The files that define each family of timed kernels and its launch
+# configuration; traffic recorded by ncu stays valid while none of them changes.
+KERNEL_SOURCES = {
+    "rows": ("ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h", "ltxk_abi.cu",
+             "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",
+             "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu"),
+    "gelu": ("ltxk_kernels.cuh", "ltxk_launch.h", "ltxk_gelu.cu"),
+}
 
 
-def source_digest():
+def kernel_family(kernel):
+    return "gelu" if kernel.startswith(("gelu", "geglu")) else "rows"
+
+
+def source_digest(family="rows"):
     h = hashlib.sha256()
-    for fn in KERNEL_SOURCES:
+    for fn in KERNEL_SOURCES[family]:
         with open(os.path.join(CSRC, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -233,7 +244,11 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         r = max(1, math.ceil(c.rows * row_frac))
         x = inp["x"][:r]
         t0 = time.perf_counter()
-        if c.kind == "add_norm":
+        if c.kind == "gelu":
+            oracle.gelu_tanh(x, threads=threads)
+        elif c.kind == "geglu":
+            oracle.geglu(x, threads=threads)
+        elif c.kind == "add_norm":
             oracle.add_rms_norm(x, inp["res"][:r], inp["w"], c.eps, threads=threads)
         elif c.kind == "adaln":
             oracle.rms_norm_adaln(x, inp["w"], inp["scale"], inp["shift"], c.eps,
@@ -244,6 +259,9 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
             oracle.rms_norm_rope(x, inp["w"], inp["cos"], inp["sin"], c.heads, c.head_dim,
                                  c.mode, c.eps, table_rows=c.seq_len, threads=threads)
         t += time.perf_counter() - t0
+        if c.kind in ("gelu", "geglu"):
+            b += (4 if c.kind == "gelu" else 6) * r * c.hidden
+            continue
         b += 4 * r * c.hidden + (2 * c.hidden if inp["w"] is not None else 0) + (
             8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0) + (
             4 * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0) + (
@@ -356,6 +374,10 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         c, d = cases[i], dev_bufs[i]
         x = d["x"] if x is None else x
         wp = None if d["w"] is None else d["w"].data_ptr()
+        if c.kind == "gelu":
+            return L.ltxk_gelu_tanh, (d["y"].data_ptr(), x.data_ptr(), c.rows * c.hidden, sptr)
+        if c.kind == "geglu":
+            return L.ltxk_geglu, (d["y"].data_ptr(), x.data_ptr(), c.rows, c.hidden, sptr)
         if c.kind == "add_norm":
             return L.ltxk_add_rms_norm, (d["y"].data_ptr(), d["h"].data_ptr(), x.data_ptr(),
                                          d["res"].data_ptr(), wp, c.rows, c.hidden, c.eps,
@@ -398,6 +420,10 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     bytes_per_step = sum(bytes_per_launch)
     plans = []
     for c in cases:
+        if c.kind in ("gelu", "geglu"):
+            plans.append("gelu_vec_kernel" if c.kind == "gelu" else
+                         "geglu_vec_kernel<unsigned int>")
+            continue
         op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
               "adaln": L.OP_RMS_NORM_ADALN, "add_norm": L.OP_ADD_RMS_NORM}[c.kind]
         st, p = L.ltxk_plan_launch(op, c.rows, c.hidden, c.head_dim, c.mode or 0, True)
@@ -465,7 +491,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
     peak, peak_kind = measured_peak()
     achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
-    digest = source_digest()
+    digest = source_digest(kernel_family(dom_name))
     traffic = recorded_traffic(dom_name, args.workload, digest)
 
     per_shape = []

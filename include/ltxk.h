@@ -160,6 +160,37 @@ LTXK_API int ltxk_add_rms_norm(void* out, void* residual_out, const void* x,
                                ltxk_stream_t stream);
 
 /*
+ * ltxk_gelu_tanh -- elementwise tanh-approximated GELU, bf16 -> bf16:
+ *   y = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+ * ("cuda-kernels" skill page, "Kernel-Specific Guidelines / GEGLU vs GELU":
+ * the approximate GELU of LTX-Video's feed-forward blocks).  Computed in
+ * fp32, rounded once to bf16 (nearest even).
+ *   out, x  n contiguous bf16 values on the device; out == x (in place) is
+ *           allowed, any other overlap returns LTXK_ERR_OVERLAP.
+ *   n       in [0, 2^40]; n == 0 is a no-op.
+ * Pointers need 2-byte alignment; 16-byte aligned pointers take the vector
+ * kernel.  Reads 2 and writes 2 bytes per element.
+ */
+LTXK_API int ltxk_gelu_tanh(void* out, const void* x, int64_t n,
+                            ltxk_stream_t stream);
+
+/*
+ * ltxk_geglu -- gated GELU over the last dimension (same page and section:
+ * GEGLU halves the last dimension):
+ *   out[r, j] = x[r, j] * gelu_tanh(x[r, hidden + j]),  j < hidden
+ * i.e. the first half of each input row is the value, the second half the
+ * gate, and the product of the fp32 value and the fp32 gelu is rounded once.
+ *   x    [rows, 2*hidden] bf16, row-major contiguous.
+ *   out  [rows, hidden] bf16; must not overlap x (LTXK_ERR_OVERLAP).
+ *   rows >= 0 (0 is a no-op); hidden in [1, LTXK_MAX_HIDDEN];
+ *        rows * hidden <= 2^40.
+ * hidden % 8 == 0 with 16-byte aligned pointers takes the vector kernel.
+ * Reads 4 and writes 2 bytes per output element.
+ */
+LTXK_API int ltxk_geglu(void* out, const void* x, int64_t rows, int64_t hidden,
+                        ltxk_stream_t stream);
+
+/*
  * ltxk_rms_norm_host -- ltxk_rms_norm for x and y in HOST memory, pipelined.
  * The rows are cut into chunks; chunk i is copied in on streams[i % n],
  * normalised in place in staging slot i % n, and copied out, so the copy-in,

@@ -46,7 +46,7 @@ KERNEL_ROWS_TMA = 3
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_adaln", "ltxk_rms_norm_host", "ltxk_add_rms_norm",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
-           "ltxk_rms_norm_noalloc",
+           "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -90,6 +90,10 @@ def _load():
     lib.ltxk_rms_norm_host.restype = I32
     lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
     lib.ltxk_rms_norm_noalloc.restype = I32
+    lib.ltxk_gelu_tanh.argtypes = [P, P, I64, P]
+    lib.ltxk_gelu_tanh.restype = I32
+    lib.ltxk_geglu.argtypes = [P, P, I64, I64, P]
+    lib.ltxk_geglu.restype = I32
     lib.ltxk_fault_status.argtypes = []
     lib.ltxk_fault_status.restype = I32
     lib.ltxk_set_path.argtypes = [I32]
@@ -146,6 +150,14 @@ def ltxk_rms_norm_host(out_host, x_host, w, rows, hidden, eps, staging, staging_
 
 def ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream) -> int:
     return _lib.ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream)
+
+
+def ltxk_gelu_tanh(out, x, n, stream) -> int:
+    return _lib.ltxk_gelu_tanh(out, x, n, stream)
+
+
+def ltxk_geglu(out, x, rows, hidden, stream) -> int:
+    return _lib.ltxk_geglu(out, x, rows, hidden, stream)
 
 
 def ltxk_fault_status() -> int:
@@ -324,3 +336,32 @@ def add_rms_norm(x, residual, weight=None, eps: float = 1e-6, out=None, residual
                            rows, hidden, eps, _stream_handle(x, stream))
     _check(st, "ltxk_add_rms_norm")
     return out, residual_out
+
+
+def gelu_tanh(x, out=None, stream=None):
+    """Tanh-approximated GELU of a bf16 tensor; ``out=x`` works in place."""
+    import torch
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    st = ltxk_gelu_tanh(_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
+                        x.numel(), _stream_handle(x, stream))
+    _check(st, "ltxk_gelu_tanh")
+    return out
+
+
+def geglu(x, out=None, stream=None):
+    """GEGLU over the last axis: ``x[..., :h] * gelu_tanh(x[..., h:])`` with
+    ``h = x.shape[-1] // 2`` (bf16)."""
+    import torch
+    if x.shape[-1] % 2:
+        raise ValueError("last axis of x must be even")
+    hidden = x.shape[-1] // 2
+    rows = x.numel() // x.shape[-1] if hidden else 0
+    if out is None:
+        out = torch.empty(*x.shape[:-1], hidden, dtype=x.dtype, device=x.device)
+    st = ltxk_geglu(_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
+                    rows, hidden, _stream_handle(x, stream))
+    _check(st, "ltxk_geglu")
+    return out

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libltxk.so")
 
 SOURCES = ["ltxk_abi.cu", "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu",
            "ltxk_rows_split.cu", "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu", "ltxk_noalloc.cu",
-           "ltxk_pipeline.cu"]
+           "ltxk_pipeline.cu", "ltxk_gelu.cu"]
 HEADERS = ["ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -74,7 +74,7 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 // Plain RMSNorm: 0 = fewest warps per row; 1 = four warps when a row is
 // exactly 3 or 4 vectors per lane; 2 = any g >= 4 with such an exact fit
 // (measured on GB300: copy speed or better for hidden 3072, 4096, 6144 and
-// 8192, at 16384-65536 rows).
+// 8192, at 16384-65536 rows); 3 = as 2, from g >= 2.
 #ifndef LTXK_PLAIN_SPLIT_RULE
 #define LTXK_PLAIN_SPLIT_RULE 2
 #endif
@@ -200,7 +200,8 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
     // more warps be resident.
     const int64_t nv = hidden / 8;
     for (int g : kGroupChoices) {
-      if (g < 4 || (LTXK_PLAIN_SPLIT_RULE == 1 && g != 4)) continue;
+      if (g < (LTXK_PLAIN_SPLIT_RULE >= 3 ? 2 : 4) || (LTXK_PLAIN_SPLIT_RULE == 1 && g != 4))
+        continue;
       if (nv % (32 * g) != 0) continue;
       const int64_t s = nv / (32 * g);
       if (s == 3 || s == 4) {

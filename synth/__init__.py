@@ -215,13 +215,18 @@ class Case:
     seq_len: int = 0               # positions per batch item (table rows)
     table: str = ""                # "1d" or "3axis"
     meta: dict = field(default_factory=dict)
-    op: str = ""                   # "adaln" for the AdaLN-modulated norm
+    op: str = ""                   # "adaln", "add_norm", "gelu", "geglu"
     weight: bool = True            # False: no weight (ones)
     rows_per_cond: int = 0         # AdaLN: rows sharing one conditioning row
 
     @property
     def elements(self) -> int:
         return self.rows * self.hidden
+
+    @property
+    def in_width(self) -> int:
+        """Elements per input row: 2 * hidden for GEGLU (value, gate)."""
+        return 2 * self.hidden if self.op == "geglu" else self.hidden
 
     @property
     def kind(self) -> str:
@@ -287,6 +292,19 @@ ADD_NORM = [Case(
     name="add_rms_norm_4x4096x3072", rows=4 * 4096, hidden=3072, seed=11,
     x_dist="normal", eps=1e-6, op="add_norm", meta={"shape": [4, 4096, 3072]})]
 
+# Tanh-approximated GELU and GEGLU of an LTX-Video-sized feed-forward block:
+# 2 x 6144 tokens, inner width 4 x 2048 = 8192; pre-activations N(0, 1) with
+# 1 % x50 outliers, which also reach the far negative tail.
+GELU = [Case(
+    name="gelu_tanh_2x6144x8192", rows=2 * 6144, hidden=8192, seed=12,
+    x_dist="normal_outliers", eps=0.0, op="gelu", weight=False,
+    meta={"shape": [2, 6144, 8192]})]
+
+GEGLU = [Case(
+    name="geglu_2x6144x16384", rows=2 * 6144, hidden=8192, seed=13,
+    x_dist="normal_outliers", eps=0.0, op="geglu", weight=False,
+    meta={"shape": [2, 6144, 16384], "out_shape": [2, 6144, 8192]})]
+
 WORKLOADS = {
     "small": SMALL,
     "sweep": SWEEP,
@@ -295,6 +313,8 @@ WORKLOADS = {
     "stress": STRESS,
     "adaln": ADALN,
     "add_norm": ADD_NORM,
+    "gelu": GELU,
+    "geglu": GEGLU,
 }
 
 STREAM_SCALE = 3
@@ -303,7 +323,7 @@ STREAM_RESIDUAL = 5
 
 
 def make_x(case: Case, threads: int | None = None) -> np.ndarray:
-    n = case.elements
+    n = case.rows * case.in_width
     if case.x_dist == "normal":
         x = normal_bf16(case.seed, STREAM_X, n, threads=threads)
     elif case.x_dist == "normal_outliers":
@@ -312,7 +332,7 @@ def make_x(case: Case, threads: int | None = None) -> np.ndarray:
         x = uniform_bf16(case.seed, STREAM_X, n, -4.0, 4.0, threads=threads)
     else:
         raise ValueError(case.x_dist)
-    return x.reshape(case.rows, case.hidden)
+    return x.reshape(case.rows, case.in_width)
 
 
 def make_w(case: Case) -> np.ndarray:
@@ -358,7 +378,12 @@ def make_inputs(case: Case, threads: int | None = None) -> dict:
 def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
     """Bytes one call must move: read x, write y, read w (all bf16), plus the
     fp32 cos/sin tables at their literal size for the fused form, or the
-    bf16 scale and shift for the AdaLN form."""
+    bf16 scale and shift for the AdaLN form.  GELU reads and writes one
+    bf16 per element; GEGLU reads two per output element and writes one."""
+    if case.kind == "gelu":
+        return 4 * case.rows * case.hidden
+    if case.kind == "geglu":
+        return 6 * case.rows * case.hidden
     b = 4 * case.rows * case.hidden + (2 * case.hidden if case.weight else 0)
     if case.kind == "add_norm":
         b += 4 * case.rows * case.hidden          # read the residual, write h

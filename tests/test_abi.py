@@ -270,3 +270,34 @@ def test_add_norm_validation(L):
     assert f(A, D, E, C, D + 8, 4, 8, 1e-6, None) == L.ERR_OVERLAP       # w in residual_out
     st, p = L.ltxk_plan_launch(L.OP_ADD_RMS_NORM, 16384, 3072, 0, 0, True)
     assert st == L.OK and (p.kernel, p.group_warps, p.vec_per_lane) == (1, 4, 4)
+
+
+def test_gelu_validation(L):
+    """Argument errors come back before any CUDA call (fake addresses are
+    never dereferenced; n == 0 launches nothing)."""
+    g = L.ltxk_gelu_tanh
+    assert g(None, B, 16, None) == L.ERR_NULL
+    assert g(A, None, 16, None) == L.ERR_NULL
+    assert g(A, B, -1, None) == L.ERR_SHAPE
+    assert g(A, B, (1 << 40) + 1, None) == L.ERR_SHAPE
+    assert g(A + 1, B, 16, None) == L.ERR_ALIGN
+    assert g(A, B + 1, 16, None) == L.ERR_ALIGN
+    assert g(A, A + 2, 16, None) == L.ERR_OVERLAP
+    assert g(A + 30, A, 16, None) == L.ERR_OVERLAP
+    assert g(A, A, 0, None) == L.OK                       # in place, empty
+    assert g(A, B, 0, None) == L.OK
+
+
+def test_geglu_validation(L):
+    f = L.ltxk_geglu
+    assert f(None, B, 4, 8, None) == L.ERR_NULL
+    assert f(A, None, 4, 8, None) == L.ERR_NULL
+    assert f(A, B, -1, 8, None) == L.ERR_SHAPE
+    assert f(A, B, 4, 0, None) == L.ERR_SHAPE
+    assert f(A, B, 4, (1 << 30) + 1, None) == L.ERR_SHAPE
+    assert f(A, B, (1 << 31) + 1, 1 << 9, None) == L.ERR_SHAPE  # rows * hidden > 2^40
+    assert f(A + 1, B, 4, 8, None) == L.ERR_ALIGN
+    assert f(A, B + 3, 4, 8, None) == L.ERR_ALIGN
+    assert f(A, A, 4, 8, None) == L.ERR_OVERLAP          # out inside x: never in place
+    assert f(A + 120, A, 4, 8, None) == L.ERR_OVERLAP    # last bytes of x
+    assert f(A, B, 0, 8, None) == L.OK
