@@ -7,7 +7,9 @@ the product path: the two share no code.
 
 The arithmetic lives in ``oracle.c`` (plain C, binary64, sequential sums); this
 module only compiles it with gcc and marshals numpy arrays through ctypes.
-bfloat16 tensors travel as ``numpy.uint16`` arrays of bit patterns.
+bfloat16 tensors travel as ``numpy.uint16`` arrays of bit patterns; the row
+operations also take ``numpy.float16`` (IEEE binary16) and ``numpy.float32``
+arrays, the pages' other two precision modes, and answer in the same type.
 
 Definition followed (the pages print no formula; see ``oracle.c`` for the
 page sections cited):
@@ -30,6 +32,11 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 INTERLEAVED = 0
 SPLIT_HALF = 1
+
+# element formats (the codes of oracle.c)
+FMT_BF16, FMT_F16, FMT_F32 = 0, 1, 2
+_FMT_OF_DTYPE = {np.dtype(np.uint16): FMT_BF16, np.dtype(np.float16): FMT_F16,
+                 np.dtype(np.float32): FMT_F32}
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +82,21 @@ def _load():
             lib.oracle_rms_norm_adaln.restype = ctypes.c_int
             lib.oracle_add_rms_norm.argtypes = [P, P, P, P, P, I64, I64, ctypes.c_float, P]
             lib.oracle_add_rms_norm.restype = ctypes.c_int
+            I32, F32 = ctypes.c_int, ctypes.c_float
+            lib.oracle_widen_fmt.argtypes = [I32, P, P, I64]
+            lib.oracle_widen_fmt.restype = None
+            lib.oracle_round_fmt.argtypes = [I32, P, P, I64]
+            lib.oracle_round_fmt.restype = None
+            lib.oracle_rms_norm_fmt.argtypes = [I32, P, P, P, I64, I64, F32, P]
+            lib.oracle_rms_norm_fmt.restype = I32
+            lib.oracle_rms_norm_rope_fmt.argtypes = [I32, P, P, P, P, P, I64, I64, I64, I32,
+                                                     F32, I64, I64, P]
+            lib.oracle_rms_norm_rope_fmt.restype = I32
+            lib.oracle_rms_norm_adaln_fmt.argtypes = [I32, P, P, P, P, P, I64, I64, I64, I64,
+                                                      F32, P]
+            lib.oracle_rms_norm_adaln_fmt.restype = I32
+            lib.oracle_add_rms_norm_fmt.argtypes = [I32, P, P, P, P, P, I64, I64, F32, P]
+            lib.oracle_add_rms_norm_fmt.restype = I32
             lib.oracle_gelu_tanh.argtypes = [P, P, I64, P]
             lib.oracle_gelu_tanh.restype = None
             lib.oracle_geglu.argtypes = [P, P, I64, I64, P]
@@ -92,6 +114,36 @@ def _u16(a, name):
     if a.dtype != np.uint16:
         raise TypeError(f"{name} must hold bfloat16 bit patterns as uint16")
     return a
+
+
+def _elems(a, name, like=None):
+    """(format code, contiguous array) of a bf16 (uint16 bits), float16 or
+    float32 array; with ``like``, the array must have like's dtype."""
+    a = np.ascontiguousarray(a)
+    fmt = _FMT_OF_DTYPE.get(a.dtype)
+    if fmt is None:
+        raise TypeError(f"{name} must be uint16 (bfloat16 bits), float16 or float32")
+    if like is not None and a.dtype != like.dtype:
+        raise TypeError(f"{name} must have the dtype of x ({like.dtype})")
+    return fmt, a
+
+
+def widen(a: np.ndarray) -> np.ndarray:
+    """Exact binary64 values of a bf16 (uint16 bits), float16 or float32 array."""
+    fmt, a = _elems(a, "a")
+    out = np.empty(a.shape, np.float64)
+    _load().oracle_widen_fmt(fmt, _ptr(a), _ptr(out), a.size)
+    return out
+
+
+def round_to(values: np.ndarray, dtype) -> np.ndarray:
+    """Round binary64 values once (RNE) to bf16 (``numpy.uint16`` bits),
+    float16 or float32."""
+    values = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(values.shape, dtype)
+    fmt, out = _elems(out, "dtype")
+    _load().oracle_round_fmt(fmt, _ptr(values), _ptr(out), values.size)
+    return out
 
 
 def widen_bf16(bits: np.ndarray) -> np.ndarray:
@@ -117,17 +169,19 @@ def _row_blocks(rows, threads):
 
 
 def rms_norm(x, w, eps, *, threads: int = 1, exact: bool = False):
-    """Oracle RMSNorm over the last axis of ``x`` (uint16 bf16 bits).
+    """Oracle RMSNorm over the last axis of ``x`` (uint16 bf16 bits, float16
+    or float32; ``w`` of the same dtype).
 
-    Returns the bf16 bit patterns, or ``(bits, exact_values)`` when ``exact``.
+    Returns the rounded values in x's dtype, or ``(values, exact_values)``
+    when ``exact``.
     ``threads`` > 1 runs disjoint row ranges concurrently (ctypes releases the
     GIL during the call); the arithmetic per row is unchanged.
     """
-    x = _u16(x, "x")
+    fmt, x = _elems(x, "x")
     H = x.shape[-1]
     rows = x.size // H if H else 0
     x2 = x.reshape(rows, H)
-    w = None if w is None else _u16(w, "w")
+    w = None if w is None else _elems(w, "w", x)[1]
     if w is not None and w.size != H:
         raise ValueError("w must have hidden elements")
     y = np.empty_like(x2)
@@ -136,8 +190,8 @@ def rms_norm(x, w, eps, *, threads: int = 1, exact: bool = False):
 
     def run(block):
         r0, r1 = block
-        rc = lib.oracle_rms_norm(
-            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), r1 - r0, H,
+        rc = lib.oracle_rms_norm_fmt(
+            fmt, _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), r1 - r0, H,
             ctypes.c_float(eps), None if ye is None else _ptr(ye[r0:r1]))
         if rc != 0:
             raise MemoryError("oracle_rms_norm failed")
@@ -151,17 +205,18 @@ def rms_norm_rope(x, w, cos, sin, heads, head_dim, mode, eps, *,
                   table_rows=None, threads: int = 1, exact: bool = False):
     """Oracle fused RMSNorm + RoPE.
 
-    ``x``: uint16 [rows, heads*head_dim]; ``cos``/``sin``: float32
+    ``x``: [rows, heads*head_dim] (bf16 bits, float16 or float32);
+    ``cos``/``sin``: float32
     [table_rows, head_dim/2]; row r uses table row ``r % table_rows``
     (``table_rows`` defaults to the tables' first dimension).
     """
-    x = _u16(x, "x")
+    fmt, x = _elems(x, "x")
     H = heads * head_dim
     if x.shape[-1] != H:
         raise ValueError("last axis of x must be heads*head_dim")
     rows = x.size // H
     x2 = x.reshape(rows, H)
-    w = None if w is None else _u16(w, "w")
+    w = None if w is None else _elems(w, "w", x)[1]
     cos = np.ascontiguousarray(cos, dtype=np.float32)
     sin = np.ascontiguousarray(sin, dtype=np.float32)
     P = head_dim // 2
@@ -175,8 +230,8 @@ def rms_norm_rope(x, w, cos, sin, heads, head_dim, mode, eps, *,
 
     def run(block):
         r0, r1 = block
-        rc = lib.oracle_rms_norm_rope(
-            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(cos), _ptr(sin),
+        rc = lib.oracle_rms_norm_rope_fmt(
+            fmt, _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(cos), _ptr(sin),
             r1 - r0, heads, head_dim, mode, ctypes.c_float(eps), table_rows,
             r0, None if ye is None else _ptr(ye[r0:r1]))
         if rc != 0:
@@ -191,16 +246,17 @@ def rms_norm_adaln(x, w, scale, shift, eps, *, rows_per_cond=None,
                    threads: int = 1, exact: bool = False):
     """Oracle AdaLN-modulated RMSNorm: norm(x) * w * (1 + scale) + shift.
 
-    ``x``: uint16 [rows, H]; ``scale``/``shift``: uint16 [n_cond, H]; row r
+    ``x``: [rows, H]; ``scale``/``shift``: [n_cond, H], all of one dtype
+    (bf16 bits, float16 or float32); row r
     uses conditioning row ``r // rows_per_cond`` (default: rows / n_cond).
     """
-    x = _u16(x, "x")
+    fmt, x = _elems(x, "x")
     H = x.shape[-1]
     rows = x.size // H
     x2 = x.reshape(rows, H)
-    w = None if w is None else _u16(w, "w")
-    scale = _u16(scale, "scale").reshape(-1, H)
-    shift = _u16(shift, "shift").reshape(-1, H)
+    w = None if w is None else _elems(w, "w", x)[1]
+    scale = _elems(scale, "scale", x)[1].reshape(-1, H)
+    shift = _elems(shift, "shift", x)[1].reshape(-1, H)
     if scale.shape != shift.shape:
         raise ValueError("scale and shift must have the same shape")
     n_cond = scale.shape[0]
@@ -214,8 +270,8 @@ def rms_norm_adaln(x, w, scale, shift, eps, *, rows_per_cond=None,
 
     def run(block):
         r0, r1 = block
-        rc = lib.oracle_rms_norm_adaln(
-            _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(scale), _ptr(shift),
+        rc = lib.oracle_rms_norm_adaln_fmt(
+            fmt, _ptr(y[r0:r1]), _ptr(x2[r0:r1]), _ptr(w), _ptr(scale), _ptr(shift),
             r1 - r0, H, rows_per_cond, r0, ctypes.c_float(eps),
             None if ye is None else _ptr(ye[r0:r1]))
         if rc != 0:
@@ -229,17 +285,17 @@ def rms_norm_adaln(x, w, scale, shift, eps, *, rows_per_cond=None,
 def add_rms_norm(x, res, w, eps, *, threads: int = 1, exact: bool = False):
     """Oracle fused residual add + RMSNorm.
 
-    Returns ``(y, h)`` bf16 bit patterns (``h = bf16(x + res)``, ``y`` the
+    Returns ``(y, h)`` in x's dtype (``h = round(x + res)``, ``y`` the
     RMSNorm of ``h``), or ``(y, h, y_exact)`` when ``exact``.
     """
-    x = _u16(x, "x")
-    res = _u16(res, "res")
+    fmt, x = _elems(x, "x")
+    res = _elems(res, "res", x)[1]
     if x.shape != res.shape:
         raise ValueError("x and res must have the same shape")
     H = x.shape[-1]
     rows = x.size // H if H else 0
     x2, r2 = x.reshape(rows, H), res.reshape(rows, H)
-    w = None if w is None else _u16(w, "w")
+    w = None if w is None else _elems(w, "w", x)[1]
     y = np.empty_like(x2)
     h = np.empty_like(x2)
     ye = np.empty(x2.shape, np.float64) if exact else None
@@ -247,8 +303,8 @@ def add_rms_norm(x, res, w, eps, *, threads: int = 1, exact: bool = False):
 
     def run(block):
         r0, r1 = block
-        rc = lib.oracle_add_rms_norm(
-            _ptr(y[r0:r1]), _ptr(h[r0:r1]), _ptr(x2[r0:r1]), _ptr(r2[r0:r1]), _ptr(w),
+        rc = lib.oracle_add_rms_norm_fmt(
+            fmt, _ptr(y[r0:r1]), _ptr(h[r0:r1]), _ptr(x2[r0:r1]), _ptr(r2[r0:r1]), _ptr(w),
             r1 - r0, H, ctypes.c_float(eps), None if ye is None else _ptr(ye[r0:r1]))
         if rc != 0:
             raise MemoryError("oracle_add_rms_norm failed")

@@ -75,36 +75,94 @@ static double widen_bf16(uint16_t bits) {
     return (double)f;
 }
 
-/* Round a binary64 value straight to bfloat16, round-to-nearest, ties to even,
- * from the IEEE-754 definition (no intermediate binary32 rounding).
+/* ---- element formats ---------------------------------------------------
  *
- * bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits, so a
- * precision of 8 significant bits; normal range starts at 2^-126 and the
- * subnormal spacing is 2^-133.  For |v| in [2^(e-1), 2^e) the spacing of
- * representable values is 2^(e-8); below the normal range it stays 2^-133. */
-static uint16_t round_to_bf16(double v) {
-    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
-    const uint16_t sign = (uint16_t)(signbit(v) ? 0x8000u : 0u);
-    double a = fabs(v);
-    if (a == 0.0) return sign;
-    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+ * "cuda-kernels" skill page, "Supported Data Types": every kernel comes in
+ * three precision modes, __half (IEEE binary16), __nv_bfloat16 and float
+ * (IEEE binary32).  Format codes used below: */
+enum { FMT_BF16 = 0, FMT_F16 = 1, FMT_F32 = 2 };
 
+/* Round a binary64 value to the nearest value of a binary floating-point
+ * format with `prec` significant bits, smallest normal exponent `emin` and
+ * largest exponent `emax`, ties to even, straight from the IEEE-754
+ * definition (no intermediate rounding).  For |v| in [2^(e-1), 2^e) the
+ * spacing of representable values is 2^(e-prec); below 2^emin it stays
+ * 2^(emin-prec+1) (subnormals).  Results beyond the largest finite value
+ * (2 - 2^(1-prec)) * 2^emax become infinities; NaN, zeros and infinities
+ * pass through. */
+static double round_binary(double v, int prec, int emin, int emax) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    const double a = fabs(v);
     int e;
     (void)frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
-    if (e < -125) e = -125;             /* subnormal range: fixed spacing */
-    const double q = ldexp(1.0, e - 8); /* spacing of bf16 values near a */
+    if (e - 1 < emin) e = emin + 1;     /* subnormal range: fixed spacing */
+    const double q = ldexp(1.0, e - prec);
     const double n = a / q;             /* exact: q is a power of two */
     double k = floor(n);
     const double frac = n - k;          /* exact */
     if (frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;
-    const double r = k * q;             /* exact; may reach 2^128 */
+    double r = k * q;                   /* exact */
+    if (r > ldexp(2.0 - ldexp(1.0, 1 - prec), emax)) r = INFINITY;
+    return signbit(v) ? -r : r;
+}
 
-    /* r is exactly representable in bfloat16 (or is 2^128, which becomes
-     * +inf in binary32), so encoding through binary32 loses nothing. */
-    const float rf = (float)r;
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits, so 8
+ * significant bits; normal range from 2^-126, subnormal spacing 2^-133.
+ * The rounded value is exactly representable in binary32 (or infinite), so
+ * its encoding is the top half of the binary32 encoding. */
+static uint16_t round_to_bf16(double v) {
+    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
+    const float rf = (float)round_binary(v, 8, -126, 127);
     uint32_t u;
     memcpy(&u, &rf, sizeof u);
-    return (uint16_t)(sign | (uint16_t)(u >> 16));
+    return (uint16_t)(u >> 16);
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits:
+ * 11 significant bits, normal range 2^-14 .. 65504, subnormal spacing 2^-24. */
+static double widen_f16(uint16_t bits) {
+    const int E = (bits >> 10) & 31;
+    const int M = bits & 1023;
+    double v;
+    if (E == 0) v = ldexp((double)M, -24);
+    else if (E == 31) v = M ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + M), E - 25);
+    return (bits & 0x8000u) ? -v : v;
+}
+
+static uint16_t round_to_f16(double v) {
+    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFE00u : 0x7E00u);
+    const double r = round_binary(v, 11, -14, 15);
+    const uint16_t sign = (uint16_t)(signbit(r) ? 0x8000u : 0u);
+    const double a = fabs(r);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+    if (a < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)(a * 16777216.0)); /* a / 2^-24 */
+    int e;
+    const double m = frexp(a, &e);      /* a = m * 2^e, m in [0.5, 1) */
+    const int E = e - 1 + 15;
+    const int M = (int)(m * 2048.0) - 1024;
+    return (uint16_t)(sign | (uint16_t)(E << 10) | (uint16_t)M);
+}
+
+/* IEEE binary32: 24 significant bits, normal range from 2^-126, subnormal
+ * spacing 2^-149.  The rounded value converts to float exactly. */
+static float round_to_f32(double v) {
+    if (isnan(v)) return signbit(v) ? -NAN : NAN;
+    return (float)round_binary(v, 24, -126, 127);
+}
+
+/* Element i of an array in format fmt, exactly, as binary64. */
+static double load_elem(int fmt, const void* p, int64_t i) {
+    if (fmt == FMT_F32) return (double)((const float*)p)[i];
+    const uint16_t b = ((const uint16_t*)p)[i];
+    return fmt == FMT_F16 ? widen_f16(b) : widen_bf16(b);
+}
+
+/* Store v into element i of an array in format fmt, rounded once (RNE). */
+static void store_elem(int fmt, void* p, int64_t i, double v) {
+    if (fmt == FMT_F32) ((float*)p)[i] = round_to_f32(v);
+    else if (fmt == FMT_F16) ((uint16_t*)p)[i] = round_to_f16(v);
+    else ((uint16_t*)p)[i] = round_to_bf16(v);
 }
 
 /* ---- element conversions, exported for the pins ------------------------ */
@@ -117,58 +175,76 @@ void oracle_round_bf16(const double* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = round_to_bf16(in[i]);
 }
 
+/* Widen / round n elements of format fmt (for the pins). */
+void oracle_widen_fmt(int fmt, const void* in, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = load_elem(fmt, in, i);
+}
+
+void oracle_round_fmt(int fmt, const double* in, void* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) store_elem(fmt, out, i, in[i]);
+}
+
 /* ---- RMSNorm ----------------------------------------------------------- */
 
-/* Normalise one row of H values into n[0..H).  w == NULL means all ones. */
-static void normalise_row(const uint16_t* xr, const uint16_t* w, int64_t H,
+/* Normalise row r of x [.., H] (format fmt) into n[0..H).  w == NULL means
+ * all ones. */
+static void normalise_row(int fmt, const void* x, int64_t r, const void* w, int64_t H,
                           float eps, double* n) {
     double ss = 0.0;
     for (int64_t j = 0; j < H; ++j) {
-        const double v = widen_bf16(xr[j]);
+        const double v = load_elem(fmt, x, r * H + j);
         ss += v * v;
     }
     const double ms = ss / (double)H;
     const double denom = sqrt(ms + (double)eps);
     for (int64_t j = 0; j < H; ++j) {
-        const double wj = w ? widen_bf16(w[j]) : 1.0;
-        n[j] = widen_bf16(xr[j]) * wj / denom;
+        const double wj = w ? load_elem(fmt, w, j) : 1.0;
+        n[j] = load_elem(fmt, x, r * H + j) * wj / denom;
     }
 }
 
-/* y[r, j] = bf16( x[r, j] * w[j] / sqrt(mean_j x[r, j]^2 + eps) ).
+/* y[r, j] = round( x[r, j] * w[j] / sqrt(mean_j x[r, j]^2 + eps) ).
  *
- * x, y: row-major [rows, H] bfloat16 bit patterns.  w: [H] or NULL (ones).
+ * x, y: row-major [rows, H] in format fmt.  w: [H] or NULL (ones).
  * y_exact: optional [rows, H] binary64 copy of the values before rounding.
- * Returns 0, or -1 if scratch memory could not be allocated. */
-int oracle_rms_norm(uint16_t* y, const uint16_t* x, const uint16_t* w,
-                    int64_t rows, int64_t H, float eps, double* y_exact) {
+ * Returns 0, -1 if scratch memory could not be allocated, -2 for an unknown
+ * format. */
+int oracle_rms_norm_fmt(int fmt, void* y, const void* x, const void* w,
+                        int64_t rows, int64_t H, float eps, double* y_exact) {
+    if (fmt < FMT_BF16 || fmt > FMT_F32) return -2;
     double* n = (double*)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
     if (!n) return -1;
     for (int64_t r = 0; r < rows; ++r) {
-        normalise_row(x + r * H, w, H, eps, n);
+        normalise_row(fmt, x, r, w, H, eps, n);
         for (int64_t j = 0; j < H; ++j) {
             if (y_exact) y_exact[r * H + j] = n[j];
-            y[r * H + j] = round_to_bf16(n[j]);
+            store_elem(fmt, y, r * H + j, n[j]);
         }
     }
     free(n);
     return 0;
 }
 
+int oracle_rms_norm(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                    int64_t rows, int64_t H, float eps, double* y_exact) {
+    return oracle_rms_norm_fmt(FMT_BF16, y, x, w, rows, H, eps, y_exact);
+}
+
 /* Fused RMSNorm then RoPE.
  *
- * x, y: row-major [rows, heads*head_dim].  w: [heads*head_dim] or NULL.
- * cos_t, sin_t: binary32 tables [table_rows, head_dim/2]; row r of x (counted
- * from first_row, the global index of the first row passed) uses table row
- * ((first_row + r) mod table_rows), i.e. x is [batch, table_rows, hidden]
- * with the sequence position as the inner row index.
+ * x, y: row-major [rows, heads*head_dim] in format fmt.  w: [heads*head_dim]
+ * or NULL.  cos_t, sin_t: binary32 tables [table_rows, head_dim/2]; row r of
+ * x (counted from first_row, the global index of the first row passed) uses
+ * table row ((first_row + r) mod table_rows), i.e. x is [batch, table_rows,
+ * hidden] with the sequence position as the inner row index.
  * mode 0 pairs (2p, 2p+1) inside each head; mode 1 pairs (p, p + head_dim/2).
  * Returns 0; -1 on allocation failure; -2 on an invalid argument. */
-int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
-                         const float* cos_t, const float* sin_t,
-                         int64_t rows, int64_t heads, int64_t head_dim,
-                         int mode, float eps, int64_t table_rows,
-                         int64_t first_row, double* y_exact) {
+int oracle_rms_norm_rope_fmt(int fmt, void* y, const void* x, const void* w,
+                             const float* cos_t, const float* sin_t,
+                             int64_t rows, int64_t heads, int64_t head_dim,
+                             int mode, float eps, int64_t table_rows,
+                             int64_t first_row, double* y_exact) {
+    if (fmt < FMT_BF16 || fmt > FMT_F32) return -2;
     if (head_dim <= 0 || head_dim % 2 != 0 || heads <= 0 || table_rows <= 0 ||
         first_row < 0)
         return -2;
@@ -180,7 +256,7 @@ int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
     if (!n || !o) { free(n); free(o); return -1; }
 
     for (int64_t r = 0; r < rows; ++r) {
-        normalise_row(x + r * H, w, H, eps, n);
+        normalise_row(fmt, x, r, w, H, eps, n);
         const int64_t pos = (first_row + r) % table_rows;
         for (int64_t h = 0; h < heads; ++h) {
             for (int64_t p = 0; p < P; ++p) {
@@ -197,7 +273,7 @@ int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
         }
         for (int64_t j = 0; j < H; ++j) {
             if (y_exact) y_exact[r * H + j] = o[j];
-            y[r * H + j] = round_to_bf16(o[j]);
+            store_elem(fmt, y, r * H + j, o[j]);
         }
     }
     free(n);
@@ -205,56 +281,82 @@ int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
     return 0;
 }
 
+int oracle_rms_norm_rope(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                         const float* cos_t, const float* sin_t,
+                         int64_t rows, int64_t heads, int64_t head_dim,
+                         int mode, float eps, int64_t table_rows,
+                         int64_t first_row, double* y_exact) {
+    return oracle_rms_norm_rope_fmt(FMT_BF16, y, x, w, cos_t, sin_t, rows, heads, head_dim,
+                                    mode, eps, table_rows, first_row, y_exact);
+}
+
 /* AdaLN-modulated RMSNorm:
- *   y[r, j] = bf16( n[r, j] * (1 + scale[c, j]) + shift[c, j] ),
+ *   y[r, j] = round( n[r, j] * (1 + scale[c, j]) + shift[c, j] ),
  *   n = the RMSNorm above (with w, or ones when w == NULL),
  *   c = r / rows_per_cond (x is [n_cond, rows_per_cond, H]).
- * scale, shift: bfloat16 [n_cond, H].  first_row is the global index of the
- * first row passed, so that row blocks keep their conditioning row.
- * Returns 0; -1 on allocation failure; -2 on an invalid argument. */
-int oracle_rms_norm_adaln(uint16_t* y, const uint16_t* x, const uint16_t* w,
-                          const uint16_t* scale, const uint16_t* shift,
-                          int64_t rows, int64_t H, int64_t rows_per_cond,
-                          int64_t first_row, float eps, double* y_exact) {
+ * scale, shift: [n_cond, H] in the format of x.  first_row is the global
+ * index of the first row passed, so that row blocks keep their conditioning
+ * row.  Returns 0; -1 on allocation failure; -2 on an invalid argument. */
+int oracle_rms_norm_adaln_fmt(int fmt, void* y, const void* x, const void* w,
+                              const void* scale, const void* shift,
+                              int64_t rows, int64_t H, int64_t rows_per_cond,
+                              int64_t first_row, float eps, double* y_exact) {
+    if (fmt < FMT_BF16 || fmt > FMT_F32) return -2;
     if (H <= 0 || rows_per_cond <= 0 || first_row < 0) return -2;
     double* n = (double*)malloc((size_t)H * sizeof(double));
     if (!n) return -1;
     for (int64_t r = 0; r < rows; ++r) {
-        normalise_row(x + r * H, w, H, eps, n);
+        normalise_row(fmt, x, r, w, H, eps, n);
         const int64_t c = (first_row + r) / rows_per_cond;
         for (int64_t j = 0; j < H; ++j) {
-            const double sc = widen_bf16(scale[c * H + j]);
-            const double sh = widen_bf16(shift[c * H + j]);
+            const double sc = load_elem(fmt, scale, c * H + j);
+            const double sh = load_elem(fmt, shift, c * H + j);
             const double v = n[j] * (1.0 + sc) + sh;
             if (y_exact) y_exact[r * H + j] = v;
-            y[r * H + j] = round_to_bf16(v);
+            store_elem(fmt, y, r * H + j, v);
         }
     }
     free(n);
     return 0;
 }
 
+int oracle_rms_norm_adaln(uint16_t* y, const uint16_t* x, const uint16_t* w,
+                          const uint16_t* scale, const uint16_t* shift,
+                          int64_t rows, int64_t H, int64_t rows_per_cond,
+                          int64_t first_row, float eps, double* y_exact) {
+    return oracle_rms_norm_adaln_fmt(FMT_BF16, y, x, w, scale, shift, rows, H, rows_per_cond,
+                                     first_row, eps, y_exact);
+}
+
 /* Fused residual add + RMSNorm:
- *   h[r, j] = bf16( x[r, j] + res[r, j] )        (the new residual stream)
- *   y[r, j] = bf16( h[r, j] * w[j] / sqrt(mean_j h[r, j]^2 + eps) )
- * x, res, h, y: row-major [rows, H] bf16.  w: [H] or NULL.
- * Returns 0, or -1 on allocation failure. */
-int oracle_add_rms_norm(uint16_t* y, uint16_t* h, const uint16_t* x,
-                        const uint16_t* res, const uint16_t* w, int64_t rows,
-                        int64_t H, float eps, double* y_exact) {
+ *   h[r, j] = round( x[r, j] + res[r, j] )        (the new residual stream)
+ *   y[r, j] = round( h[r, j] * w[j] / sqrt(mean_j h[r, j]^2 + eps) )
+ * x, res, h, y: row-major [rows, H] in format fmt.  w: [H] or NULL.
+ * Returns 0, -1 on allocation failure, -2 for an unknown format. */
+int oracle_add_rms_norm_fmt(int fmt, void* y, void* h, const void* x, const void* res,
+                            const void* w, int64_t rows, int64_t H, float eps,
+                            double* y_exact) {
+    if (fmt < FMT_BF16 || fmt > FMT_F32) return -2;
     double* n = (double*)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
     if (!n) return -1;
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t j = 0; j < H; ++j)
-            h[r * H + j] = round_to_bf16(widen_bf16(x[r * H + j]) + widen_bf16(res[r * H + j]));
-        normalise_row(h + r * H, w, H, eps, n);
+            store_elem(fmt, h, r * H + j,
+                       load_elem(fmt, x, r * H + j) + load_elem(fmt, res, r * H + j));
+        normalise_row(fmt, h, r, w, H, eps, n);
         for (int64_t j = 0; j < H; ++j) {
             if (y_exact) y_exact[r * H + j] = n[j];
-            y[r * H + j] = round_to_bf16(n[j]);
+            store_elem(fmt, y, r * H + j, n[j]);
         }
     }
     free(n);
     return 0;
+}
+
+int oracle_add_rms_norm(uint16_t* y, uint16_t* h, const uint16_t* x,
+                        const uint16_t* res, const uint16_t* w, int64_t rows,
+                        int64_t H, float eps, double* y_exact) {
+    return oracle_add_rms_norm_fmt(FMT_BF16, y, h, x, res, w, rows, H, eps, y_exact);
 }
 
 /* tanh-approximated GELU of one value, binary64. */

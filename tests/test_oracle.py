@@ -541,3 +541,142 @@ def test_geglu_value_times_gelu_of_gate(oracle_mod):
     big = np.concatenate([x[:, :h], bits_of(np.full((rows, h), 16.0))], axis=1)
     np.testing.assert_array_equal(oracle_mod.geglu(big),
                                   oracle_mod.round_bf16(oracle_mod.widen_bf16(x[:, :h]) * 16))
+
+
+# ---- the other two precision modes ("cuda-kernels" page, "Supported Data
+# Types": __half, __nv_bfloat16 and float) --------------------------------
+
+ALL16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+def test_f16_widen_all_patterns(oracle_mod):
+    """Every binary16 pattern decodes to numpy's own binary16 value."""
+    h = ALL16.view(np.float16)
+    got = oracle_mod.widen(h)
+    ref = h.astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_f16_round_identity_and_midpoints(oracle_mod):
+    h = ALL16.view(np.float16)
+    fin = np.isfinite(h)
+    back = oracle_mod.round_to(h[fin].astype(np.float64), np.float16).view(np.uint16)
+    assert np.array_equal(back, ALL16[fin])
+    # the midpoint of two neighbours (exact in binary64) goes to the even one;
+    # a hair either side goes to the nearer one
+    pos = np.arange(0, 0x7C00, dtype=np.uint16)
+    lo = pos[:-1].view(np.float16).astype(np.float64)
+    hi = pos[1:].view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2
+    even = np.where(pos[:-1] % 2 == 0, pos[:-1], pos[1:])
+    assert np.array_equal(oracle_mod.round_to(mid, np.float16).view(np.uint16), even)
+    assert np.array_equal(oracle_mod.round_to(-mid, np.float16).view(np.uint16), even | 0x8000)
+    eps = (hi - lo) * 2.0 ** -20
+    assert np.array_equal(oracle_mod.round_to(mid - eps, np.float16).view(np.uint16), pos[:-1])
+    assert np.array_equal(oracle_mod.round_to(mid + eps, np.float16).view(np.uint16), pos[1:])
+
+
+def test_f16_round_specials(oracle_mod):
+    v = np.array([65504.0, 65519.99, 65520.0, -65520.0, 1e300, np.inf, -np.inf, 0.0, -0.0,
+                  2.0 ** -25, 2.0 ** -25 * 1.0001, 2.0 ** -24, 3 * 2.0 ** -26, 2.0 ** -14])
+    got = oracle_mod.round_to(v, np.float16).view(np.uint16)
+    assert list(got) == [0x7BFF, 0x7BFF, 0x7C00, 0xFC00, 0x7C00, 0x7C00, 0xFC00, 0x0000, 0x8000,
+                         0x0000, 0x0001, 0x0001, 0x0001, 0x0400]
+    assert np.isnan(oracle_mod.round_to(np.array([np.nan]), np.float16)[0])
+
+
+def test_f16_round_matches_numpy_conversion(oracle_mod):
+    """numpy converts binary64 to binary16 with its own round-to-nearest-even."""
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(200000) * np.exp2(rng.uniform(-30, 17, 200000))
+    got = oracle_mod.round_to(v, np.float16)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16)
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+
+
+def test_f32_round_matches_hardware_conversion(oracle_mod):
+    """The host's binary64 -> binary32 conversion (round to nearest even) is
+    an independent implementation of the same rounding."""
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal(200000) * np.exp2(rng.uniform(-155, 130, 200000))
+    # exact midpoints between binary32 neighbours, subnormal ones included
+    f = (rng.integers(1, 0x7F7FFFFF, 100000, dtype=np.uint64).astype(np.uint32)).view(np.float32)
+    nxt = np.nextafter(f, np.float32(np.inf))
+    mids = (f.astype(np.float64) + nxt.astype(np.float64)) / 2
+    for vals in (v, mids, -mids):
+        got = oracle_mod.round_to(vals, np.float32)
+        with np.errstate(over="ignore"):
+            ref = vals.astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    big = np.float64(np.finfo(np.float32).max)
+    half_ulp = 2.0 ** 103
+    got = oracle_mod.round_to(np.array([big + half_ulp * 0.999, big + half_ulp]), np.float32)
+    assert got[0] == np.finfo(np.float32).max and np.isinf(got[1])
+
+
+def _shared_values(seed, rows, H):
+    """Values exactly representable in bf16, binary16 and binary32: 8
+    significant bits, magnitudes within binary16's normal range."""
+    x = synth.uniform_bf16(seed, 0, rows * H, -4.0, 4.0).reshape(rows, H)
+    xf = synth.bf16_bits_to_f32(x)
+    xf = np.where(np.abs(xf) < 2.0 ** -13, 0.0, xf).astype(np.float32)
+    return synth.to_bf16_bits(xf), xf
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_formats_share_the_arithmetic(oracle_mod, dtype):
+    """Inputs that every format holds exactly give the same exact results in
+    every format, and each output is that format's rounding of them."""
+    xb, xf = _shared_values(21, 6, 32)
+    wb, wf = _shared_values(22, 1, 32)
+    wb, wf = wb[0], wf[0]
+    cast = (lambda a: a.astype(dtype))
+    _, e_b = oracle_mod.rms_norm(xb, wb, 1e-6, exact=True)
+    y, e = oracle_mod.rms_norm(cast(xf), cast(wf), 1e-6, exact=True)
+    bits = (lambda a: a.view(np.uint16 if dtype == np.float16 else np.uint32))
+    assert y.dtype == dtype and np.array_equal(e, e_b)
+    assert np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+    c, s = synth.rope_table_1d(6, 8)
+    for mode in (0, 1):
+        _, e_b = oracle_mod.rms_norm_rope(xb, wb, c, s, 4, 8, mode, 1e-6, exact=True)
+        y, e = oracle_mod.rms_norm_rope(cast(xf), cast(wf), c, s, 4, 8, mode, 1e-6, exact=True)
+        assert np.array_equal(e, e_b) and np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+    sb, sf = _shared_values(23, 2, 32)
+    tb, tf = _shared_values(24, 2, 32)
+    _, e_b = oracle_mod.rms_norm_adaln(xb, wb, sb, tb, 1e-6, rows_per_cond=3, exact=True)
+    y, e = oracle_mod.rms_norm_adaln(cast(xf), cast(wf), cast(sf), cast(tf), 1e-6,
+                                     rows_per_cond=3, exact=True)
+    assert np.array_equal(e, e_b) and np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+    rb, rf = _shared_values(25, 6, 32)
+    y, h, e = oracle_mod.add_rms_norm(cast(xf), cast(rf), cast(wf), 1e-6, exact=True)
+    assert np.array_equal(bits(h), bits(oracle_mod.round_to(xf.astype(np.float64) + rf, dtype)))
+    _, e_h = oracle_mod.rms_norm(h, cast(wf), 1e-6, exact=True)
+    assert np.array_equal(e, e_h) and np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_formats_match_torch_rms_norm_fp64(oracle_mod, dtype):
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((8, 3072)) * 3).astype(dtype)
+    w = (1 + 0.1 * rng.standard_normal(3072)).astype(dtype)
+    _, ye = oracle_mod.rms_norm(x, w, 1e-6, exact=True)
+    ref = F.rms_norm(torch.from_numpy(x.astype(np.float64)), (3072,),
+                     torch.from_numpy(w.astype(np.float64)),
+                     eps=float(np.float32(1e-6))).numpy()
+    np.testing.assert_allclose(ye, ref, rtol=1e-12, atol=1e-300)
+
+
+def test_formats_reject_mixed_dtypes(oracle_mod):
+    x = np.zeros((2, 8), np.float16)
+    with pytest.raises(TypeError):
+        oracle_mod.rms_norm(x, np.ones(8, np.float32), 1e-6)
+    with pytest.raises(TypeError):
+        oracle_mod.rms_norm(x.astype(np.float64), None, 1e-6)

@@ -7,6 +7,7 @@ import importlib.util
 import os
 import shutil
 
+import numpy as np
 import pytest
 
 import test_oracle as pins
@@ -19,8 +20,9 @@ MUTANTS = [
     ("eps_outside_root", "sqrt(ms + (double)eps)", "(sqrt(ms) + (double)eps)"),
     ("mean_over_h_minus_1", "ss / (double)H", "ss / (double)(H - 1)"),
     ("sum_not_mean", "ss / (double)H", "ss"),
-    ("weight_ignored", "w ? widen_bf16(w[j]) : 1.0", "1.0"),
-    ("weight_divides", "widen_bf16(xr[j]) * wj / denom", "widen_bf16(xr[j]) / wj / denom"),
+    ("weight_ignored", "w ? load_elem(fmt, w, j) : 1.0", "1.0"),
+    ("weight_divides", "load_elem(fmt, x, r * H + j) * wj / denom",
+     "load_elem(fmt, x, r * H + j) / wj / denom"),
     ("rope_sign_a", "o[ia] = a * c - b * s;", "o[ia] = a * c + b * s;"),
     ("rope_sign_b", "o[ib] = a * s + b * c;", "o[ib] = b * c - a * s;"),
     ("rope_cos_sin_swapped", "o[ib] = a * s + b * c;", "o[ib] = a * c + b * s;"),
@@ -35,23 +37,36 @@ MUTANTS = [
      "frac >= 0.5"),
     ("round_truncates", "if (frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;",
      ""),
-    ("subnormal_spacing", "if (e < -125) e = -125;", "if (e < -126) e = -126;"),
-    ("precision_9_bits", "ldexp(1.0, e - 8)", "ldexp(1.0, e - 9)"),
+    ("subnormal_spacing", "if (e - 1 < emin) e = emin + 1;", "if (e < emin) e = emin;"),
+    ("precision_plus_one_bit", "ldexp(1.0, e - prec)", "ldexp(1.0, e - prec - 1)"),
     ("adaln_scale_not_plus_one", "n[j] * (1.0 + sc) + sh", "n[j] * sc + sh"),
     ("adaln_shift_subtracted", "n[j] * (1.0 + sc) + sh", "n[j] * (1.0 + sc) - sh"),
     ("adaln_scale_shift_swapped", "n[j] * (1.0 + sc) + sh", "n[j] * (1.0 + sh) + sc"),
     ("adaln_cond_ignores_first_row", "(first_row + r) / rows_per_cond", "r / rows_per_cond"),
     ("adaln_cond_modulo", "(first_row + r) / rows_per_cond", "(first_row + r) % rows_per_cond"),
-    ("add_norm_of_x", "normalise_row(h + r * H, w, H, eps, n);",
-     "normalise_row(x + r * H, w, H, eps, n);"),
-    ("add_subtracts", "widen_bf16(x[r * H + j]) + widen_bf16(res[r * H + j])",
-     "widen_bf16(x[r * H + j]) - widen_bf16(res[r * H + j])"),
+    ("add_norm_of_x", "normalise_row(fmt, h, r, w, H, eps, n);",
+     "normalise_row(fmt, x, r, w, H, eps, n);"),
+    ("add_subtracts", "load_elem(fmt, x, r * H + j) + load_elem(fmt, res, r * H + j)",
+     "load_elem(fmt, x, r * H + j) - load_elem(fmt, res, r * H + j)"),
     ("gelu_cubic_coefficient", "0.044715 * x * x * x", "0.0447 * x * x * x"),
     ("gelu_exp_sign", "x / (1.0 + exp(-2.0 * z))", "x / (1.0 + exp(2.0 * z))"),
     ("gelu_half_scale", "sqrt(2.0 / M_PI)", "sqrt(1.0 / M_PI)"),
     ("geglu_halves_swapped",
      "widen_bf16(x[r * 2 * h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + h + j]))",
      "widen_bf16(x[r * 2 * h + h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + j]))"),
+    ("overflow_kept_finite", "if (r > ldexp(2.0 - ldexp(1.0, 1 - prec), emax)) r = INFINITY;", ""),
+    ("f16_exponent_bias", "ldexp((double)(1024 + M), E - 25)", "ldexp((double)(1024 + M), E - 24)"),
+    ("f16_subnormal_scale", "v = ldexp((double)M, -24)", "v = ldexp((double)M, -25)"),
+    ("f16_round_10_bits", "round_binary(v, 11, -14, 15)", "round_binary(v, 10, -14, 15)"),
+    ("f16_round_emin", "round_binary(v, 11, -14, 15)", "round_binary(v, 11, -15, 15)"),
+    ("f16_round_emax", "round_binary(v, 11, -14, 15)", "round_binary(v, 11, -14, 16)"),
+    ("f16_encode_mantissa", "(int)(m * 2048.0) - 1024", "(int)(m * 2048.0) - 1023"),
+    ("f32_round_23_bits", "round_binary(v, 24, -126, 127)", "round_binary(v, 23, -126, 127)"),
+    ("f32_round_emin", "round_binary(v, 24, -126, 127)", "round_binary(v, 24, -125, 127)"),
+    ("f16_read_as_bf16", "return fmt == FMT_F16 ? widen_f16(b) : widen_bf16(b);",
+     "return widen_bf16(b);"),
+    ("f32_stored_as_f16", "if (fmt == FMT_F32) ((float*)p)[i] = round_to_f32(v);",
+     "if (fmt == FMT_F32) ((float*)p)[i] = (float)widen_f16(round_to_f16(v));"),
 ]
 
 
@@ -93,6 +108,15 @@ def _pin_calls():
         ("gelu_torch", pins.test_gelu_matches_tanh_form_and_torch, ()),
         ("gelu_tails", pins.test_gelu_tails, ()),
         ("geglu", pins.test_geglu_value_times_gelu_of_gate, ()),
+        ("f16_widen", pins.test_f16_widen_all_patterns, ()),
+        ("f16_midpoints", pins.test_f16_round_identity_and_midpoints, ()),
+        ("f16_specials", pins.test_f16_round_specials, ()),
+        ("f16_numpy", pins.test_f16_round_matches_numpy_conversion, ()),
+        ("f32_hw", pins.test_f32_round_matches_hardware_conversion, ()),
+        ("fmt_shared_f16", pins.test_formats_share_the_arithmetic, (np.float16,)),
+        ("fmt_shared_f32", pins.test_formats_share_the_arithmetic, (np.float32,)),
+        ("fmt_torch_f16", pins.test_formats_match_torch_rms_norm_fp64, (np.float16,)),
+        ("fmt_torch_f32", pins.test_formats_match_torch_rms_norm_fp64, (np.float32,)),
     ]
     return calls
 
