@@ -56,6 +56,10 @@ WORKLOAD_TITLES = {
              "no weight, scale/shift [2, 2048] ~ N(0, 0.5), seed 10",
     "add_norm": "fused residual add + RMSNorm, h = x + residual, y = RMSNorm(h), "
                 "[4, 4096, 3072], x, residual ~ N(0,1), w ~ N(1,0.1), seed 11",
+    "f16": "fp16 RMSNorm [4x4096x3072], N(0,1) with 1% x50 outliers, w ~ N(1,0.1), "
+           "eps 1e-6, seed 14",
+    "f32": "fp32 RMSNorm [4x4096x3072], N(0,1) with 1% x50 outliers, w ~ N(1,0.1), "
+           "eps 1e-6, seed 15",
     "gelu": "tanh-approximated GELU, x [2, 6144, 8192] (LTX-Video feed-forward inner "
             "width), N(0,1) with 1% x50 outliers, seed 12",
     "geglu": "GEGLU value * gelu_tanh(gate), x [2, 6144, 2x8192] -> [2, 6144, 8192], "
@@ -262,10 +266,11 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         if c.kind in ("gelu", "geglu"):
             b += (4 if c.kind == "gelu" else 6) * r * c.hidden
             continue
-        b += 4 * r * c.hidden + (2 * c.hidden if inp["w"] is not None else 0) + (
+        e = inp["x"].dtype.itemsize
+        b += 2 * e * r * c.hidden + (e * c.hidden if inp["w"] is not None else 0) + (
             8 * min(r, c.seq_len) * (c.head_dim // 2) if c.mode is not None else 0) + (
-            4 * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0) + (
-            4 * r * c.hidden if c.kind == "add_norm" else 0)
+            2 * e * (-(-r // c.rows_per_cond)) * c.hidden if c.kind == "adaln" else 0) + (
+            2 * e * r * c.hidden if c.kind == "add_norm" else 0)
     return t, b
 
 
@@ -327,16 +332,27 @@ def run_reference(args, cases, inputs, world, rank):
 
 # ------------------------------------------------------------- GPU timing --
 
-def kernel_name(plan, mode):
+DTYPE_CODES = {"bf16": 0, "f16": 1, "f32": 2}
+
+
+def kernel_name(plan, mode, dtype="bf16"):
     """Kernel instance name as ncu prints it; mode None = plain, 0/1 = RoPE
-    pairing, 3 = AdaLN, 4 = residual add + RMSNorm."""
+    pairing, 3 = AdaLN, 4 = residual add + RMSNorm; the last template
+    argument is the element format (0 bf16, 1 fp16, 2 fp32)."""
     import rope_element_dit_gb300 as L
     km = 0 if mode is None else {0: 1, 1: 2, 3: 3, 4: 4}[mode]
+    f = DTYPE_CODES[dtype]
     if plan.kernel == L.KERNEL_ROWS_VEC:
-        return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}>"
+        return f"rows_vec_kernel<{km}, {plan.group_warps}, {plan.vec_per_lane}, {f}>"
     if plan.kernel == L.KERNEL_ROWS_TMA:
         return f"rows_tma_kernel<{km}, {plan.vec_per_lane}>"
-    return f"rows_elem_kernel<{km}>"
+    return f"rows_elem_kernel<{km}, {f}>"
+
+
+def _tensor(a):
+    """torch view of a generated array (bf16 bit patterns travel as int16)."""
+    import torch
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
 
 
 def run_ltxk(args, cases, inputs, world, rank, local):
@@ -355,16 +371,16 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     # resident inputs and outputs
     dev_bufs = []
     for c, inp in zip(cases, inputs):
-        d = {"x": torch.from_numpy(inp["x"].view(np.int16)).to(dev),
-             "w": (None if inp["w"] is None
-                   else torch.from_numpy(inp["w"].view(np.int16)).to(dev)),
-             "y": torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)}
+        xt = _tensor(inp["x"])
+        d = {"x": xt.to(dev),
+             "w": None if inp["w"] is None else _tensor(inp["w"]).to(dev),
+             "y": torch.empty(c.rows * c.hidden, dtype=xt.dtype, device=dev)}
         if c.kind == "add_norm":
-            d["res"] = torch.from_numpy(inp["res"].view(np.int16)).to(dev)
-            d["h"] = torch.empty(c.rows * c.hidden, dtype=torch.int16, device=dev)
+            d["res"] = _tensor(inp["res"]).to(dev)
+            d["h"] = torch.empty(c.rows * c.hidden, dtype=xt.dtype, device=dev)
         if c.kind == "adaln":
-            d["scale"] = torch.from_numpy(inp["scale"].view(np.int16)).to(dev)
-            d["shift"] = torch.from_numpy(inp["shift"].view(np.int16)).to(dev)
+            d["scale"] = _tensor(inp["scale"]).to(dev)
+            d["shift"] = _tensor(inp["shift"]).to(dev)
         if c.mode is not None:
             d["cos"] = torch.from_numpy(inp["cos"]).to(dev)
             d["sin"] = torch.from_numpy(inp["sin"]).to(dev)
@@ -386,6 +402,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             return L.ltxk_rms_norm_adaln, (
                 d["y"].data_ptr(), x.data_ptr(), wp, d["scale"].data_ptr(),
                 d["shift"].data_ptr(), c.rows, c.hidden, c.rows_per_cond, c.eps, sptr)
+        if c.mode is None and c.dtype != "bf16":
+            return L.ltxk_rms_norm_dt, (d["y"].data_ptr(), x.data_ptr(), wp, c.rows, c.hidden,
+                                        c.eps, DTYPE_CODES[c.dtype], sptr)
         if c.mode is None:
             return L.ltxk_rms_norm, (d["y"].data_ptr(), x.data_ptr(), wp,
                                      c.rows, c.hidden, c.eps, sptr)
@@ -426,8 +445,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             continue
         op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
               "adaln": L.OP_RMS_NORM_ADALN, "add_norm": L.OP_ADD_RMS_NORM}[c.kind]
-        st, p = L.ltxk_plan_launch(op, c.rows, c.hidden, c.head_dim, c.mode or 0, True)
-        plans.append(kernel_name(p, {"adaln": 3, "add_norm": 4}.get(c.kind, c.mode)))
+        st, p = L.ltxk_plan_launch_dt(op, DTYPE_CODES[c.dtype], c.rows, c.hidden, c.head_dim,
+                                      c.mode or 0, True)
+        plans.append(kernel_name(p, {"adaln": 3, "add_norm": 4}.get(c.kind, c.mode), c.dtype))
 
     for i in range(args.warmup):
         flush_l2(i)
@@ -513,12 +533,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     # forms copy x in, call, and copy y out on one stream.
     e2e = None
     if not args.no_e2e:
-        hx = [torch.from_numpy(inp["x"].view(np.int16)).reshape(-1).pin_memory()
-              for inp in inputs]
-        hy = [torch.empty(c.rows * c.hidden, dtype=torch.int16).pin_memory() for c in cases]
-        h2d = sum(h.numel() * 2 for h in hx)
-        d2h = sum(h.numel() * 2 for h in hy)
-        pipelined = all(c.kind == "norm" for c in cases)
+        hx = [_tensor(inp["x"]).reshape(-1).pin_memory() for inp in inputs]
+        hy = [torch.empty(c.rows * c.hidden, dtype=d["y"].dtype).pin_memory()
+              for c, d in zip(cases, dev_bufs)]
+        h2d = sum(h.numel() * h.element_size() for h in hx)
+        d2h = sum(h.numel() * h.element_size() for h in hy)
+        pipelined = all(c.kind == "norm" and c.dtype == "bf16" for c in cases)
         if pipelined:
             pstreams = [torch.cuda.Stream(dev) for _ in range(3)]
             staging = torch.empty(3 * (16 << 20), dtype=torch.uint8, device=dev)
@@ -579,7 +599,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(float(step_ms.mean()), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "dtype": "f32", "io_dtype": cases[0].dtype, "data": "synthetic",
         "config": {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload,
                    "timing": "CUDA events around each launch on the launching stream; "
                              "a GPU spin before each launch keeps host launch latency "

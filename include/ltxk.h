@@ -74,11 +74,17 @@ typedef enum {
     LTXK_ERR_OVERLAP = 5,   /* out partially overlaps x, or overlaps w/cos/sin */
     LTXK_ERR_CUDA = 6,      /* a CUDA runtime call or the launch failed; see
                                ltxk_last_cuda_error() */
-    LTXK_ERR_TIMEOUT = 7    /* a kernel gave up waiting for a bulk copy (see
+    LTXK_ERR_TIMEOUT = 7,   /* a kernel gave up waiting for a bulk copy (see
                                ltxk_fault_status) */
+    LTXK_ERR_DTYPE = 8      /* unknown LTXK_DTYPE_* code */
 } ltxk_status;
 
 enum { LTXK_ROPE_INTERLEAVED = 0, LTXK_ROPE_SPLIT_HALF = 1 };
+
+/* Element types of the rows, weight and conditioning vectors ("cuda-kernels"
+ * skill page, "Supported Data Types": every kernel in three precision modes).
+ * RoPE tables stay fp32 in every mode. */
+enum { LTXK_DTYPE_BF16 = 0, LTXK_DTYPE_F16 = 1, LTXK_DTYPE_F32 = 2 };
 
 /* Largest hidden size (elements per row) the library accepts. */
 #define LTXK_MAX_HIDDEN (1 << 30)
@@ -158,6 +164,40 @@ LTXK_API int ltxk_add_rms_norm(void* out, void* residual_out, const void* x,
                                const void* residual, const void* w,
                                int64_t rows, int64_t hidden, float eps,
                                ltxk_stream_t stream);
+
+/*
+ * The same four row operations for rows of element type `dtype`
+ * (LTXK_DTYPE_BF16, _F16 or _F32); x, out, w and (AdaLN) scale and shift,
+ * (residual add) residual and residual_out all have that type, and every
+ * output is one round-to-nearest-even of the fp32 result to it.
+ *   - Arguments, layouts and overlap rules are those of the bf16 calls
+ *     above; pointers need the alignment of the element type (2 or 4
+ *     bytes), 16-byte alignment (and hidden % 8 == 0) takes the vector
+ *     kernels.
+ *   - ltxk_rms_norm_rope_dt takes tables [seq_len, head_dim/2] with row r
+ *     using table row r mod seq_len, as ltxk_rms_norm_rope_seq (seq_len =
+ *     rows gives per-row tables).
+ *   - Numerics: for fp16, x*w is exact in fp32 as for bf16, so every output
+ *     is within 1 fp16 ulp of the exact value.  For fp32 rows, x*w itself
+ *     rounds, and the output carries the fp32 error of the sum of squares,
+ *     rsqrtf and one or two products (a few ulp; more under cancellation in
+ *     RoPE or AdaLN).  fp16 outputs beyond 65504 round to infinity.
+ * An unknown dtype returns LTXK_ERR_DTYPE before any other check.
+ */
+LTXK_API int ltxk_rms_norm_dt(void* out, const void* x, const void* w, int64_t rows,
+                              int64_t hidden, float eps, int dtype, ltxk_stream_t stream);
+LTXK_API int ltxk_rms_norm_rope_dt(void* out, const void* x, const void* w,
+                                   const float* cos, const float* sin, int64_t rows,
+                                   int heads, int head_dim, int mode, float eps,
+                                   int64_t seq_len, int dtype, ltxk_stream_t stream);
+LTXK_API int ltxk_rms_norm_adaln_dt(void* out, const void* x, const void* w,
+                                    const void* scale, const void* shift, int64_t rows,
+                                    int64_t hidden, int64_t rows_per_cond, float eps,
+                                    int dtype, ltxk_stream_t stream);
+LTXK_API int ltxk_add_rms_norm_dt(void* out, void* residual_out, const void* x,
+                                  const void* residual, const void* w, int64_t rows,
+                                  int64_t hidden, float eps, int dtype,
+                                  ltxk_stream_t stream);
 
 /*
  * ltxk_gelu_tanh -- elementwise tanh-approximated GELU, bf16 -> bf16:
@@ -322,6 +362,10 @@ typedef struct {
  */
 LTXK_API int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim,
                      int mode, int vector_ok, ltxk_plan* plan);
+
+/* ltxk_plan_launch for rows of element type `dtype` (LTXK_DTYPE_*). */
+LTXK_API int ltxk_plan_launch_dt(int op, int dtype, int64_t rows, int64_t hidden,
+                                 int head_dim, int mode, int vector_ok, ltxk_plan* plan);
 
 #ifdef __cplusplus
 }

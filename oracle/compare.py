@@ -91,3 +91,78 @@ def _round_bits(v: np.ndarray) -> np.ndarray:
     # the oracle's own rounding (imported lazily: oracle builds a C library)
     import oracle
     return oracle.round_bf16(v)
+
+
+# ---- float16 and float32 outputs (the pages' other precision modes) --------
+#
+# The same rule on the format's own bit patterns: ordinal distance (+0 and -0
+# both at 0), NaN equal to NaN; spacing from the format's precision (binary16:
+# 11 significant bits, fixed spacing 2^-24 below 2^-14; binary32: 24 bits,
+# 2^-149 below 2^-126).
+
+_FMT = {np.dtype(np.float16): (np.uint16, 11, -14), np.dtype(np.float32): (np.uint32, 24, -126)}
+
+
+def _fmt_of(a):
+    a = np.asarray(a)
+    if a.dtype not in _FMT:
+        raise TypeError("float16 or float32 expected")
+    return a, _FMT[a.dtype]
+
+
+def ordinal_fmt(a: np.ndarray) -> np.ndarray:
+    a, (ut, prec, _) = _fmt_of(a)
+    b = a.view(ut).astype(np.int64)
+    top = 1 << (8 * np.dtype(ut).itemsize - 1)
+    mag = b & (top - 1)
+    return np.where(b & top, -mag, mag)
+
+
+def spacing_fmt(v: np.ndarray, dtype) -> np.ndarray:
+    _, prec, emin = _FMT[np.dtype(dtype)]
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, e = np.frexp(a)
+    e = np.maximum(e, emin + 1)
+    return np.ldexp(1.0, e - prec)
+
+
+def compare_fmt(got: np.ndarray, ref: np.ndarray, max_ulps: int = 1) -> dict:
+    """compare_bf16 for float16 / float32 arrays of the same dtype."""
+    got, _ = _fmt_of(np.asarray(got).reshape(-1))
+    ref, _ = _fmt_of(np.asarray(ref).reshape(-1))
+    if got.dtype != ref.dtype or got.shape != ref.shape:
+        raise ValueError("got and ref must have one dtype and shape")
+    gn, rn = np.isnan(got), np.isnan(ref)
+    d = np.abs(ordinal_fmt(got) - ordinal_fmt(ref))
+    d = np.where(gn & rn, 0, d)
+    bad = np.flatnonzero(d > max_ulps)
+    return {"elements": int(got.size), "exact": int(np.count_nonzero(d == 0)),
+            "one_ulp": int(np.count_nonzero(d == 1)), "over_tolerance": int(bad.size),
+            "max_ulps": int(d.max()) if d.size else 0,
+            "nan_mismatch": int(np.count_nonzero(gn != rn)),
+            "first_bad": [int(i) for i in bad[:8]],
+            "ok": bad.size == 0 and not np.any(gn != rn)}
+
+
+def compare_fmt_bounded(got: np.ndarray, exact: np.ndarray, bound: np.ndarray) -> dict:
+    """compare_bf16_bounded for float16 / float32 outputs: within 1 ulp of
+    the correctly rounded exact value, or |got - exact| <= half a spacing +
+    ``bound``."""
+    import oracle
+    got, _ = _fmt_of(np.asarray(got).reshape(-1))
+    exact = np.asarray(exact, dtype=np.float64).reshape(-1)
+    bound = np.asarray(bound, dtype=np.float64)
+    bound = bound.reshape(-1) if bound.size == exact.size else np.broadcast_to(bound, exact.shape)
+    ref = oracle.round_to(exact, got.dtype)
+    d = np.abs(ordinal_fmt(got) - ordinal_fmt(ref))
+    g = got.astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        sp = np.maximum(spacing_fmt(g, got.dtype), spacing_fmt(exact, got.dtype))
+        close = np.abs(g - exact) <= 0.5 * sp + bound
+    ok = (d <= 1) | close | (np.isnan(g) & np.isnan(exact))
+    bad = np.flatnonzero(~ok)
+    return {"elements": int(got.size), "exact": int(np.count_nonzero(d == 0)),
+            "one_ulp": int(np.count_nonzero(d == 1)),
+            "beyond_1ulp_within_bound": int(np.count_nonzero(ok & (d > 1))),
+            "over_tolerance": int(bad.size), "first_bad": [int(i) for i in bad[:8]],
+            "ok": bad.size == 0}

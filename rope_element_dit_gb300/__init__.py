@@ -1,5 +1,6 @@
-"""Python binding of libltxk.so: bf16 RMSNorm and fused RMSNorm + RoPE on
-one GB300 GPU.
+"""Python binding of libltxk.so: RMSNorm and its fused forms (RoPE, AdaLN,
+residual add) for bf16, fp16 and fp32 rows, and tanh GELU / GEGLU, on one
+GB300 GPU.
 
 The functions named ``ltxk_*`` mirror the C ABI in ``include/ltxk.h`` one to
 one (integer device pointers in, an ``ltxk_status`` integer out).  The
@@ -24,6 +25,11 @@ ERR_MODE = 4
 ERR_OVERLAP = 5
 ERR_CUDA = 6
 ERR_TIMEOUT = 7
+ERR_DTYPE = 8
+
+DTYPE_BF16 = 0
+DTYPE_F16 = 1
+DTYPE_F32 = 2
 
 PATH_AUTO = 0
 PATH_REGISTERS = 1
@@ -47,6 +53,8 @@ EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_adaln", "ltxk_rms_norm_host", "ltxk_add_rms_norm",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
+           "ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
+           "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -90,6 +98,15 @@ def _load():
     lib.ltxk_rms_norm_host.restype = I32
     lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
     lib.ltxk_rms_norm_noalloc.restype = I32
+    lib.ltxk_rms_norm_dt.argtypes = [P, P, P, I64, I64, F32, I32, P]
+    lib.ltxk_rms_norm_rope_dt.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, I32, P]
+    lib.ltxk_rms_norm_adaln_dt.argtypes = [P, P, P, P, P, I64, I64, I64, F32, I32, P]
+    lib.ltxk_add_rms_norm_dt.argtypes = [P, P, P, P, P, I64, I64, F32, I32, P]
+    for f in ("ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
+              "ltxk_add_rms_norm_dt"):
+        getattr(lib, f).restype = I32
+    lib.ltxk_plan_launch_dt.argtypes = [I32, I32, I64, I64, I32, I32, I32, ctypes.POINTER(Plan)]
+    lib.ltxk_plan_launch_dt.restype = I32
     lib.ltxk_gelu_tanh.argtypes = [P, P, I64, P]
     lib.ltxk_gelu_tanh.restype = I32
     lib.ltxk_geglu.argtypes = [P, P, I64, I64, P]
@@ -150,6 +167,36 @@ def ltxk_rms_norm_host(out_host, x_host, w, rows, hidden, eps, staging, staging_
 
 def ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream) -> int:
     return _lib.ltxk_rms_norm_noalloc(out, x, w, rows, hidden, eps, stream)
+
+
+def ltxk_rms_norm_dt(out, x, w, rows, hidden, eps, dtype, stream) -> int:
+    return _lib.ltxk_rms_norm_dt(out, x, w, rows, hidden, eps, dtype, stream)
+
+
+def ltxk_rms_norm_rope_dt(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len,
+                          dtype, stream) -> int:
+    return _lib.ltxk_rms_norm_rope_dt(out, x, w, cos, sin, rows, heads, head_dim, mode, eps,
+                                      seq_len, dtype, stream)
+
+
+def ltxk_rms_norm_adaln_dt(out, x, w, scale, shift, rows, hidden, rows_per_cond, eps, dtype,
+                           stream) -> int:
+    return _lib.ltxk_rms_norm_adaln_dt(out, x, w, scale, shift, rows, hidden, rows_per_cond,
+                                       eps, dtype, stream)
+
+
+def ltxk_add_rms_norm_dt(out, residual_out, x, residual, w, rows, hidden, eps, dtype,
+                         stream) -> int:
+    return _lib.ltxk_add_rms_norm_dt(out, residual_out, x, residual, w, rows, hidden, eps, dtype,
+                                     stream)
+
+
+def ltxk_plan_launch_dt(op, dtype, rows, hidden, head_dim, mode, vector_ok):
+    """Returns (status, Plan)."""
+    p = Plan()
+    st = _lib.ltxk_plan_launch_dt(op, dtype, rows, hidden, head_dim, mode,
+                                  1 if vector_ok else 0, ctypes.byref(p))
+    return st, p
 
 
 def ltxk_gelu_tanh(out, x, n, stream) -> int:
@@ -215,18 +262,27 @@ def _dev_ptr(t, name, dtype):
     return t.data_ptr()
 
 
-def rms_norm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
-    """y = x * weight / sqrt(mean(x^2, -1) + eps) over the last axis (bf16)."""
+def _dtype_code(t):
     import torch
+    codes = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype} (bfloat16, float16 or float32)")
+    return codes[t.dtype]
+
+
+def rms_norm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
+    """y = x * weight / sqrt(mean(x^2, -1) + eps) over the last axis
+    (bfloat16, float16 or float32; weight and out of x's dtype)."""
+    import torch
+    code = _dtype_code(x)
     hidden = x.shape[-1]
     rows = x.numel() // hidden if hidden else 0
     if out is None:
         out = torch.empty_like(x)
-    st = ltxk_rms_norm(_dev_ptr(out, "out", torch.bfloat16),
-                       _dev_ptr(x, "x", torch.bfloat16),
-                       _dev_ptr(weight, "weight", torch.bfloat16),
-                       rows, hidden, eps, _stream_handle(x, stream))
-    _check(st, "ltxk_rms_norm")
+    st = ltxk_rms_norm_dt(_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype),
+                          _dev_ptr(weight, "weight", x.dtype),
+                          rows, hidden, eps, code, _stream_handle(x, stream))
+    _check(st, "ltxk_rms_norm_dt")
     return out
 
 
@@ -241,6 +297,7 @@ def rms_norm_rope(x, weight, cos, sin, heads: int, head_dim: int,
     tables.
     """
     import torch
+    code = _dtype_code(x)
     hidden = heads * head_dim
     if x.shape[-1] != hidden:
         raise ValueError("last axis of x must be heads*head_dim")
@@ -248,11 +305,14 @@ def rms_norm_rope(x, weight, cos, sin, heads: int, head_dim: int,
     if out is None:
         out = torch.empty_like(x)
     table_rows = cos.numel() // (head_dim // 2) if seq_len is None else seq_len
-    args = (_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
-            _dev_ptr(weight, "weight", torch.bfloat16),
+    args = (_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype),
+            _dev_ptr(weight, "weight", x.dtype),
             _dev_ptr(cos, "cos", torch.float32), _dev_ptr(sin, "sin", torch.float32),
             rows, heads, head_dim, mode, eps)
-    if table_rows == rows and seq_len is None:
+    if code != DTYPE_BF16:
+        st = ltxk_rms_norm_rope_dt(*args, table_rows, code, _stream_handle(x, stream))
+        _check(st, "ltxk_rms_norm_rope_dt")
+    elif table_rows == rows and seq_len is None:
         st = ltxk_rms_norm_rope(*args, _stream_handle(x, stream))
         _check(st, "ltxk_rms_norm_rope")
     else:
@@ -270,6 +330,7 @@ def rms_norm_adaln(x, weight, scale, shift, eps: float = 1e-6, rows_per_cond=Non
     length for x ``[B, S, hidden]`` and conditioning ``[B, hidden]``).
     """
     import torch
+    code = _dtype_code(x)
     hidden = x.shape[-1]
     rows = x.numel() // hidden if hidden else 0
     n_cond = scale.numel() // hidden if hidden else 0
@@ -277,13 +338,12 @@ def rms_norm_adaln(x, weight, scale, shift, eps: float = 1e-6, rows_per_cond=Non
         rows_per_cond = max(1, -(-rows // max(1, n_cond)))
     if out is None:
         out = torch.empty_like(x)
-    st = ltxk_rms_norm_adaln(_dev_ptr(out, "out", torch.bfloat16),
-                             _dev_ptr(x, "x", torch.bfloat16),
-                             _dev_ptr(weight, "weight", torch.bfloat16),
-                             _dev_ptr(scale, "scale", torch.bfloat16),
-                             _dev_ptr(shift, "shift", torch.bfloat16),
-                             rows, hidden, rows_per_cond, eps, _stream_handle(x, stream))
-    _check(st, "ltxk_rms_norm_adaln")
+    st = ltxk_rms_norm_adaln_dt(_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype),
+                                _dev_ptr(weight, "weight", x.dtype),
+                                _dev_ptr(scale, "scale", x.dtype),
+                                _dev_ptr(shift, "shift", x.dtype),
+                                rows, hidden, rows_per_cond, eps, code, _stream_handle(x, stream))
+    _check(st, "ltxk_rms_norm_adaln_dt")
     return out
 
 
@@ -322,19 +382,20 @@ def add_rms_norm(x, residual, weight=None, eps: float = 1e-6, out=None, residual
     """h = x + residual (bf16), y = RMSNorm(h); returns ``(y, h)``.  Pass
     ``residual_out=residual`` to update the residual stream in place."""
     import torch
+    code = _dtype_code(x)
     hidden = x.shape[-1]
     rows = x.numel() // hidden if hidden else 0
     if out is None:
         out = torch.empty_like(x)
     if residual_out is None:
         residual_out = torch.empty_like(x)
-    st = ltxk_add_rms_norm(_dev_ptr(out, "out", torch.bfloat16),
-                           _dev_ptr(residual_out, "residual_out", torch.bfloat16),
-                           _dev_ptr(x, "x", torch.bfloat16),
-                           _dev_ptr(residual, "residual", torch.bfloat16),
-                           _dev_ptr(weight, "weight", torch.bfloat16),
-                           rows, hidden, eps, _stream_handle(x, stream))
-    _check(st, "ltxk_add_rms_norm")
+    st = ltxk_add_rms_norm_dt(_dev_ptr(out, "out", x.dtype),
+                              _dev_ptr(residual_out, "residual_out", x.dtype),
+                              _dev_ptr(x, "x", x.dtype),
+                              _dev_ptr(residual, "residual", x.dtype),
+                              _dev_ptr(weight, "weight", x.dtype),
+                              rows, hidden, eps, code, _stream_handle(x, stream))
+    _check(st, "ltxk_add_rms_norm_dt")
     return out, residual_out
 
 

@@ -19,9 +19,12 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libltxk.so")
 
-SOURCES = ["ltxk_abi.cu", "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu",
-           "ltxk_rows_split.cu", "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu", "ltxk_noalloc.cu",
-           "ltxk_pipeline.cu", "ltxk_gelu.cu"]
+SOURCES = ["ltxk_abi.cu", "ltxk_noalloc.cu", "ltxk_pipeline.cu", "ltxk_gelu.cu"]
+# Row-kernel instance files, compiled once per element format (LTXK_FMT:
+# 0 bf16, 1 fp16, 2 fp32).
+ROW_SOURCES = ["ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",
+               "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu"]
+FORMATS = {0: "bf16", 1: "f16", 2: "f32"}
 HEADERS = ["ltxk_kernels.cuh", "ltxk_instances.cuh", "ltxk_launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -59,12 +62,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(),
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "ltxk.h")]
     objs = []
     jobs = []
-    for src in SOURCES:
+    units = [(src, src.replace(".cu", ".o"), []) for src in SOURCES]
+    units += [(src, src.replace(".cu", f".{name}.o"), [f"-DLTXK_FMT={fmt}"])
+              for src in ROW_SOURCES for fmt, name in FORMATS.items()]
+    for src, obj, defs in units:
         s = os.path.join(CSRC, src)
-        o = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        o = os.path.join(obj_dir, obj)
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defs, *extra_flags, "-c", s, "-o", o]
             jobs.append(cmd)
 
     def run(cmd):
@@ -76,7 +82,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(),
         if verbose and (r.stdout or r.stderr):
             print(r.stdout + r.stderr, flush=True)
 
-    with ThreadPoolExecutor(max_workers=len(jobs) or 1) as ex:
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         list(ex.map(run, jobs))
 
     if force or jobs or _stale(lib, objs):

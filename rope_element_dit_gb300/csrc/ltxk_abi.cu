@@ -27,7 +27,7 @@ namespace {
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_path{LTXK_PATH_AUTO};
 
-constexpr int kMaxVplSlots = 16;
+constexpr int kMaxVplSlots = 16;   // fp32 rows: 8 (twice the registers per slot)
 constexpr int kGroupChoices[] = {1, 2, 4, 8, 16, 32};
 // Dynamic shared memory a TMA-ring CTA aims for: two CTAs per SM share the
 // 228 KB of an SM, so each keeps about 100 KB of rows in flight.
@@ -48,6 +48,10 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
   return a0 < b0 + nb && b0 < a0 + na;
 }
+
+int max_vpl(int fmt) { return fmt == ltxk::kF32 ? 8 : kMaxVplSlots; }
+
+int elem_bytes(int fmt) { return fmt == ltxk::kF32 ? 4 : 2; }
 
 int bucket_vpl(int need) {
   if (need <= 4) return 4;
@@ -183,8 +187,9 @@ int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
   return LTXK_OK;
 }
 
-int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool vector_ok,
-              int path, ltxk_plan* p) {
+int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int mode,
+              bool vector_ok, int path, ltxk_plan* p) {
+  if (fmt != ltxk::kBf16 && fmt != ltxk::kF16 && fmt != ltxk::kF32) return LTXK_ERR_DTYPE;
   const int st = check_shape(op, rows, hidden, head_dim, mode);
   if (st != LTXK_OK) return st;
   *p = ltxk_plan{LTXK_KERNEL_NONE, 0, 0, 0, 0, 0, 0};
@@ -219,18 +224,21 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
     // split-half slots are (lo, hi) pairs: nv/2 units of two slots each
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
-    const int max_slots = row_only                   ? LTXK_PLAIN_MAX_SLOTS
-                          : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
-                                                     : LTXK_ROPE_MAX_SLOTS_SPLIT;
+    const int cap = max_vpl(fmt);
+    int max_slots = row_only                   ? LTXK_PLAIN_MAX_SLOTS
+                    : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
+                                               : LTXK_ROPE_MAX_SLOTS_SPLIT;
+    if (max_slots > cap) max_slots = cap;
     for (int g : kGroupChoices) {
       const int64_t need = (units + 32 * g - 1) / (32 * g) * slots_per_unit;
       if (need > max_slots && g < 32) continue;
-      if (need > kMaxVplSlots) continue;
+      if (need > cap) continue;
       p->group_warps = g;
       p->vec_per_lane = bucket_vpl(static_cast<int>(need));
       // The TMA ring is used only on request: measured on GB300 it trails
       // the register kernel on every workload here.
-      if (g == 1 && path == LTXK_PATH_TMA && km != ltxk::kAdaLN && km != ltxk::kAddNorm) {
+      if (g == 1 && path == LTXK_PATH_TMA && km != ltxk::kAdaLN && km != ltxk::kAddNorm &&
+          fmt == ltxk::kBf16) {
         const uint32_t stride = tma_stride(hidden);
         int stages = static_cast<int>((kTmaSmemTarget - ltxk::kTmaBarBytes) /
                                       (ltxk::kTmaWarps * stride));
@@ -255,34 +263,57 @@ int make_plan(int op, int64_t rows, int64_t hidden, int head_dim, int mode, bool
   return LTXK_OK;
 }
 
-const void* kernel_fn(const ltxk_plan& p, int km) {
+template <int FMT>
+const void* vec_fn(int km, int g, int vpl) {
+  switch (km) {
+    case ltxk::kPlain: return ltxk::rows_vec_ptr<ltxk::kPlain, FMT>(g, vpl);
+    case ltxk::kInterleaved: return ltxk::rows_vec_ptr<ltxk::kInterleaved, FMT>(g, vpl);
+    case ltxk::kSplitHalf: return ltxk::rows_vec_ptr<ltxk::kSplitHalf, FMT>(g, vpl);
+    case ltxk::kAdaLN: return ltxk::rows_vec_ptr<ltxk::kAdaLN, FMT>(g, vpl);
+    case ltxk::kAddNorm: return ltxk::rows_vec_ptr<ltxk::kAddNorm, FMT>(g, vpl);
+    default: return nullptr;
+  }
+}
+
+template <int FMT>
+const void* elem_fn(int km) {
+  switch (km) {
+    case ltxk::kPlain: return ltxk::rows_elem_ptr<ltxk::kPlain, FMT>();
+    case ltxk::kInterleaved: return ltxk::rows_elem_ptr<ltxk::kInterleaved, FMT>();
+    case ltxk::kSplitHalf: return ltxk::rows_elem_ptr<ltxk::kSplitHalf, FMT>();
+    case ltxk::kAdaLN: return ltxk::rows_elem_ptr<ltxk::kAdaLN, FMT>();
+    case ltxk::kAddNorm: return ltxk::rows_elem_ptr<ltxk::kAddNorm, FMT>();
+    default: return nullptr;
+  }
+}
+
+const void* kernel_fn(const ltxk_plan& p, int km, int fmt) {
   switch (p.kernel) {
     case LTXK_KERNEL_ROWS_VEC:
-      if (km == ltxk::kPlain) return ltxk::rows_vec_plain_ptr(p.group_warps, p.vec_per_lane);
-      if (km == ltxk::kInterleaved)
-        return ltxk::rows_vec_interleaved_ptr(p.group_warps, p.vec_per_lane);
-      if (km == ltxk::kAdaLN) return ltxk::rows_vec_adaln_ptr(p.group_warps, p.vec_per_lane);
-      if (km == ltxk::kAddNorm)
-        return ltxk::rows_vec_addnorm_ptr(p.group_warps, p.vec_per_lane);
-      return ltxk::rows_vec_split_ptr(p.group_warps, p.vec_per_lane);
+      if (fmt == ltxk::kF16) return vec_fn<ltxk::kF16>(km, p.group_warps, p.vec_per_lane);
+      if (fmt == ltxk::kF32) return vec_fn<ltxk::kF32>(km, p.group_warps, p.vec_per_lane);
+      return vec_fn<ltxk::kBf16>(km, p.group_warps, p.vec_per_lane);
     case LTXK_KERNEL_ROWS_TMA:
       if (km == ltxk::kPlain) return ltxk::rows_tma_plain_ptr(p.vec_per_lane);
       if (km == ltxk::kInterleaved) return ltxk::rows_tma_interleaved_ptr(p.vec_per_lane);
       return ltxk::rows_tma_split_ptr(p.vec_per_lane);
     case LTXK_KERNEL_ROWS_ELEM:
-      return ltxk::rows_elem_kernel_ptr(km);
+      if (fmt == ltxk::kF16) return elem_fn<ltxk::kF16>(km);
+      if (fmt == ltxk::kF32) return elem_fn<ltxk::kF32>(km);
+      return elem_fn<ltxk::kBf16>(km);
     default:
       return nullptr;
   }
 }
 
-int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStream_t stream,
-           int path, int skip_first_copy = 0, uint64_t wait_limit_ns = kWaitLimitNs) {
+int launch(int op, int mode, int fmt, const ltxk::RowArgs& args, bool vector_ok,
+           cudaStream_t stream, int path, int skip_first_copy = 0,
+           uint64_t wait_limit_ns = kWaitLimitNs) {
   ltxk_plan p;
-  int st = make_plan(op, args.rows, args.hidden, args.head_dim, mode, vector_ok, path, &p);
+  int st = make_plan(op, fmt, args.rows, args.hidden, args.head_dim, mode, vector_ok, path, &p);
   if (st != LTXK_OK || p.kernel == LTXK_KERNEL_NONE) return st;
   const int km = kernel_mode(op, mode);
-  const void* fn = kernel_fn(p, km);
+  const void* fn = kernel_fn(p, km, fmt);
   if (fn == nullptr) return fail_cuda(cudaErrorInvalidDeviceFunction);
   int dev = 0, sms = 0, per_sm = 0;
   unsigned int* fault = nullptr;
@@ -313,42 +344,114 @@ int launch(int op, int mode, const ltxk::RowArgs& args, bool vector_ok, cudaStre
   return LTXK_OK;
 }
 
+// Element format of an LTXK_DTYPE_* code, or -1.
+int fmt_of(int dtype) {
+  switch (dtype) {
+    case LTXK_DTYPE_BF16: return ltxk::kBf16;
+    case LTXK_DTYPE_F16: return ltxk::kF16;
+    case LTXK_DTYPE_F32: return ltxk::kF32;
+    default: return -1;
+  }
+}
+
 int rope_common(void* out, const void* x, const void* w, const float* cos, const float* sin,
                 int64_t rows, int heads, int head_dim, int mode, float eps, int64_t table_rows,
-                cudaStream_t stream) {
+                int fmt, cudaStream_t stream) {
+  if (fmt < 0) return LTXK_ERR_DTYPE;
   if (out == nullptr || x == nullptr || cos == nullptr || sin == nullptr) return LTXK_ERR_NULL;
   if (heads < 1 || head_dim < 2 || head_dim % 2 != 0 || table_rows < 1) return LTXK_ERR_SHAPE;
   const int64_t hidden = static_cast<int64_t>(heads) * head_dim;
   int st = check_shape(LTXK_OP_RMS_NORM_ROPE, rows, hidden, head_dim, mode);
   if (st != LTXK_OK) return st;
   if (table_rows > INT64_MAX / 8 / head_dim) return LTXK_ERR_SHAPE;
-  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2)) ||
+  const int esz = elem_bytes(fmt);
+  if (!aligned_to(out, esz) || !aligned_to(x, esz) || (w && !aligned_to(w, esz)) ||
       !aligned_to(cos, 4) || !aligned_to(sin, 4))
     return LTXK_ERR_ALIGN;
-  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * esz;
   const uint64_t tbytes = static_cast<uint64_t>(table_rows) * (head_dim / 2) * 4;
   if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
-  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2) ||
+  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * esz) ||
       overlaps(out, xbytes, cos, tbytes) || overlaps(out, xbytes, sin, tbytes))
     return LTXK_ERR_OVERLAP;
   if (rows == 0) return LTXK_OK;
   const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
                          aligned_to(cos, 16) && aligned_to(sin, 16);
-  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
-                  static_cast<const uint16_t*>(w), cos, sin, rows, table_rows,
-                  static_cast<int>(hidden), head_dim, eps};
-  return launch(LTXK_OP_RMS_NORM_ROPE, mode, a, vector_ok, stream, g_path.load());
+  ltxk::RowArgs a{out, x, w, cos, sin, rows, table_rows, static_cast<int>(hidden), head_dim, eps};
+  return launch(LTXK_OP_RMS_NORM_ROPE, mode, fmt, a, vector_ok, stream, g_path.load());
 }
 
-int norm_checks(void* out, const void* x, const void* w, int64_t rows, int64_t hidden) {
+int norm_checks(void* out, const void* x, const void* w, int64_t rows, int64_t hidden, int fmt) {
+  if (fmt < 0) return LTXK_ERR_DTYPE;
   if (out == nullptr || x == nullptr) return LTXK_ERR_NULL;
   int st = check_shape(LTXK_OP_RMS_NORM, rows, hidden, 0, 0);
   if (st != LTXK_OK) return st;
-  if (!aligned_to(out, 2) || !aligned_to(x, 2) || (w && !aligned_to(w, 2))) return LTXK_ERR_ALIGN;
-  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
+  const int esz = elem_bytes(fmt);
+  if (!aligned_to(out, esz) || !aligned_to(x, esz) || (w && !aligned_to(w, esz)))
+    return LTXK_ERR_ALIGN;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * esz;
   if (out != x && overlaps(out, xbytes, x, xbytes)) return LTXK_ERR_OVERLAP;
-  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * 2)) return LTXK_ERR_OVERLAP;
+  if (overlaps(out, xbytes, w, static_cast<uint64_t>(hidden) * esz)) return LTXK_ERR_OVERLAP;
   return LTXK_OK;
+}
+
+int rms_norm_fmt(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
+                 float eps, int fmt, cudaStream_t stream) {
+  int st = norm_checks(out, x, w, rows, hidden, fmt);
+  if (st != LTXK_OK || rows == 0) return st;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16));
+  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps};
+  return launch(LTXK_OP_RMS_NORM, 0, fmt, a, vector_ok, stream, g_path.load());
+}
+
+int adaln_fmt(void* out, const void* x, const void* w, const void* scale, const void* shift,
+              int64_t rows, int64_t hidden, int64_t rows_per_cond, float eps, int fmt,
+              cudaStream_t stream) {
+  if (fmt < 0) return LTXK_ERR_DTYPE;
+  if (scale == nullptr || shift == nullptr) return LTXK_ERR_NULL;
+  int st = norm_checks(out, x, w, rows, hidden, fmt);
+  if (st != LTXK_OK) return st;
+  if (rows_per_cond < 1) return LTXK_ERR_SHAPE;
+  const int esz = elem_bytes(fmt);
+  if (!aligned_to(scale, esz) || !aligned_to(shift, esz)) return LTXK_ERR_ALIGN;
+  const int64_t n_cond = rows == 0 ? 0 : (rows - 1) / rows_per_cond + 1;
+  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * esz;
+  const uint64_t cbytes = static_cast<uint64_t>(n_cond) * hidden * esz;
+  if (overlaps(out, xbytes, scale, cbytes) || overlaps(out, xbytes, shift, cbytes))
+    return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
+                         aligned_to(scale, 16) && aligned_to(shift, 16);
+  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps,
+                  scale, shift, rows_per_cond};
+  return launch(LTXK_OP_RMS_NORM_ADALN, 0, fmt, a, vector_ok, stream, g_path.load());
+}
+
+int add_norm_fmt(void* out, void* residual_out, const void* x, const void* residual,
+                 const void* w, int64_t rows, int64_t hidden, float eps, int fmt,
+                 cudaStream_t stream) {
+  if (fmt < 0) return LTXK_ERR_DTYPE;
+  if (residual_out == nullptr || residual == nullptr) return LTXK_ERR_NULL;
+  int st = norm_checks(out, x, w, rows, hidden, fmt);
+  if (st != LTXK_OK) return st;
+  const int esz = elem_bytes(fmt);
+  if (!aligned_to(residual_out, esz) || !aligned_to(residual, esz)) return LTXK_ERR_ALIGN;
+  const uint64_t bytes = static_cast<uint64_t>(rows) * hidden * esz;
+  const uint64_t wbytes = static_cast<uint64_t>(hidden) * esz;
+  // the two outputs must be disjoint; an output may coincide exactly with an
+  // input (every row is read before it is written) but not partly overlap one
+  if (overlaps(out, bytes, residual_out, bytes)) return LTXK_ERR_OVERLAP;
+  if (residual_out != x && overlaps(residual_out, bytes, x, bytes)) return LTXK_ERR_OVERLAP;
+  if (residual_out != residual && overlaps(residual_out, bytes, residual, bytes))
+    return LTXK_ERR_OVERLAP;
+  if (out != residual && overlaps(out, bytes, residual, bytes)) return LTXK_ERR_OVERLAP;
+  if (overlaps(residual_out, bytes, w, wbytes)) return LTXK_ERR_OVERLAP;
+  if (rows == 0) return LTXK_OK;
+  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
+                         aligned_to(residual, 16) && aligned_to(residual_out, 16);
+  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps,
+                  nullptr, nullptr, 0, residual, residual_out};
+  return launch(LTXK_OP_ADD_RMS_NORM, 0, fmt, a, vector_ok, stream, g_path.load());
 }
 
 }  // namespace
@@ -361,13 +464,12 @@ extern "C" {
 
 int ltxk_rms_norm(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
                   float eps, ltxk_stream_t stream) {
-  int st = norm_checks(out, x, w, rows, hidden);
-  if (st != LTXK_OK || rows == 0) return st;
-  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16));
-  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
-                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
-                  static_cast<int>(hidden), 0, eps};
-  return launch(LTXK_OP_RMS_NORM, 0, a, vector_ok, stream, g_path.load());
+  return rms_norm_fmt(out, x, w, rows, hidden, eps, ltxk::kBf16, stream);
+}
+
+int ltxk_rms_norm_dt(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
+                     float eps, int dtype, ltxk_stream_t stream) {
+  return rms_norm_fmt(out, x, w, rows, hidden, eps, fmt_of(dtype), stream);
 }
 
 int ltxk_rms_norm_rope(void* out, const void* x, const void* w, const float* cos,
@@ -376,63 +478,48 @@ int ltxk_rms_norm_rope(void* out, const void* x, const void* w, const float* cos
   // Per-row tables: row r uses table row r.  With rows == 0 there is no
   // table at all; any positive table_rows gives the same (empty) launch.
   return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps,
-                     rows > 0 ? rows : 1, stream);
+                     rows > 0 ? rows : 1, ltxk::kBf16, stream);
 }
 
 int ltxk_rms_norm_rope_seq(void* out, const void* x, const void* w, const float* cos,
                            const float* sin, int64_t rows, int heads, int head_dim, int mode,
                            float eps, int64_t seq_len, ltxk_stream_t stream) {
-  return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len, stream);
+  return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len,
+                     ltxk::kBf16, stream);
+}
+
+int ltxk_rms_norm_rope_dt(void* out, const void* x, const void* w, const float* cos,
+                          const float* sin, int64_t rows, int heads, int head_dim, int mode,
+                          float eps, int64_t seq_len, int dtype, ltxk_stream_t stream) {
+  return rope_common(out, x, w, cos, sin, rows, heads, head_dim, mode, eps, seq_len,
+                     fmt_of(dtype), stream);
 }
 
 int ltxk_rms_norm_adaln(void* out, const void* x, const void* w, const void* scale,
                         const void* shift, int64_t rows, int64_t hidden, int64_t rows_per_cond,
                         float eps, ltxk_stream_t stream) {
-  if (scale == nullptr || shift == nullptr) return LTXK_ERR_NULL;
-  int st = norm_checks(out, x, w, rows, hidden);
-  if (st != LTXK_OK) return st;
-  if (rows_per_cond < 1) return LTXK_ERR_SHAPE;
-  if (!aligned_to(scale, 2) || !aligned_to(shift, 2)) return LTXK_ERR_ALIGN;
-  const int64_t n_cond = rows == 0 ? 0 : (rows - 1) / rows_per_cond + 1;
-  const uint64_t xbytes = static_cast<uint64_t>(rows) * hidden * 2;
-  const uint64_t cbytes = static_cast<uint64_t>(n_cond) * hidden * 2;
-  if (overlaps(out, xbytes, scale, cbytes) || overlaps(out, xbytes, shift, cbytes))
-    return LTXK_ERR_OVERLAP;
-  if (rows == 0) return LTXK_OK;
-  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
-                         aligned_to(scale, 16) && aligned_to(shift, 16);
-  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
-                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
-                  static_cast<int>(hidden), 0, eps, static_cast<const uint16_t*>(scale),
-                  static_cast<const uint16_t*>(shift), rows_per_cond};
-  return launch(LTXK_OP_RMS_NORM_ADALN, 0, a, vector_ok, stream, g_path.load());
+  return adaln_fmt(out, x, w, scale, shift, rows, hidden, rows_per_cond, eps, ltxk::kBf16,
+                   stream);
+}
+
+int ltxk_rms_norm_adaln_dt(void* out, const void* x, const void* w, const void* scale,
+                           const void* shift, int64_t rows, int64_t hidden,
+                           int64_t rows_per_cond, float eps, int dtype, ltxk_stream_t stream) {
+  return adaln_fmt(out, x, w, scale, shift, rows, hidden, rows_per_cond, eps, fmt_of(dtype),
+                   stream);
 }
 
 int ltxk_add_rms_norm(void* out, void* residual_out, const void* x, const void* residual,
                       const void* w, int64_t rows, int64_t hidden, float eps,
                       ltxk_stream_t stream) {
-  if (residual_out == nullptr || residual == nullptr) return LTXK_ERR_NULL;
-  int st = norm_checks(out, x, w, rows, hidden);
-  if (st != LTXK_OK) return st;
-  if (!aligned_to(residual_out, 2) || !aligned_to(residual, 2)) return LTXK_ERR_ALIGN;
-  const uint64_t bytes = static_cast<uint64_t>(rows) * hidden * 2;
-  const uint64_t wbytes = static_cast<uint64_t>(hidden) * 2;
-  // the two outputs must be disjoint; an output may coincide exactly with an
-  // input (every row is read before it is written) but not partly overlap one
-  if (overlaps(out, bytes, residual_out, bytes)) return LTXK_ERR_OVERLAP;
-  if (residual_out != x && overlaps(residual_out, bytes, x, bytes)) return LTXK_ERR_OVERLAP;
-  if (residual_out != residual && overlaps(residual_out, bytes, residual, bytes))
-    return LTXK_ERR_OVERLAP;
-  if (out != residual && overlaps(out, bytes, residual, bytes)) return LTXK_ERR_OVERLAP;
-  if (overlaps(residual_out, bytes, w, wbytes)) return LTXK_ERR_OVERLAP;
-  if (rows == 0) return LTXK_OK;
-  const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
-                         aligned_to(residual, 16) && aligned_to(residual_out, 16);
-  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
-                  static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
-                  static_cast<int>(hidden), 0, eps, nullptr, nullptr, 0,
-                  static_cast<const uint16_t*>(residual), static_cast<uint16_t*>(residual_out)};
-  return launch(LTXK_OP_ADD_RMS_NORM, 0, a, vector_ok, stream, g_path.load());
+  return add_norm_fmt(out, residual_out, x, residual, w, rows, hidden, eps, ltxk::kBf16, stream);
+}
+
+int ltxk_add_rms_norm_dt(void* out, void* residual_out, const void* x, const void* residual,
+                         const void* w, int64_t rows, int64_t hidden, float eps, int dtype,
+                         ltxk_stream_t stream) {
+  return add_norm_fmt(out, residual_out, x, residual, w, rows, hidden, eps, fmt_of(dtype),
+                      stream);
 }
 
 int ltxk_fault_status(void) {
@@ -461,16 +548,16 @@ int ltxk_set_path(int path) {
 
 int ltxk_diag_missing_copy(void* out, const void* x, int64_t rows, int64_t hidden,
                            uint64_t wait_limit_ns, ltxk_stream_t stream) {
-  int st = norm_checks(out, x, nullptr, rows, hidden);
+  int st = norm_checks(out, x, nullptr, rows, hidden, ltxk::kBf16);
   if (st != LTXK_OK) return st;
   if (hidden % 8 != 0 || hidden > 4096 || wait_limit_ns < 1000ull ||
       wait_limit_ns > 10000000000ull)
     return LTXK_ERR_SHAPE;
   if (!aligned_to(out, 16) || !aligned_to(x, 16)) return LTXK_ERR_ALIGN;
   if (rows == 0) return LTXK_OK;
-  ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x), nullptr,
-                  nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, 1e-6f};
-  return launch(LTXK_OP_RMS_NORM, 0, a, true, stream, LTXK_PATH_TMA, 1, wait_limit_ns);
+  ltxk::RowArgs a{out, x, nullptr, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, 1e-6f};
+  return launch(LTXK_OP_RMS_NORM, 0, ltxk::kBf16, a, true, stream, LTXK_PATH_TMA, 1,
+                wait_limit_ns);
 }
 
 const char* ltxk_status_string(int status) {
@@ -483,6 +570,7 @@ const char* ltxk_status_string(int status) {
     case LTXK_ERR_OVERLAP: return "output overlaps an input (other than exactly in place)";
     case LTXK_ERR_CUDA: return "CUDA runtime error (see ltxk_last_cuda_error)";
     case LTXK_ERR_TIMEOUT: return "a kernel gave up waiting for a bulk copy";
+    case LTXK_ERR_DTYPE: return "unknown element type";
     default: return "unknown status";
   }
 }
@@ -492,7 +580,16 @@ int ltxk_last_cuda_error(void) { return g_last_cuda_error; }
 int ltxk_plan_launch(int op, int64_t rows, int64_t hidden, int head_dim, int mode, int vector_ok,
                      ltxk_plan* plan) {
   if (plan == nullptr) return LTXK_ERR_NULL;
-  return make_plan(op, rows, hidden, head_dim, mode, vector_ok != 0, g_path.load(), plan);
+  return make_plan(op, ltxk::kBf16, rows, hidden, head_dim, mode, vector_ok != 0, g_path.load(),
+                   plan);
+}
+
+int ltxk_plan_launch_dt(int op, int dtype, int64_t rows, int64_t hidden, int head_dim, int mode,
+                        int vector_ok, ltxk_plan* plan) {
+  if (plan == nullptr) return LTXK_ERR_NULL;
+  const int fmt = fmt_of(dtype);
+  if (fmt < 0) return LTXK_ERR_DTYPE;
+  return make_plan(op, fmt, rows, hidden, head_dim, mode, vector_ok != 0, g_path.load(), plan);
 }
 
 }  // extern "C"

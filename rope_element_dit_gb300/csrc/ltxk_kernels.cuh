@@ -1,11 +1,13 @@
-// ltxk_kernels.cuh -- device code for bf16 RMSNorm and fused RMSNorm + RoPE
-// on sm_103a (GB300).
+// ltxk_kernels.cuh -- device code for RMSNorm and fused RMSNorm + RoPE on
+// sm_103a (GB300), for bf16, fp16 and fp32 rows.
 //
 // The operation (no formula is printed on the pages; this is the definition
 // the library implements):
 //   per row r:  ms = (1/H) sum_j x_j^2,  n_j = x_j * w_j / sqrt(ms + eps)
 //   fused:      per head and pair (a, b):  a' = a c - b s,  b' = a s + b c
-//   one round-to-nearest-even to bfloat16 at the end.
+//   one round-to-nearest-even to the row format (bf16, fp16 or fp32) at the
+//   end ("cuda-kernels" page, "Supported Data Types": the three precision
+//   modes).
 // Sources: "cuda-kernels" skill page (Hugging Face), "Kernel-Specific
 // Guidelines / RMSNorm" and "/ RoPE", "Core Kernel Patterns / Vectorized
 // Memory Access" and "/ Warp Shuffle Reductions"; "ltx-kernels" README,
@@ -19,8 +21,9 @@
 //     warp, then (G > 1) a fixed-order sum of the G warp totals through
 //     shared memory.  Every thread ends with the same bit-identical total.
 //   * inv_rms = rsqrtf(ss / H + eps); y = (x * w) * inv_rms, where x * w is
-//     exact in fp32 (two 8-bit significands), so each output is one fp32
-//     rounding away from (x w) * inv_rms before the final bf16 rounding.
+//     exact in fp32 for bf16 and fp16 rows (two significands of at most 11
+//     bits), so each output is one fp32 rounding away from (x w) * inv_rms
+//     before the final rounding; fp32 rows add one rounding of x * w.
 //   * RoPE rotates (u, v) = (x_a w_a, x_b w_b) (both exact) and scales by
 //     inv_rms afterwards; u c - v s and u s + v c are evaluated with Kahan's
 //     2x2-determinant algorithm (W. Kahan; error bound in Jeannerod, Louvet &
@@ -33,6 +36,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,10 +44,13 @@ namespace ltxk {
 
 enum Mode : int { kPlain = 0, kInterleaved = 1, kSplitHalf = 2, kAdaLN = 3, kAddNorm = 4 };
 
+// Element formats of the rows, weight and conditioning (tables are fp32).
+enum Fmt : int { kBf16 = 0, kF16 = 1, kF32 = 2 };
+
 struct RowArgs {
-  uint16_t* out;            // [rows, hidden] bf16
-  const uint16_t* x;        // [rows, hidden] bf16
-  const uint16_t* w;        // [hidden] bf16 or nullptr (ones)
+  void* out;                // [rows, hidden] in the row format
+  const void* x;            // [rows, hidden]
+  const void* w;            // [hidden] or nullptr (ones)
   const float* cos_t;       // [table_rows, head_dim/2] fp32 (fused only)
   const float* sin_t;
   int64_t rows;
@@ -51,11 +58,11 @@ struct RowArgs {
   int hidden;
   int head_dim;
   float eps;
-  const uint16_t* scale;    // AdaLN: [n_cond, hidden] bf16
-  const uint16_t* shift;    // AdaLN: [n_cond, hidden] bf16
+  const void* scale;        // AdaLN: [n_cond, hidden]
+  const void* shift;        // AdaLN: [n_cond, hidden]
   int64_t rows_per_cond;    // AdaLN: row r uses conditioning row r / rows_per_cond
-  const uint16_t* res;      // residual add: [rows, hidden] bf16 residual in
-  uint16_t* h_out;          // residual add: [rows, hidden] bf16 h = x + res out
+  const void* res;          // residual add: [rows, hidden] residual in
+  void* h_out;              // residual add: [rows, hidden] h = x + res out
 };
 
 // ---- element helpers -----------------------------------------------------
@@ -101,17 +108,6 @@ __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y
 __device__ __forceinline__ float2 bf2_of(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
 
 __device__ __forceinline__ uint32_t pack_f2(float2 v) { return pack_bf2(v.x, v.y); }
-
-// bf16(a + b) for the 8 bf16 lanes of two vectors.  The fp32 sum of two
-// bf16 values is exact unless their exponents differ by 16 or more, and then
-// the smaller one is far below half a bf16 spacing of the larger, so the one
-// RNE conversion gives the correctly rounded bf16 sum.
-__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
-  return make_uint4(pack_f2(__fadd2_rn(bf2_of(a.x), bf2_of(b.x))),
-                    pack_f2(__fadd2_rn(bf2_of(a.y), bf2_of(b.y))),
-                    pack_f2(__fadd2_rn(bf2_of(a.z), bf2_of(b.z))),
-                    pack_f2(__fadd2_rn(bf2_of(a.w), bf2_of(b.w))));
-}
 
 // Kahan's a*b - c*d on both lanes.
 __device__ __forceinline__ float2 diff_of_products2(float2 a, float2 b, float2 c, float2 d) {
@@ -187,18 +183,154 @@ __device__ __forceinline__ void group_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
-// Sum of squares of 8 bf16 values, as two fp32 partial sums (even, odd).
-__device__ __forceinline__ float2 sumsq8(uint4 v, float2 s) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
+
+// ---- element formats -------------------------------------------------------
+//
+// A slot always holds 8 consecutive elements: one 16-byte vector of bf16 or
+// fp16, two of fp32.  Pair i (0..3) of a slot is its elements 2i and 2i+1,
+// widened exactly to fp32; pack() rounds four pairs once (RNE) into a slot.
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <int FMT>
+struct Io;
+
+template <>
+struct Io<kBf16> {
+  using Vec = uint4;
+  static constexpr int kWords = 4;   // registers per slot
+  static constexpr int kBytes = 2;
+  __device__ static Vec load(const void* p, int64_t e) {
+    return ld_stream16(static_cast<const uint16_t*>(p) + e);
+  }
+  __device__ static Vec load_ro(const void* p, int64_t e) {
+    return ld_ro16(static_cast<const uint16_t*>(p) + e);
+  }
+  __device__ static void store(void* p, int64_t e, const Vec& v) {
+    st16(static_cast<uint16_t*>(p) + e, v);
+  }
+  __device__ static float2 pair(const Vec& v, int i) { return bf2_of(word_of(v, i)); }
+  __device__ static Vec pack(float2 a, float2 b, float2 c, float2 d) {
+    return make_uint4(pack_f2(a), pack_f2(b), pack_f2(c), pack_f2(d));
+  }
+  __device__ static Vec ones() { return make_uint4(kOnes2, kOnes2, kOnes2, kOnes2); }
+  __device__ static void launder_vec(Vec& v) { launder(v); }
+  __device__ static float get(const void* p, int64_t e) {
+    return bf_to_f(static_cast<const uint16_t*>(p)[e]);
+  }
+  __device__ static void put(void* p, int64_t e, float f) {
+    static_cast<uint16_t*>(p)[e] = f_to_bf(f);
+  }
+};
+
+template <>
+struct Io<kF16> {
+  using Vec = uint4;
+  static constexpr int kWords = 4;
+  static constexpr int kBytes = 2;
+  __device__ static Vec load(const void* p, int64_t e) {
+    return ld_stream16(static_cast<const uint16_t*>(p) + e);
+  }
+  __device__ static Vec load_ro(const void* p, int64_t e) {
+    return ld_ro16(static_cast<const uint16_t*>(p) + e);
+  }
+  __device__ static void store(void* p, int64_t e, const Vec& v) {
+    st16(static_cast<uint16_t*>(p) + e, v);
+  }
+  __device__ static float2 pair(const Vec& v, int i) {
+    const uint32_t u = word_of(v, i);
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+  }
+  __device__ static uint32_t pack2(float2 f) {
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  __device__ static Vec pack(float2 a, float2 b, float2 c, float2 d) {
+    return make_uint4(pack2(a), pack2(b), pack2(c), pack2(d));
+  }
+  __device__ static Vec ones() {
+    constexpr uint32_t k = 0x3C003C00u;   // two fp16 1.0 values
+    return make_uint4(k, k, k, k);
+  }
+  __device__ static void launder_vec(Vec& v) { launder(v); }
+  __device__ static float get(const void* p, int64_t e) {
+    return __half2float(__ushort_as_half(static_cast<const uint16_t*>(p)[e]));
+  }
+  __device__ static void put(void* p, int64_t e, float f) {
+    static_cast<uint16_t*>(p)[e] = __half_as_ushort(__float2half_rn(f));
+  }
+};
+
+struct V32 {
+  uint4 lo, hi;   // elements 0-3 and 4-7 as fp32 bit patterns
+};
+
+template <>
+struct Io<kF32> {
+  using Vec = V32;
+  static constexpr int kWords = 8;
+  static constexpr int kBytes = 4;
+  __device__ static Vec load(const void* p, int64_t e) {
+    const float* f = static_cast<const float*>(p) + e;
+    return V32{ld_stream16(f), ld_stream16(f + 4)};
+  }
+  __device__ static Vec load_ro(const void* p, int64_t e) {
+    const float* f = static_cast<const float*>(p) + e;
+    return V32{ld_ro16(f), ld_ro16(f + 4)};
+  }
+  __device__ static void store(void* p, int64_t e, const Vec& v) {
+    float* f = static_cast<float*>(p) + e;
+    st16(f, v.lo);
+    st16(f + 4, v.hi);
+  }
+  __device__ static float2 pair(const Vec& v, int i) {
+    const uint4& h = i < 2 ? v.lo : v.hi;
+    return (i & 1) ? make_float2(__uint_as_float(h.z), __uint_as_float(h.w))
+                   : make_float2(__uint_as_float(h.x), __uint_as_float(h.y));
+  }
+  __device__ static Vec pack(float2 a, float2 b, float2 c, float2 d) {
+    return V32{make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b.x),
+                          __float_as_uint(b.y)),
+               make_uint4(__float_as_uint(c.x), __float_as_uint(c.y), __float_as_uint(d.x),
+                          __float_as_uint(d.y))};
+  }
+  __device__ static Vec ones() {
+    constexpr uint32_t k = 0x3F800000u;
+    return V32{make_uint4(k, k, k, k), make_uint4(k, k, k, k)};
+  }
+  __device__ static void launder_vec(Vec& v) {
+    launder(v.lo);
+    launder(v.hi);
+  }
+  __device__ static float get(const void* p, int64_t e) { return static_cast<const float*>(p)[e]; }
+  __device__ static void put(void* p, int64_t e, float f) { static_cast<float*>(p)[e] = f; }
+};
+
+// Sum of squares of a slot's 8 values, as two fp32 partial sums (even, odd).
+template <int FMT>
+__device__ __forceinline__ float2 sumsq8(const typename Io<FMT>::Vec& v, float2 s) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 p = bf2_of(u[i]);
+    const float2 p = Io<FMT>::pair(v, i);
     s = __ffma2_rn(p, p, s);
   }
   return s;
 }
 
-constexpr uint32_t kOnes2 = 0x3F803F80u;   // two bf16 1.0 values
+// round(a + b) for the 8 lanes of two slots.  For bf16 and fp16 the fp32 sum
+// of two values is exact unless their exponents differ by more than 12, and
+// then the smaller is far below half a spacing of the larger, so the one RNE
+// conversion gives the correctly rounded sum; for fp32 it is one rounding.
+template <int FMT>
+__device__ __forceinline__ typename Io<FMT>::Vec add8(const typename Io<FMT>::Vec& a,
+                                                      const typename Io<FMT>::Vec& b) {
+  using I = Io<FMT>;
+  return I::pack(__fadd2_rn(I::pair(a, 0), I::pair(b, 0)), __fadd2_rn(I::pair(a, 1), I::pair(b, 1)),
+                 __fadd2_rn(I::pair(a, 2), I::pair(b, 2)), __fadd2_rn(I::pair(a, 3), I::pair(b, 3)));
+}
 
 // ---- slot map, reduction and epilogue shared by the vectorised kernels ----
 //
@@ -270,27 +402,25 @@ struct SlotMap {
     }
   }
 
-  // Load this thread's slots of one row (fetch(off) returns 16 bytes).
-  template <class Fetch>
-  __device__ __forceinline__ void load(uint4 (&v)[VPL], Fetch&& fetch) const {
+  // Load this thread's slots of one row (fetch(off) returns one slot).
+  template <class Vec, class Fetch>
+  __device__ __forceinline__ void load(Vec (&v)[VPL], Fetch&& fetch) const {
     if constexpr (MODE == kSplitHalf) {
       each_pair([&](int j, int lo, int hi, int, bool ok) {
-        v[2 * j] = ok ? fetch(lo) : make_uint4(0u, 0u, 0u, 0u);
-        v[2 * j + 1] = ok ? fetch(hi) : make_uint4(0u, 0u, 0u, 0u);
+        v[2 * j] = ok ? fetch(lo) : Vec{};
+        v[2 * j + 1] = ok ? fetch(hi) : Vec{};
       });
     } else {
-      each_slot([&](int k, int off, int, bool ok) {
-        v[k] = ok ? fetch(off) : make_uint4(0u, 0u, 0u, 0u);
-      });
+      each_slot([&](int k, int off, int, bool ok) { v[k] = ok ? fetch(off) : Vec{}; });
     }
   }
 };
 
-template <int VPL>
-__device__ __forceinline__ float slots_sumsq(const uint4 (&v)[VPL]) {
+template <int FMT, int VPL>
+__device__ __forceinline__ float slots_sumsq(const typename Io<FMT>::Vec (&v)[VPL]) {
   float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < VPL; ++k) ss = sumsq8(v[k], ss);
+  for (int k = 0; k < VPL; ++k) ss = sumsq8<FMT>(v[k], ss);
   return ss.x + ss.y;
 }
 
@@ -299,52 +429,46 @@ __device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
 }
 
 // Scale (and rotate) the thread's slots of one row and store them.
-template <int MODE, int VPL, int GT>
+template <int MODE, int VPL, int GT, int FMT>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
-                                             uint4 (&v)[VPL], const SlotMap<MODE, VPL, GT>& m,
-                                             float inv_rms) {
+                                             typename Io<FMT>::Vec (&v)[VPL],
+                                             const SlotMap<MODE, VPL, GT>& m, float inv_rms) {
+  using I = Io<FMT>;
+  using Vec = typename I::Vec;
 #pragma unroll
-  for (int k = 0; k < VPL; ++k) launder(v[k]);
+  for (int k = 0; k < VPL; ++k) I::launder_vec(v[k]);
   const bool has_w = a.w != nullptr;
-  uint16_t* yr = a.out + row * a.hidden;
-  const uint4 ones = make_uint4(kOnes2, kOnes2, kOnes2, kOnes2);
+  const int64_t rb = row * a.hidden;
+  const Vec ones = I::ones();
   const float2 inv2 = make_float2(inv_rms, inv_rms);
   if constexpr (MODE == kPlain || MODE == kAddNorm) {
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
-      const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
-      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-      uint32_t o[4];
+      const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
+      float2 o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)   // (x * w) is exact; one rounding by inv_rms
-        o[i] = pack_f2(__fmul2_rn(__fmul2_rn(bf2_of(xu[i]), bf2_of(wu[i])), inv2));
-      st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+      for (int i = 0; i < 4; ++i)   // (x * w) exact for 16-bit formats; one rounding by inv_rms
+        o[i] = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+      I::store(a.out, rb + off, I::pack(o[0], o[1], o[2], o[3]));
     });
     return;
   } else if constexpr (MODE == kAdaLN) {
     // y = n * (1 + scale) + shift with n = (x * w) * inv_rms; one conditioning
     // row serves rows_per_cond rows, so its vectors come from L1/L2
-    const int64_t c = row / a.rows_per_cond;
-    const uint16_t* scr = a.scale + c * a.hidden;
-    const uint16_t* shr = a.shift + c * a.hidden;
+    const int64_t cb = (row / a.rows_per_cond) * a.hidden;
     const float2 one2 = make_float2(1.f, 1.f);
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
-      const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
-      const uint4 sv = ld_ro16(scr + off);
-      const uint4 tv = ld_ro16(shr + off);
-      const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-      const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-      const uint32_t su[4] = {sv.x, sv.y, sv.z, sv.w};
-      const uint32_t tu[4] = {tv.x, tv.y, tv.z, tv.w};
-      uint32_t o[4];
+      const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
+      const Vec sv = I::load_ro(a.scale, cb + off);
+      const Vec tv = I::load_ro(a.shift, cb + off);
+      float2 o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 n = __fmul2_rn(__fmul2_rn(bf2_of(xu[i]), bf2_of(wu[i])), inv2);
-        o[i] = pack_f2(__ffma2_rn(n, __fadd2_rn(one2, bf2_of(su[i])), bf2_of(tu[i])));
+        const float2 n = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+        o[i] = __ffma2_rn(n, __fadd2_rn(one2, I::pair(sv, i)), I::pair(tv, i));
       }
-      st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+      I::store(a.out, rb + off, I::pack(o[0], o[1], o[2], o[3]));
     });
     return;
   } else {
@@ -362,30 +486,26 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       }
       m.each_slot([&](int k, int off, int pair0, bool ok) {
         if (!ok) return;
-        const uint4 wv = has_w ? ld_ro16(a.w + off) : ones;
+        const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
         const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
         const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
         const float2 c[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
         const float2 s[2] = {make_float2(s4.x, s4.y), make_float2(s4.z, s4.w)};
-        const uint32_t xu[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        const uint32_t wu[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t o[4];
+        float2 o[4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          // words 2h and 2h+1 hold pairs 2h and 2h+1: lane x of each float2
-          // is the first pair, lane y the second
-          const uint32_t x0 = xu[2 * h], x1 = xu[2 * h + 1];
-          const uint32_t w0 = wu[2 * h], w1 = wu[2 * h + 1];
-          const float2 u = __fmul2_rn(make_float2(bf_lo(x0), bf_lo(x1)),
-                                      make_float2(bf_lo(w0), bf_lo(w1)));   // a * w, exact
-          const float2 q = __fmul2_rn(make_float2(bf_hi(x0), bf_hi(x1)),
-                                      make_float2(bf_hi(w0), bf_hi(w1)));   // b * w, exact
+          // pairs 2h and 2h+1 of the slot are rotation pairs 2h and 2h+1:
+          // lane x of each float2 is the first of them, lane y the second
+          const float2 x0 = I::pair(v[k], 2 * h), x1 = I::pair(v[k], 2 * h + 1);
+          const float2 w0 = I::pair(wv, 2 * h), w1 = I::pair(wv, 2 * h + 1);
+          const float2 u = __fmul2_rn(make_float2(x0.x, x1.x), make_float2(w0.x, w1.x));   // a * w
+          const float2 q = __fmul2_rn(make_float2(x0.y, x1.y), make_float2(w0.y, w1.y));   // b * w
           const float2 ra = __fmul2_rn(diff_of_products2(u, c[h], q, s[h]), inv2);
-          const float2 rb = __fmul2_rn(diff_of_products2(u, s[h], neg2(q), c[h]), inv2);
-          o[2 * h] = pack_bf2(ra.x, rb.x);
-          o[2 * h + 1] = pack_bf2(ra.y, rb.y);
+          const float2 rb2 = __fmul2_rn(diff_of_products2(u, s[h], neg2(q), c[h]), inv2);
+          o[2 * h] = make_float2(ra.x, rb2.x);
+          o[2 * h + 1] = make_float2(ra.y, rb2.y);
         }
-        st16(yr + off, make_uint4(o[0], o[1], o[2], o[3]));
+        I::store(a.out, rb + off, I::pack(o[0], o[1], o[2], o[3]));
       });
     } else {
       // Same idea: when the pair-vector stride is a multiple of the vectors
@@ -401,8 +521,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       m.each_pair([&](int j, int lo_off, int hi_off, int pair0, bool ok) {
         if (!ok) return;
         const int kl = 2 * j, kh = 2 * j + 1;
-        const uint4 wl = has_w ? ld_ro16(a.w + lo_off) : ones;
-        const uint4 wh = has_w ? ld_ro16(a.w + hi_off) : ones;
+        const Vec wl = has_w ? I::load_ro(a.w, lo_off) : ones;
+        const Vec wh = has_w ? I::load_ro(a.w, hi_off) : ones;
         const float4 c0 = same_cols ? c0h : ld_ro16f(ct + pair0);
         const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
         const float4 s0 = same_cols ? s0h : ld_ro16f(st + pair0);
@@ -411,20 +531,16 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
                              make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
         const float2 s[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
                              make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
-        const uint32_t xl[4] = {v[kl].x, v[kl].y, v[kl].z, v[kl].w};
-        const uint32_t xh[4] = {v[kh].x, v[kh].y, v[kh].z, v[kh].w};
-        const uint32_t wlu[4] = {wl.x, wl.y, wl.z, wl.w};
-        const uint32_t whu[4] = {wh.x, wh.y, wh.z, wh.w};
-        uint32_t ol[4], oh[4];
+        float2 ol[4], oh[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // pairs 2i, 2i+1: (lo word i, hi word i)
-          const float2 u = __fmul2_rn(bf2_of(xl[i]), bf2_of(wlu[i]));   // exact
-          const float2 q = __fmul2_rn(bf2_of(xh[i]), bf2_of(whu[i]));   // exact
-          ol[i] = pack_f2(__fmul2_rn(diff_of_products2(u, c[i], q, s[i]), inv2));
-          oh[i] = pack_f2(__fmul2_rn(diff_of_products2(u, s[i], neg2(q), c[i]), inv2));
+        for (int i = 0; i < 4; ++i) {   // rotation pairs 2i, 2i+1: (lo pair i, hi pair i)
+          const float2 u = __fmul2_rn(I::pair(v[kl], i), I::pair(wl, i));
+          const float2 q = __fmul2_rn(I::pair(v[kh], i), I::pair(wh, i));
+          ol[i] = __fmul2_rn(diff_of_products2(u, c[i], q, s[i]), inv2);
+          oh[i] = __fmul2_rn(diff_of_products2(u, s[i], neg2(q), c[i]), inv2);
         }
-        st16(yr + lo_off, make_uint4(ol[0], ol[1], ol[2], ol[3]));
-        st16(yr + hi_off, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+        I::store(a.out, rb + lo_off, I::pack(ol[0], ol[1], ol[2], ol[3]));
+        I::store(a.out, rb + hi_off, I::pack(oh[0], oh[1], oh[2], oh[3]));
       });
     }
   }
@@ -444,8 +560,9 @@ struct GroupShape {
   static constexpr int kGroupsPerCta = kBlock / kThreadsPerGroup;
 };
 
-// Register budget per thread of the register kernel: the row's 4*VPL words
-// plus what the epilogue needs (weights, and for RoPE the cos/sin vectors).
+// Register budget per thread of the register kernel: the row's kWords*VPL
+// words plus what the epilogue needs (weights, and for RoPE the cos/sin
+// vectors).
 // Capping it lets more warps, hence more bytes of x, be in flight per SM.
 #ifndef LTXK_REG_EXTRA_PLAIN
 #define LTXK_REG_EXTRA_PLAIN 32
@@ -456,26 +573,29 @@ struct GroupShape {
 #ifndef LTXK_REG_EXTRA_SPLIT
 #define LTXK_REG_EXTRA_SPLIT 96
 #endif
-template <int MODE, int VPL>
+template <int MODE, int VPL, int FMT>
 struct RegBudget {
+  static constexpr int kW = Io<FMT>::kWords;
   static constexpr int kRegs =
-      4 * VPL + (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
-                 : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
-                 : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
-                 : MODE == kAddNorm      ? 4 * VPL + LTXK_REG_EXTRA_PLAIN  // x and res in flight
-                                         : LTXK_REG_EXTRA_PLAIN + 16);
+      kW * VPL + (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
+                  : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
+                  : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
+                  : MODE == kAddNorm      ? kW * VPL + LTXK_REG_EXTRA_PLAIN  // x and res in flight
+                                          : LTXK_REG_EXTRA_PLAIN + 16);
 };
-template <int MODE, int G, int VPL>
+template <int MODE, int G, int VPL, int FMT>
 struct VecLaunch {
   static constexpr int kBlock = GroupShape<G>::kBlock;
-  static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, VPL>::kRegs);
+  static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, VPL, FMT>::kRegs);
   static constexpr int kMinBlocks = kMin < 1 ? 1 : kMin;
 };
 
-template <int MODE, int G, int VPL>
-__global__ void __launch_bounds__(VecLaunch<MODE, G, VPL>::kBlock,
-                                  VecLaunch<MODE, G, VPL>::kMinBlocks)
+template <int MODE, int G, int VPL, int FMT>
+__global__ void __launch_bounds__(VecLaunch<MODE, G, VPL, FMT>::kBlock,
+                                  VecLaunch<MODE, G, VPL, FMT>::kMinBlocks)
 rows_vec_kernel(const RowArgs a) {
+  using I = Io<FMT>;
+  using Vec = typename I::Vec;
   using S = GroupShape<G>;
   constexpr int GT = S::kThreadsPerGroup;
   static_assert(MODE != kSplitHalf || VPL % 2 == 0, "split-half slots come in pairs");
@@ -492,27 +612,27 @@ rows_vec_kernel(const RowArgs a) {
   int parity = 0;
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
        row < a.rows; row += row_step) {
-    const uint16_t* xr = a.x + row * a.hidden;
+    const int64_t rb = row * a.hidden;
     if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
       const int64_t ahead = row + LTXK_L2_PREFETCH_ROWS * row_step;
-      if (ahead < a.rows) prefetch_l2(a.x + ahead * a.hidden, static_cast<uint32_t>(a.hidden) * 2u);
+      if (ahead < a.rows)
+        prefetch_l2(static_cast<const char*>(a.x) + ahead * a.hidden * I::kBytes,
+                    static_cast<uint32_t>(a.hidden) * I::kBytes);
     }
-    uint4 v[VPL];
-    m.load(v, [&](int off) { return ld_stream16(xr + off); });
+    Vec v[VPL];
+    m.load(v, [&](int off) { return I::load(a.x, rb + off); });
     if constexpr (MODE == kAddNorm) {
-      // h = bf16(x + res): stored as the new residual stream, then normalised
-      const uint16_t* rr = a.res + row * a.hidden;
-      uint16_t* hr = a.h_out + row * a.hidden;
-      uint4 rv[VPL];
-      m.load(rv, [&](int off) { return ld_stream16(rr + off); });
+      // h = round(x + res): stored as the new residual stream, then normalised
+      Vec rv[VPL];
+      m.load(rv, [&](int off) { return I::load(a.res, rb + off); });
 #pragma unroll
-      for (int k = 0; k < VPL; ++k) v[k] = add_bf16x8(v[k], rv[k]);
+      for (int k = 0; k < VPL; ++k) v[k] = add8<FMT>(v[k], rv[k]);
       m.each_slot([&](int k, int off, int, bool ok) {
-        if (ok) st16(hr + off, v[k]);
+        if (ok) I::store(a.h_out, rb + off, v[k]);
       });
     }
 
-    float ss = warp_sum(slots_sumsq(v));
+    float ss = warp_sum(slots_sumsq<FMT>(v));
     if (G > 1) {
       if (lane == 0) red[parity][group][warp_in_group] = ss;
       if (S::kGroupsPerCta == 1) __syncthreads();
@@ -522,7 +642,7 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    row_epilogue<MODE, VPL, GT>(a, row, v, m, inv_rms_of(ss, a));
+    row_epilogue<MODE, VPL, GT, FMT>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 
@@ -635,7 +755,8 @@ rows_tma_kernel(const TmaArgs ta) {
       const int64_t r = first + i * nwarps;
       if (r >= a.rows) break;
       if (i == 0 && ta.skip_first_copy) continue;
-      bulk_load(ring + i * ta.stage_stride, a.x + r * a.hidden, row_bytes, bars + 8 * i);
+      bulk_load(ring + i * ta.stage_stride, static_cast<const uint16_t*>(a.x) + r * a.hidden,
+                row_bytes, bars + 8 * i);
     }
   }
 
@@ -667,11 +788,12 @@ rows_tma_kernel(const TmaArgs ta) {
         // order this warp's generic-proxy reads of the buffer before the
         // async-proxy write that refills it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        bulk_load(buf, a.x + next * a.hidden, row_bytes, bars + 8 * s);
+        bulk_load(buf, static_cast<const uint16_t*>(a.x) + next * a.hidden, row_bytes,
+                  bars + 8 * s);
       }
     }
-    const float ss = warp_sum(slots_sumsq(v));
-    row_epilogue<MODE, VPL, 32>(a, row, v, m, inv_rms_of(ss, a));
+    const float ss = warp_sum(slots_sumsq<kBf16>(v));
+    row_epilogue<MODE, VPL, 32, kBf16>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 
@@ -695,30 +817,27 @@ __device__ __forceinline__ float block_sum(float v, float* scratch /* [32] */) {
   return t;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kElemBlock)
 rows_elem_kernel(const RowArgs a) {
+  using I = Io<FMT>;
   __shared__ float scratch[32];
   const int64_t H = a.hidden;
   const bool has_w = a.w != nullptr;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
-    const uint16_t* xr = a.x + row * H;
-    uint16_t* yr = a.out + row * H;
+    const int64_t rb = row * H;
     float ss = 0.f;
     if (MODE == kAddNorm) {
-      // h = bf16(x + res), stored as the new residual stream; each thread
+      // h = round(x + res), stored as the new residual stream; each thread
       // reads back only the elements it wrote itself
-      const uint16_t* rr = a.res + row * H;
-      uint16_t* hr = a.h_out + row * H;
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-        const uint16_t hb = f_to_bf(__fadd_rn(bf_to_f(xr[j]), bf_to_f(rr[j])));
-        hr[j] = hb;
-        const float v = bf_to_f(hb);
+        I::put(a.h_out, rb + j, __fadd_rn(I::get(a.x, rb + j), I::get(a.res, rb + j)));
+        const float v = I::get(a.h_out, rb + j);
         ss = __fmaf_rn(v, v, ss);
       }
     } else {
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-        const float v = bf_to_f(xr[j]);
+        const float v = I::get(a.x, rb + j);
         ss = __fmaf_rn(v, v, ss);
       }
     }
@@ -728,18 +847,18 @@ rows_elem_kernel(const RowArgs a) {
     ss = block_sum(ss, scratch);
     const float inv_rms = rsqrtf(__fdiv_rn(ss, static_cast<float>(H)) + a.eps);
     if (MODE == kPlain || MODE == kAddNorm) {
-      const uint16_t* src = MODE == kAddNorm ? a.h_out + row * H : xr;
+      const void* src = MODE == kAddNorm ? static_cast<const void*>(a.h_out) : a.x;
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-        const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
-        yr[j] = f_to_bf(__fmul_rn(__fmul_rn(bf_to_f(src[j]), wj), inv_rms));
+        const float wj = has_w ? I::get(a.w, j) : 1.f;
+        I::put(a.out, rb + j, __fmul_rn(__fmul_rn(I::get(src, rb + j), wj), inv_rms));
       }
     } else if (MODE == kAdaLN) {
-      const int64_t c = row / a.rows_per_cond;
+      const int64_t cb = (row / a.rows_per_cond) * H;
       for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-        const float wj = has_w ? bf_to_f(a.w[j]) : 1.f;
-        const float n = __fmul_rn(__fmul_rn(bf_to_f(xr[j]), wj), inv_rms);
-        const float sc = __fadd_rn(1.f, bf_to_f(a.scale[c * H + j]));
-        yr[j] = f_to_bf(__fmaf_rn(n, sc, bf_to_f(a.shift[c * H + j])));
+        const float wj = has_w ? I::get(a.w, j) : 1.f;
+        const float n = __fmul_rn(__fmul_rn(I::get(a.x, rb + j), wj), inv_rms);
+        const float sc = __fadd_rn(1.f, I::get(a.scale, cb + j));
+        I::put(a.out, rb + j, __fmaf_rn(n, sc, I::get(a.shift, cb + j)));
       }
     } else {
       const int64_t D = a.head_dim, P = D >> 1;
@@ -750,15 +869,15 @@ rows_elem_kernel(const RowArgs a) {
         const int64_t head = q / P, p = q - head * P;
         const int64_t ia = MODE == kInterleaved ? head * D + 2 * p : head * D + p;
         const int64_t ib = MODE == kInterleaved ? ia + 1 : ia + P;
-        const float wa = has_w ? bf_to_f(a.w[ia]) : 1.f;
-        const float wb = has_w ? bf_to_f(a.w[ib]) : 1.f;
-        const float u = __fmul_rn(bf_to_f(xr[ia]), wa);
-        const float v = __fmul_rn(bf_to_f(xr[ib]), wb);
+        const float wa = has_w ? I::get(a.w, ia) : 1.f;
+        const float wb = has_w ? I::get(a.w, ib) : 1.f;
+        const float u = __fmul_rn(I::get(a.x, rb + ia), wa);
+        const float v = __fmul_rn(I::get(a.x, rb + ib), wb);
         const float c = ct[p], s = st[p];
         const float ra = __fmul_rn(diff_of_products(u, c, v, s), inv_rms);
-        const float rb = __fmul_rn(sum_of_products(u, s, v, c), inv_rms);
-        yr[ia] = f_to_bf(ra);
-        yr[ib] = f_to_bf(rb);
+        const float rb2 = __fmul_rn(sum_of_products(u, s, v, c), inv_rms);
+        I::put(a.out, rb + ia, ra);
+        I::put(a.out, rb + ib, rb2);
       }
     }
   }

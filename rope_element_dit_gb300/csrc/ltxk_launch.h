@@ -2,26 +2,42 @@
 // (ltxk_abi.cu) and the translation units that instantiate the kernels.
 #pragma once
 
+#include "ltxk_kernels.cuh"
+
 namespace ltxk {
 
-// Kernel function for (group warps, vector slots per lane), or nullptr if
-// that combination is not instantiated.  One function per pairing mode.
-const void* rows_vec_plain_ptr(int group_warps, int vec_per_lane);
-const void* rows_vec_interleaved_ptr(int group_warps, int vec_per_lane);
-const void* rows_vec_split_ptr(int group_warps, int vec_per_lane);
-const void* rows_vec_adaln_ptr(int group_warps, int vec_per_lane);
-const void* rows_vec_addnorm_ptr(int group_warps, int vec_per_lane);
+// Register kernel of a pairing mode and element format for (group warps,
+// vector slots per lane), or nullptr if that combination is not
+// instantiated; element-wise kernel of a mode and format.  The instance
+// file of each mode defines them for the format it is compiled for.
+template <int MODE, int FMT>
+const void* rows_vec_ptr(int group_warps, int vec_per_lane);
+template <int MODE, int FMT>
+const void* rows_elem_ptr();
 
-// TMA ring kernel for vector slots per lane, or nullptr.
+#define LTXK_DECLARE_ROW_GETTERS(MODE, FMT)                      \
+  template <>                                                    \
+  const void* rows_vec_ptr<MODE, FMT>(int group_warps, int vec_per_lane); \
+  template <>                                                    \
+  const void* rows_elem_ptr<MODE, FMT>();
+#define LTXK_DECLARE_FMT_GETTERS(FMT)          \
+  LTXK_DECLARE_ROW_GETTERS(kPlain, FMT)        \
+  LTXK_DECLARE_ROW_GETTERS(kInterleaved, FMT)  \
+  LTXK_DECLARE_ROW_GETTERS(kSplitHalf, FMT)    \
+  LTXK_DECLARE_ROW_GETTERS(kAdaLN, FMT)        \
+  LTXK_DECLARE_ROW_GETTERS(kAddNorm, FMT)
+LTXK_DECLARE_FMT_GETTERS(kBf16)
+LTXK_DECLARE_FMT_GETTERS(kF16)
+LTXK_DECLARE_FMT_GETTERS(kF32)
+#undef LTXK_DECLARE_FMT_GETTERS
+#undef LTXK_DECLARE_ROW_GETTERS
+
+// TMA ring kernel (bf16 rows) for vector slots per lane, or nullptr.
 const void* rows_tma_plain_ptr(int vec_per_lane);
 const void* rows_tma_interleaved_ptr(int vec_per_lane);
 const void* rows_tma_split_ptr(int vec_per_lane);
 
 // Record a cudaError_t for ltxk_last_cuda_error() (calling thread).
 void record_cuda_error(int e);
-
-// Element-wise kernel for a mode (0 plain, 1 interleaved, 2 split-half,
-// 3 AdaLN, 4 residual add + RMSNorm).
-const void* rows_elem_kernel_ptr(int mode);
 
 }  // namespace ltxk

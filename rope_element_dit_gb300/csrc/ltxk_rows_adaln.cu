@@ -1,7 +1,6 @@
-// Instances of the vectorised row kernel for the AdaLN-modulated RMSNorm.
+// Instances of the row kernels for the AdaLN-modulated RMSNorm, in the
+// element format given by LTXK_FMT (this file is compiled once per format).
 #include "ltxk_instances.cuh"
 #include "ltxk_launch.h"
 
-namespace ltxk {
-const void* rows_vec_adaln_ptr(int g, int vpl) { return select_rows_vec<kAdaLN>(g, vpl); }
-}  // namespace ltxk
+LTXK_DEFINE_ROW_GETTERS(kAdaLN)

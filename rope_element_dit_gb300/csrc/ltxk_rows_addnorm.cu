@@ -1,7 +1,6 @@
-// Instances of the vectorised row kernel for the fused residual add + RMSNorm.
+// Instances of the row kernels for the fused residual add + RMSNorm, in the
+// element format given by LTXK_FMT (this file is compiled once per format).
 #include "ltxk_instances.cuh"
 #include "ltxk_launch.h"
 
-namespace ltxk {
-const void* rows_vec_addnorm_ptr(int g, int vpl) { return select_rows_vec<kAddNorm>(g, vpl); }
-}  // namespace ltxk
+LTXK_DEFINE_ROW_GETTERS(kAddNorm)

@@ -1,8 +1,12 @@
-// Instances of the vectorised row kernel for plain RMSNorm.
+// Instances of the row kernels for plain RMSNorm, in the element format
+// given by LTXK_FMT (this file is compiled once per format).
 #include "ltxk_instances.cuh"
 #include "ltxk_launch.h"
 
+LTXK_DEFINE_ROW_GETTERS(kPlain)
+
+#if LTXK_FMT == 0
 namespace ltxk {
 const void* rows_tma_plain_ptr(int vpl) { return select_rows_tma<kPlain>(vpl); }
-const void* rows_vec_plain_ptr(int g, int vpl) { return select_rows_vec<kPlain>(g, vpl); }
 }  // namespace ltxk
+#endif

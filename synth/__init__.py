@@ -97,8 +97,19 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _chunked(n: int, fn, threads: int | None) -> np.ndarray:
-    out = np.empty(n, dtype=np.uint16)
+# Element formats of generated arrays: bf16 as uint16 bit patterns, the other
+# two as numpy floats (binary64 -> format, round to nearest even).
+FORMATS = {"bf16": np.uint16, "f16": np.float16, "f32": np.float32}
+
+
+def to_format(v: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "bf16":
+        return to_bf16_bits(v)
+    return np.asarray(v, dtype=np.float64).astype(FORMATS[fmt])
+
+
+def _chunked(n: int, fn, threads: int | None, fmt: str = "bf16") -> np.ndarray:
+    out = np.empty(n, dtype=FORMATS[fmt])
     starts = list(range(0, n, _CHUNK))
     if len(starts) <= 1:
         if n:
@@ -116,8 +127,9 @@ def _chunked(n: int, fn, threads: int | None) -> np.ndarray:
 
 
 def normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0,
-                std: float = 1.0, threads: int | None = None) -> np.ndarray:
-    """n draws of N(mean, std^2), rounded to bfloat16 (bit patterns)."""
+                std: float = 1.0, threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
+    """n draws of N(mean, std^2), rounded to bfloat16 (bit patterns), or to
+    float16 / float32 with ``fmt``."""
     key = stream_key(seed, stream)
 
     def fn(s, c):
@@ -125,28 +137,29 @@ def normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0,
         u0 = _unit_open_right(z[0::2])
         u1 = _unit_open_left(z[1::2])
         g = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u0)
-        return to_bf16_bits(mean + std * g)
+        return to_format(mean + std * g, fmt)
 
-    return _chunked(n, fn, threads)
+    return _chunked(n, fn, threads, fmt)
 
 
 def uniform_bf16(seed: int, stream: int, n: int, lo: float, hi: float,
-                 threads: int | None = None) -> np.ndarray:
-    """n draws of U[lo, hi), rounded to bfloat16 (bit patterns)."""
+                 threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
+    """n draws of U[lo, hi), rounded to bfloat16 (bit patterns), or to
+    float16 / float32 with ``fmt``."""
     key = stream_key(seed, stream)
 
     def fn(s, c):
         u = _unit_open_right(raw(key, s, c))
-        return to_bf16_bits(lo + (hi - lo) * u)
+        return to_format(lo + (hi - lo) * u, fmt)
 
-    return _chunked(n, fn, threads)
+    return _chunked(n, fn, threads, fmt)
 
 
 def normal_with_outliers_bf16(seed: int, n: int, frac: float, scale: float,
-                              threads: int | None = None) -> np.ndarray:
+                              threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
     """N(0,1) draws where each element, independently with probability
     ``frac`` (its own uniform from the OUTLIER stream), is multiplied by
-    ``scale`` before the bfloat16 rounding."""
+    ``scale`` before the rounding to bfloat16 (or ``fmt``)."""
     kx = stream_key(seed, STREAM_X)
     ko = stream_key(seed, STREAM_OUTLIER)
 
@@ -156,9 +169,9 @@ def normal_with_outliers_bf16(seed: int, n: int, frac: float, scale: float,
              * np.cos(2.0 * math.pi * _unit_open_right(z[0::2])))
         sel = _unit_open_right(raw(ko, s, c)) < frac
         g = np.where(sel, g * scale, g)
-        return to_bf16_bits(g)
+        return to_format(g, fmt)
 
-    return _chunked(n, fn, threads)
+    return _chunked(n, fn, threads, fmt)
 
 
 # ---- rotary tables (inputs of the fused operation) -------------------------
@@ -218,6 +231,7 @@ class Case:
     op: str = ""                   # "adaln", "add_norm", "gelu", "geglu"
     weight: bool = True            # False: no weight (ones)
     rows_per_cond: int = 0         # AdaLN: rows sharing one conditioning row
+    dtype: str = "bf16"            # element format of x, w, scale, shift, res
 
     @property
     def elements(self) -> int:
@@ -305,6 +319,14 @@ GEGLU = [Case(
     x_dist="normal_outliers", eps=0.0, op="geglu", weight=False,
     meta={"shape": [2, 6144, 16384], "out_shape": [2, 6144, 8192]})]
 
+# The pages' other two precision modes on the largest sweep shape
+# [4, 4096, 3072]: RMSNorm in float16 and in float32, N(0,1) with 1% x50
+# outliers (the sweep's recipe), w ~ N(1, 0.1).
+F16 = [Case(name="rms_norm_f16_4x4096x3072", rows=4 * 4096, hidden=3072, seed=14,
+            x_dist="normal_outliers", eps=1e-6, dtype="f16", meta={"shape": [4, 4096, 3072]})]
+F32 = [Case(name="rms_norm_f32_4x4096x3072", rows=4 * 4096, hidden=3072, seed=15,
+            x_dist="normal_outliers", eps=1e-6, dtype="f32", meta={"shape": [4, 4096, 3072]})]
+
 WORKLOADS = {
     "small": SMALL,
     "sweep": SWEEP,
@@ -315,6 +337,8 @@ WORKLOADS = {
     "add_norm": ADD_NORM,
     "gelu": GELU,
     "geglu": GEGLU,
+    "f16": F16,
+    "f32": F32,
 }
 
 STREAM_SCALE = 3
@@ -324,20 +348,21 @@ STREAM_RESIDUAL = 5
 
 def make_x(case: Case, threads: int | None = None) -> np.ndarray:
     n = case.rows * case.in_width
+    f = case.dtype
     if case.x_dist == "normal":
-        x = normal_bf16(case.seed, STREAM_X, n, threads=threads)
+        x = normal_bf16(case.seed, STREAM_X, n, threads=threads, fmt=f)
     elif case.x_dist == "normal_outliers":
-        x = normal_with_outliers_bf16(case.seed, n, 0.01, 50.0, threads=threads)
+        x = normal_with_outliers_bf16(case.seed, n, 0.01, 50.0, threads=threads, fmt=f)
     elif case.x_dist == "uniform4":
-        x = uniform_bf16(case.seed, STREAM_X, n, -4.0, 4.0, threads=threads)
+        x = uniform_bf16(case.seed, STREAM_X, n, -4.0, 4.0, threads=threads, fmt=f)
     else:
         raise ValueError(case.x_dist)
     return x.reshape(case.rows, case.in_width)
 
 
 def make_w(case: Case) -> np.ndarray:
-    """Weight ~ N(1, 0.1), bfloat16."""
-    return normal_bf16(case.seed, STREAM_WEIGHT, case.hidden, 1.0, 0.1)
+    """Weight ~ N(1, 0.1), in the case's format."""
+    return normal_bf16(case.seed, STREAM_WEIGHT, case.hidden, 1.0, 0.1, fmt=case.dtype)
 
 
 def make_tables(case: Case):
@@ -359,8 +384,10 @@ def make_cond(case: Case):
     if case.kind != "adaln":
         return None, None
     n = case.n_cond * case.hidden
-    sc = normal_bf16(case.seed, STREAM_SCALE, n, 0.0, case.meta.get("scale_std", 0.5))
-    sh = normal_bf16(case.seed, STREAM_SHIFT, n, 0.0, case.meta.get("shift_std", 0.5))
+    sc = normal_bf16(case.seed, STREAM_SCALE, n, 0.0, case.meta.get("scale_std", 0.5),
+                     fmt=case.dtype)
+    sh = normal_bf16(case.seed, STREAM_SHIFT, n, 0.0, case.meta.get("shift_std", 0.5),
+                     fmt=case.dtype)
     return sc.reshape(case.n_cond, case.hidden), sh.reshape(case.n_cond, case.hidden)
 
 
@@ -370,7 +397,7 @@ def make_inputs(case: Case, threads: int | None = None) -> dict:
     res = None
     if case.kind == "add_norm":
         res = normal_bf16(case.seed, STREAM_RESIDUAL, case.elements,
-                          threads=threads).reshape(case.rows, case.hidden)
+                          threads=threads, fmt=case.dtype).reshape(case.rows, case.hidden)
     return {"x": make_x(case, threads), "w": make_w(case) if case.weight else None,
             "cos": cos, "sin": sin, "scale": scale, "shift": shift, "res": res}
 
@@ -384,11 +411,12 @@ def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
         return 4 * case.rows * case.hidden
     if case.kind == "geglu":
         return 6 * case.rows * case.hidden
-    b = 4 * case.rows * case.hidden + (2 * case.hidden if case.weight else 0)
+    e = 4 if case.dtype == "f32" else 2
+    b = 2 * e * case.rows * case.hidden + (e * case.hidden if case.weight else 0)
     if case.kind == "add_norm":
-        b += 4 * case.rows * case.hidden          # read the residual, write h
+        b += 2 * e * case.rows * case.hidden      # read the residual, write h
     if case.kind == "adaln":
-        b += 2 * 2 * case.n_cond * case.hidden
+        b += 2 * e * case.n_cond * case.hidden
     if case.mode is not None:
         P = case.head_dim // 2
         table_rows = case.rows if per_row_tables else case.seq_len

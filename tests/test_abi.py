@@ -301,3 +301,41 @@ def test_geglu_validation(L):
     assert f(A, A, 4, 8, None) == L.ERR_OVERLAP          # out inside x: never in place
     assert f(A + 120, A, 4, 8, None) == L.ERR_OVERLAP    # last bytes of x
     assert f(A, B, 0, 8, None) == L.OK
+
+
+def test_plans_per_format(L):
+    """fp32 rows use at most 8 slots per lane; the TMA ring stays bf16-only."""
+    old = L.ltxk_set_path(L.PATH_TMA)
+    try:
+        for op in (L.OP_RMS_NORM, L.OP_RMS_NORM_ROPE):
+            st, p = L.ltxk_plan_launch_dt(op, L.DTYPE_F16, 64, 2048, 64, 1, True)
+            assert st == L.OK and p.kernel == L.KERNEL_ROWS_VEC
+        st, p = L.ltxk_plan_launch_dt(L.OP_RMS_NORM, L.DTYPE_BF16, 64, 2048, 0, 0, True)
+        assert st == L.OK and p.kernel == L.KERNEL_ROWS_TMA
+    finally:
+        L.ltxk_set_path(old)
+    st, p = L.ltxk_plan_launch_dt(L.OP_RMS_NORM, L.DTYPE_F32, 64, 4096 * 3, 0, 0, True)
+    assert st == L.OK and p.vec_per_lane <= 8
+
+
+def test_dtype_validation(L):
+    """Unknown dtypes and element-size rules come back before any CUDA call."""
+    assert L.ltxk_rms_norm_dt(A, B, W, 4, 8, 1e-6, 3, None) == L.ERR_DTYPE
+    assert L.ltxk_rms_norm_dt(None, B, W, 4, 8, 1e-6, -1, None) == L.ERR_DTYPE
+    assert L.ltxk_rms_norm_rope_dt(A, B, W, C, C, 4, 2, 8, 0, 1e-6, 4, 7, None) == L.ERR_DTYPE
+    assert L.ltxk_rms_norm_adaln_dt(A, B, W, C, C, 4, 8, 2, 1e-6, 9, None) == L.ERR_DTYPE
+    assert L.ltxk_add_rms_norm_dt(A, C, B, W, None, 4, 8, 1e-6, 5, None) == L.ERR_DTYPE
+    st, _ = L.ltxk_plan_launch_dt(L.OP_RMS_NORM, 3, 4, 8, 0, 0, True)
+    assert st == L.ERR_DTYPE
+    # fp32 elements need 4-byte alignment; 2 bytes is enough for the 16-bit types
+    assert L.ltxk_rms_norm_dt(A, B + 2, W, 4, 8, 1e-6, L.DTYPE_F32, None) == L.ERR_ALIGN
+    assert L.ltxk_rms_norm_dt(A, B + 2, W, 0, 8, 1e-6, L.DTYPE_F16, None) == L.OK
+    # overlap is measured in bytes of the element type: 4 x 8 fp32 = 128 bytes
+    assert L.ltxk_rms_norm_dt(A, A + 96, None, 4, 8, 1e-6, L.DTYPE_F32, None) == L.ERR_OVERLAP
+    assert L.ltxk_rms_norm_dt(A, A + 64, None, 0, 8, 1e-6, L.DTYPE_F16, None) == L.OK
+    assert L.ltxk_rms_norm_dt(A, B, A + 100, 4, 8, 1e-6, L.DTYPE_F32, None) == L.ERR_OVERLAP
+    assert L.ltxk_add_rms_norm_dt(A, A + 64, B, C, None, 4, 8, 1e-6, L.DTYPE_F32,
+                                  None) == L.ERR_OVERLAP
+    assert L.ltxk_rms_norm_adaln_dt(A, B, None, A + 124, C, 4, 8, 2, 1e-6, L.DTYPE_F32,
+                                    None) == L.ERR_OVERLAP
+    assert L.ltxk_status_string(L.ERR_DTYPE) == "unknown element type"

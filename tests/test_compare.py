@@ -45,3 +45,32 @@ def test_bounded_rule_accepts_rounding_and_rejects_errors():
     assert compare_bf16_bounded(off, ye, bound)["over_tolerance"] > 0.99 * y.size
     # (three steps can cross a binade edge, where the spacing doubles)
     assert compare_bf16_bounded(off, ye, 8 * spacing_bf16(ye))["ok"]
+
+
+def test_compare_fmt_neighbours_and_nan():
+    from oracle.compare import compare_fmt
+    for dt in (np.float16, np.float32):
+        a = np.array([1.0, -2.0, 0.0, np.nan, 65000.0 if dt == np.float16 else 3e38], dt)
+        b = np.nextafter(a, dt(np.inf)).astype(dt)
+        b[3] = np.nan
+        r = compare_fmt(b, a)
+        assert r["ok"] and r["one_ulp"] == 4, r
+        c = np.nextafter(b, dt(np.inf)).astype(dt)
+        assert not compare_fmt(c, a)["ok"]
+        assert compare_fmt(np.array([-0.0], dt), np.array([0.0], dt))["exact"] == 1
+        assert not compare_fmt(np.array([np.nan], dt), np.array([1.0], dt))["ok"]
+
+
+def test_compare_fmt_bounded_rejects_a_few_ulp_off():
+    from oracle.compare import compare_fmt_bounded
+    for dt in (np.float16, np.float32):
+        exact = np.linspace(0.5, 3.0, 101)
+        got = exact.astype(dt)
+        assert compare_fmt_bounded(got, exact, 0.0)["ok"]
+        off = got.copy()
+        for _ in range(3):
+            off = np.nextafter(off, dt(np.inf)).astype(dt)
+        assert not compare_fmt_bounded(off, exact, 0.0)["ok"]
+        # a bound of 4 spacings accepts them again
+        sp = np.abs(np.nextafter(got, dt(np.inf)).astype(np.float64) - got)
+        assert compare_fmt_bounded(off, exact, 4 * sp)["ok"]
