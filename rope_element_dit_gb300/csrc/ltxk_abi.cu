@@ -49,6 +49,12 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+// Multiplier for the kernels' div_fast: floor((2^64 - 1) / d) + 1 for
+// 2 <= d < 2^32, else 0 (the kernel divides).
+uint64_t div_mul(int64_t d) {
+  return (d < 2 || d >= (int64_t{1} << 32)) ? 0 : UINT64_MAX / static_cast<uint64_t>(d) + 1;
+}
+
 int max_vpl(int fmt) { return fmt == ltxk::kF32 ? 8 : kMaxVplSlots; }
 
 int elem_bytes(int fmt) { return fmt == ltxk::kF32 ? 4 : 2; }
@@ -378,6 +384,7 @@ int rope_common(void* out, const void* x, const void* w, const float* cos, const
   const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
                          aligned_to(cos, 16) && aligned_to(sin, 16);
   ltxk::RowArgs a{out, x, w, cos, sin, rows, table_rows, static_cast<int>(hidden), head_dim, eps};
+  a.table_mul = div_mul(table_rows);
   return launch(LTXK_OP_RMS_NORM_ROPE, mode, fmt, a, vector_ok, stream, g_path.load());
 }
 
@@ -424,6 +431,7 @@ int adaln_fmt(void* out, const void* x, const void* w, const void* scale, const 
                          aligned_to(scale, 16) && aligned_to(shift, 16);
   ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps,
                   scale, shift, rows_per_cond};
+  a.cond_mul = div_mul(rows_per_cond);
   return launch(LTXK_OP_RMS_NORM_ADALN, 0, fmt, a, vector_ok, stream, g_path.load());
 }
 

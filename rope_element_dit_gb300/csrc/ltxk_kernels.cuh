@@ -63,7 +63,22 @@ struct RowArgs {
   int64_t rows_per_cond;    // AdaLN: row r uses conditioning row r / rows_per_cond
   const void* res;          // residual add: [rows, hidden] residual in
   void* h_out;              // residual add: [rows, hidden] h = x + res out
+  uint64_t table_mul;       // div_fast multiplier of table_rows (0: divide)
+  uint64_t cond_mul;        // div_fast multiplier of rows_per_cond (0: divide)
 };
+
+// n / d for n >= 0, d >= 1, given m = floor((2^64 - 1) / d) + 1 for
+// 2 <= d < 2^32 and m = 0 otherwise (W. Granlund and P. Montgomery, "Division
+// by invariant integers using multiplication", PLDI 1994: a rounded-up
+// reciprocal and a high product).  For n < 2^32, n*m / 2^64 exceeds n/d by
+// less than n / 2^64 < 1/d, which cannot carry past the next integer, so
+// the high 64 bits of n*m are the quotient: one 64-bit multiply-high instead
+// of a 64-bit division.
+__device__ __forceinline__ int64_t div_fast(int64_t n, int64_t d, uint64_t m) {
+  if (m != 0 && n < (int64_t{1} << 32))
+    return static_cast<int64_t>(__umul64hi(static_cast<uint64_t>(n), m));
+  return d == 1 ? n : n / d;
+}
 
 // ---- element helpers -----------------------------------------------------
 
@@ -140,6 +155,21 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
+
+// Bring the line holding p toward the SM (1: into L1, 2: into L2) without
+// holding a register.
+template <int LEVEL>
+__device__ __forceinline__ void prefetch_line(const void* p) {
+  if constexpr (LEVEL == 1) asm volatile("prefetch.global.L1 [%0];" :: "l"(p));
+  else asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+// Fused kernels: prefetch the row's cos/sin columns right after the row's
+// loads are issued, so that their first touch (cold after the row's start)
+// overlaps the wait for x instead of following it (0 = off, 1 = L1, 2 = L2).
+#ifndef LTXK_TABLE_PREFETCH
+#define LTXK_TABLE_PREFETCH 0
+#endif
 
 // Rows ahead that the register kernel asks the bulk-copy engine to bring
 // into L2 (0 = off).
@@ -455,7 +485,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   } else if constexpr (MODE == kAdaLN) {
     // y = n * (1 + scale) + shift with n = (x * w) * inv_rms; one conditioning
     // row serves rows_per_cond rows, so its vectors come from L1/L2
-    const int64_t cb = (row / a.rows_per_cond) * a.hidden;
+    const int64_t cb = div_fast(row, a.rows_per_cond, a.cond_mul) * a.hidden;
     const float2 one2 = make_float2(1.f, 1.f);
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
@@ -472,7 +502,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
     });
     return;
   } else {
-    const int64_t pos = row % a.table_rows;
+    const int64_t pos = row - div_fast(row, a.table_rows, a.table_mul) * a.table_rows;
     const float* ct = a.cos_t + pos * m.P;
     const float* st = a.sin_t + pos * m.P;
     if constexpr (MODE == kInterleaved) {
@@ -573,15 +603,31 @@ struct GroupShape {
 #ifndef LTXK_REG_EXTRA_SPLIT
 #define LTXK_REG_EXTRA_SPLIT 96
 #endif
+#ifndef LTXK_REG_EXTRA_ADALN
+#define LTXK_REG_EXTRA_ADALN (LTXK_REG_EXTRA_PLAIN + 16)
+#endif
+// Software pipelining of the register kernel: a warp issues the loads of
+// its next row before the epilogue of the current one, so HBM reads keep
+// flowing while rows are scaled and stored (costs one more row of slots in
+// registers).  Not for the residual-add form (two rows of inputs already).
+#ifndef LTXK_PIPELINE
+#define LTXK_PIPELINE 0
+#endif
+template <int MODE>
+struct Pipelined {
+  static constexpr bool value = LTXK_PIPELINE != 0 && MODE != kAddNorm;
+};
+
 template <int MODE, int VPL, int FMT>
 struct RegBudget {
   static constexpr int kW = Io<FMT>::kWords;
   static constexpr int kRegs =
-      kW * VPL + (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
+      kW * VPL * (Pipelined<MODE>::value ? 2 : 1) +
+                 (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
                   : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
                   : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
                   : MODE == kAddNorm      ? kW * VPL + LTXK_REG_EXTRA_PLAIN  // x and res in flight
-                                          : LTXK_REG_EXTRA_PLAIN + 16);
+                                          : LTXK_REG_EXTRA_ADALN);
 };
 template <int MODE, int G, int VPL, int FMT>
 struct VecLaunch {
@@ -609,9 +655,13 @@ rows_vec_kernel(const RowArgs a) {
   const SlotMap<MODE, VPL, GT> m(a, t);
 
   const int64_t row_step = static_cast<int64_t>(gridDim.x) * S::kGroupsPerCta;
+  constexpr bool kPipe = Pipelined<MODE>::value;
   int parity = 0;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
-       row < a.rows; row += row_step) {
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
+  Vec v[VPL];
+  if (kPipe && first < a.rows)
+    m.load(v, [&](int off) { return I::load(a.x, first * a.hidden + off); });
+  for (int64_t row = first; row < a.rows; row += row_step) {
     const int64_t rb = row * a.hidden;
     if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
       const int64_t ahead = row + LTXK_L2_PREFETCH_ROWS * row_step;
@@ -619,8 +669,19 @@ rows_vec_kernel(const RowArgs a) {
         prefetch_l2(static_cast<const char*>(a.x) + ahead * a.hidden * I::kBytes,
                     static_cast<uint32_t>(a.hidden) * I::kBytes);
     }
-    Vec v[VPL];
-    m.load(v, [&](int off) { return I::load(a.x, rb + off); });
+    Vec nv[kPipe ? VPL : 1];
+    if constexpr (kPipe) {
+      const int64_t next = row + row_step;
+      if (next < a.rows) m.load(nv, [&](int off) { return I::load(a.x, next * a.hidden + off); });
+    } else {
+      m.load(v, [&](int off) { return I::load(a.x, rb + off); });
+    }
+    if constexpr ((MODE == kInterleaved || MODE == kSplitHalf) && LTXK_TABLE_PREFETCH > 0) {
+      const int64_t pos = row - div_fast(row, a.table_rows, a.table_mul) * a.table_rows;
+      const int col = MODE == kInterleaved ? (m.a0 >> 1) : m.b0 * 8;
+      prefetch_line<LTXK_TABLE_PREFETCH>(a.cos_t + pos * m.P + col);
+      prefetch_line<LTXK_TABLE_PREFETCH>(a.sin_t + pos * m.P + col);
+    }
     if constexpr (MODE == kAddNorm) {
       // h = round(x + res): stored as the new residual stream, then normalised
       Vec rv[VPL];
@@ -643,6 +704,10 @@ rows_vec_kernel(const RowArgs a) {
       parity ^= 1;
     }
     row_epilogue<MODE, VPL, GT, FMT>(a, row, v, m, inv_rms_of(ss, a));
+    if constexpr (kPipe) {
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) v[k] = nv[k];
+    }
   }
 }
 
