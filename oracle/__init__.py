@@ -97,6 +97,9 @@ def _load():
             lib.oracle_rms_norm_adaln_fmt.restype = I32
             lib.oracle_add_rms_norm_fmt.argtypes = [I32, P, P, P, P, P, I64, I64, F32, P]
             lib.oracle_add_rms_norm_fmt.restype = I32
+            lib.oracle_rope_positions.argtypes = [I32, P, P, I64, I64, I64, I32, I64, I64, I64,
+                                                  I64, I64, I64, ctypes.c_double, I64, P]
+            lib.oracle_rope_positions.restype = I32
             lib.oracle_gelu_tanh.argtypes = [P, P, I64, P]
             lib.oracle_gelu_tanh.restype = None
             lib.oracle_geglu.argtypes = [P, P, I64, I64, P]
@@ -312,6 +315,41 @@ def add_rms_norm(x, res, w, eps, *, threads: int = 1, exact: bool = False):
     _run_blocks(run, rows, threads)
     y, h = y.reshape(x.shape), h.reshape(x.shape)
     return (y, h, ye.reshape(x.shape)) if exact else (y, h)
+
+
+def rope(x, heads, head_dim, mode, grid, pairs, theta=10000.0, *, threads: int = 1,
+         exact: bool = False):
+    """Oracle standalone RoPE with angles from token positions.
+
+    ``x``: [rows, heads*head_dim] (bf16 bits, float16 or float32); row r is
+    token ``r mod (T*H*W)`` of ``grid = (T, H, W)``; ``pairs = (nt, nh, nw)``
+    split the head_dim/2 pairs over the axes (1D text: ``grid = (S, 1, 1)``,
+    ``pairs = (head_dim/2, 0, 0)``).  Pair k of an axis with n pairs turns by
+    ``coordinate * theta**(-k/n)``.
+    """
+    fmt, x = _elems(x, "x")
+    HD = heads * head_dim
+    if x.shape[-1] != HD:
+        raise ValueError("last axis of x must be heads*head_dim")
+    rows = x.size // HD
+    x2 = x.reshape(rows, HD)
+    y = np.empty_like(x2)
+    ye = np.empty(x2.shape, np.float64) if exact else None
+    T, H, W = grid
+    nt, nh, nw = pairs
+    lib = _load()
+
+    def run(block):
+        r0, r1 = block
+        rc = lib.oracle_rope_positions(fmt, _ptr(y[r0:r1]), _ptr(x2[r0:r1]), r1 - r0, heads,
+                                       head_dim, mode, T, H, W, nt, nh, nw, float(theta), r0,
+                                       None if ye is None else _ptr(ye[r0:r1]))
+        if rc != 0:
+            raise RuntimeError(f"oracle_rope_positions failed ({rc})")
+
+    _run_blocks(run, rows, threads)
+    y = y.reshape(x.shape)
+    return (y, ye.reshape(x.shape)) if exact else y
 
 
 def gelu_tanh(x, *, threads: int = 1, exact: bool = False):

@@ -359,6 +359,77 @@ int oracle_add_rms_norm(uint16_t* y, uint16_t* h, const uint16_t* x,
     return oracle_add_rms_norm_fmt(FMT_BF16, y, h, x, res, w, rows, H, eps, y_exact);
 }
 
+/* ---- standalone RoPE with angles from token positions -------------------
+ *
+ * "cuda-kernels" page, "Kernel-Specific Guidelines / RoPE": x is
+ * [batch, seq, heads, head_dim] (1D text) or [batch, t*h*w, heads, head_dim]
+ * (3D video), and LTX-Video computes its own rotary angles.  The pages give
+ * no frequency formula; the definition used (the one the table inputs of the
+ * fused form are built with):
+ *   token s = r mod (T*H*W) of row r has coordinates
+ *     (ct, ch, cw) = (s / (H*W), (s / W) mod H, s mod W);
+ *   the head_dim/2 pairs split into consecutive groups of nt, nh, nw pairs
+ *   (axis t, then h, then w; 1D text is nt = head_dim/2 with H = W = 1);
+ *   pair k of an axis with n pairs turns by angle = coordinate * theta^(-k/n);
+ *   a' = a cos - b sin, b' = a sin + b cos on the pairs of every head, with
+ *   the pairing of `mode` as for the fused form; one rounding to the format.
+ * No normalisation: y is x rotated. */
+static void rope_angles(int64_t s, int64_t T, int64_t H, int64_t W,
+                        int64_t nt, int64_t nh, int64_t nw, double theta,
+                        double* c, double* sn) {
+    (void)T;
+    const int64_t coord[3] = {s / (H * W), (s / W) % H, s % W};
+    const int64_t n[3] = {nt, nh, nw};
+    int64_t p = 0;
+    for (int axis = 0; axis < 3; ++axis) {
+        for (int64_t k = 0; k < n[axis]; ++k, ++p) {
+            const double ang = (double)coord[axis] * pow(theta, -(double)k / (double)n[axis]);
+            c[p] = cos(ang);
+            sn[p] = sin(ang);
+        }
+    }
+}
+
+/* x, y: [rows, heads*head_dim] in format fmt; row r is token
+ * (first_row + r) mod (T*H*W).  Returns 0, -1 on allocation failure, -2 on
+ * an invalid argument. */
+int oracle_rope_positions(int fmt, void* y, const void* x, int64_t rows,
+                          int64_t heads, int64_t head_dim, int mode,
+                          int64_t T, int64_t H, int64_t W,
+                          int64_t nt, int64_t nh, int64_t nw, double theta,
+                          int64_t first_row, double* y_exact) {
+    if (fmt < FMT_BF16 || fmt > FMT_F32) return -2;
+    if (heads <= 0 || head_dim <= 0 || head_dim % 2 != 0 || (mode != 0 && mode != 1))
+        return -2;
+    if (T <= 0 || H <= 0 || W <= 0 || nt < 0 || nh < 0 || nw < 0 ||
+        nt + nh + nw != head_dim / 2 || !(theta > 0.0) || first_row < 0)
+        return -2;
+    const int64_t P = head_dim / 2, HD = heads * head_dim;
+    double* c = (double*)malloc((size_t)P * sizeof(double));
+    double* sn = (double*)malloc((size_t)P * sizeof(double));
+    if (!c || !sn) { free(c); free(sn); return -1; }
+    for (int64_t r = 0; r < rows; ++r) {
+        rope_angles((first_row + r) % (T * H * W), T, H, W, nt, nh, nw, theta, c, sn);
+        for (int64_t h = 0; h < heads; ++h) {
+            for (int64_t p = 0; p < P; ++p) {
+                int64_t ia, ib;
+                if (mode == 0) { ia = h * head_dim + 2 * p; ib = ia + 1; }
+                else           { ia = h * head_dim + p;     ib = ia + P; }
+                const double a = load_elem(fmt, x, r * HD + ia);
+                const double b = load_elem(fmt, x, r * HD + ib);
+                const double ya = a * c[p] - b * sn[p];
+                const double yb = a * sn[p] + b * c[p];
+                if (y_exact) { y_exact[r * HD + ia] = ya; y_exact[r * HD + ib] = yb; }
+                store_elem(fmt, y, r * HD + ia, ya);
+                store_elem(fmt, y, r * HD + ib, yb);
+            }
+        }
+    }
+    free(c);
+    free(sn);
+    return 0;
+}
+
 /* tanh-approximated GELU of one value, binary64. */
 static double gelu_tanh(double x) {
     const double z = sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x);

@@ -680,3 +680,105 @@ def test_formats_reject_mixed_dtypes(oracle_mod):
         oracle_mod.rms_norm(x, np.ones(8, np.float32), 1e-6)
     with pytest.raises(TypeError):
         oracle_mod.rms_norm(x.astype(np.float64), None, 1e-6)
+
+
+# ---- standalone RoPE with angles from token positions ("Kernel-Specific
+# Guidelines / RoPE": 1D [batch, seq, heads, head_dim], 3D [batch, t*h*w,
+# heads, head_dim]) ----------------------------------------------------------
+
+def _unit_pairs(rows, heads, D, mode, which):
+    """Rows whose every rotation pair is (1, 0) (which=0) or (0, 1) (which=1),
+    as float32 (exact in every format)."""
+    x = np.zeros((rows, heads, D), np.float32)
+    P = D // 2
+    if mode == 0:
+        x[:, :, which::2] = 1.0
+    else:
+        x[:, :, which * P:(which + 1) * P] = 1.0
+    return x.reshape(rows, heads * D)
+
+
+def _pair(ye, heads, D, mode, p):
+    """(first, second) element of pair p of head 0 of every row."""
+    P = D // 2
+    ia, ib = (2 * p, 2 * p + 1) if mode == 0 else (p, p + P)
+    return ye[:, ia], ye[:, ib]
+
+
+def test_rope_positions_identity_at_token_zero(oracle_mod):
+    x = synth.normal_bf16(90, 0, 3 * 4 * 16).reshape(3, 64)
+    for mode in (0, 1):
+        y = oracle_mod.rope(x, 4, 16, mode, (1, 1, 1), (8, 0, 0))
+        assert np.array_equal(y, x)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_positions_closed_form_frequencies(oracle_mod, mode):
+    """1D, head_dim 128, theta 1e4: pair k turns by position * 1e4^(-k/64);
+    pair 32 by position/100 and pair 16 by position/10 (exact in reals), and
+    pair 0 by the position itself.  Row 100 is position 100."""
+    import math
+    D = 128
+    for which in (0, 1):
+        x = _unit_pairs(101, 1, D, mode, which)
+        _, ye = oracle_mod.rope(x, 1, D, mode, (4096, 1, 1), (64, 0, 0), 10000.0, exact=True)
+        for p, ang in ((32, 1.0), (16, 10.0), (0, 100.0)):
+            a, b = _pair(ye, 1, D, mode, p)
+            if which == 0:   # (1, 0) -> (cos, sin)
+                assert abs(a[100] - math.cos(ang)) < 1e-13 and abs(b[100] - math.sin(ang)) < 1e-13
+            else:            # (0, 1) -> (-sin, cos)
+                assert abs(a[100] + math.sin(ang)) < 1e-13 and abs(b[100] - math.cos(ang)) < 1e-13
+
+
+def test_rope_positions_three_axis_coordinates(oracle_mod):
+    """Grid (3, 4, 5), pairs (2, 3, 3): token (1*4 + 2)*5 + 3 = 33 has
+    coordinates (1, 2, 3); the first pair of each axis turns by the
+    coordinate, the second pair of the two-pair t axis by 1e4^(-1/2) = 0.01."""
+    import math
+    D = 16
+    x = _unit_pairs(34, 1, D, 0, 0)
+    _, ye = oracle_mod.rope(x, 1, D, 0, (3, 4, 5), (2, 3, 3), 10000.0, exact=True)
+    for p, ang in ((0, 1.0), (2, 2.0), (5, 3.0), (1, 0.01)):
+        a, b = _pair(ye, 1, D, 0, p)
+        assert abs(a[33] - math.cos(ang)) < 1e-13 and abs(b[33] - math.sin(ang)) < 1e-13
+
+
+def test_rope_positions_angle_is_additive_in_position(oracle_mod):
+    """cos(t(p+q)) = cos(tp)cos(tq) - sin(tp)sin(tq) for every pair: the angle
+    is linear in the position, with no offset."""
+    D = 32
+    x = _unit_pairs(40, 1, D, 0, 0)
+    _, ye = oracle_mod.rope(x, 1, D, 0, (64, 1, 1), (16, 0, 0), 500.0, exact=True)
+    c, s = ye[:, 0::2], ye[:, 1::2]
+    for p, q in ((3, 5), (7, 11), (0, 13), (19, 20)):
+        assert np.allclose(c[p + q], c[p] * c[q] - s[p] * s[q], atol=1e-12)
+        assert np.allclose(s[p + q], s[p] * c[q] + c[p] * s[q], atol=1e-12)
+
+
+def test_rope_positions_norms_wrap_and_permutation(oracle_mod):
+    heads, D = 3, 12
+    x = synth.normal_bf16(91, 0, 50 * heads * D).reshape(50, heads * D)
+    grid, pairs = (2, 3, 4), (2, 2, 2)
+    y0, e0 = oracle_mod.rope(x, heads, D, 0, grid, pairs, exact=True)
+    xw = oracle_mod.widen_bf16(x).reshape(50, heads, D // 2, 2)
+    ew = e0.reshape(50, heads, D // 2, 2)
+    assert np.allclose(np.hypot(ew[..., 0], ew[..., 1]), np.hypot(xw[..., 0], xw[..., 1]),
+                       rtol=1e-14, atol=1e-300)
+    # row r and row r + 24 are the same token
+    y1 = oracle_mod.rope(np.concatenate([x[24:48], x[:24]]), heads, D, 0, grid, pairs)
+    assert np.array_equal(y1[:24], y0[24:48]) and np.array_equal(y1[24:48], y0[:24])
+    # row blocks on several threads keep their tokens
+    assert np.array_equal(oracle_mod.rope(x, heads, D, 0, grid, pairs, threads=4), y0)
+    # split-half is interleaved under the pair permutation
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])
+    xs = x.reshape(50, heads, D)[:, :, perm].reshape(50, heads * D)
+    ys = oracle_mod.rope(xs, heads, D, 1, grid, pairs)
+    assert np.array_equal(ys.reshape(50, heads, D)[:, :, np.argsort(perm)].reshape(50, -1), y0)
+
+
+def test_rope_positions_rejects_bad_arguments(oracle_mod):
+    x = np.zeros((2, 16), np.uint16)
+    for grid, pairs, theta in (((2, 1, 1), (3, 0, 0), 1e4), ((0, 1, 1), (4, 0, 0), 1e4),
+                               ((2, 1, 1), (4, 0, 0), 0.0), ((2, 1, 1), (5, -1, 0), 1e4)):
+        with pytest.raises(RuntimeError):
+            oracle_mod.rope(x, 2, 8, 0, grid, pairs, theta)

@@ -65,6 +65,16 @@ MUTANTS = [
     ("f32_round_emin", "round_binary(v, 24, -126, 127)", "round_binary(v, 24, -125, 127)"),
     ("f16_read_as_bf16", "return fmt == FMT_F16 ? widen_f16(b) : widen_bf16(b);",
      "return widen_bf16(b);"),
+    ("rpos_exponent_doubled", "pow(theta, -(double)k / (double)n[axis])",
+     "pow(theta, -2.0 * (double)k / (double)n[axis])"),
+    ("rpos_axes_reversed", "{s / (H * W), (s / W) % H, s % W}", "{s % W, (s / W) % H, s / (H * W)}"),
+    ("rpos_w_h_swapped", "{s / (H * W), (s / W) % H, s % W}", "{s / (H * W), s % W, (s / W) % H}"),
+    ("rpos_ignores_first_row", "rope_angles((first_row + r) % (T * H * W)",
+     "rope_angles((r) % (T * H * W)"),
+    ("rpos_sign_a", "const double ya = a * c[p] - b * sn[p];", "const double ya = a * c[p] + b * sn[p];"),
+    ("rpos_sign_b", "const double yb = a * sn[p] + b * c[p];", "const double yb = b * c[p] - a * sn[p];"),
+    ("rpos_position_plus_one", "const double ang = (double)coord[axis] *",
+     "const double ang = (double)(coord[axis] + 1) *"),
     ("f32_stored_as_f16", "if (fmt == FMT_F32) ((float*)p)[i] = round_to_f32(v);",
      "if (fmt == FMT_F32) ((float*)p)[i] = (float)widen_f16(round_to_f16(v));"),
 ]
@@ -117,6 +127,12 @@ def _pin_calls():
         ("fmt_shared_f32", pins.test_formats_share_the_arithmetic, (np.float32,)),
         ("fmt_torch_f16", pins.test_formats_match_torch_rms_norm_fp64, (np.float16,)),
         ("fmt_torch_f32", pins.test_formats_match_torch_rms_norm_fp64, (np.float32,)),
+        ("rpos_identity", pins.test_rope_positions_identity_at_token_zero, ()),
+        ("rpos_closed0", pins.test_rope_positions_closed_form_frequencies, (0,)),
+        ("rpos_closed1", pins.test_rope_positions_closed_form_frequencies, (1,)),
+        ("rpos_3axis", pins.test_rope_positions_three_axis_coordinates, ()),
+        ("rpos_additive", pins.test_rope_positions_angle_is_additive_in_position, ()),
+        ("rpos_norms", pins.test_rope_positions_norms_wrap_and_permutation, ()),
     ]
     return calls
 
