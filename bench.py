@@ -60,6 +60,10 @@ WORKLOAD_TITLES = {
            "eps 1e-6, seed 14",
     "f32": "fp32 RMSNorm [4x4096x3072], N(0,1) with 1% x50 outliers, w ~ N(1,0.1), "
            "eps 1e-6, seed 15",
+    "rope_pos_text": "standalone RoPE, angles from 1D positions on the device, x [2, 4096, "
+                     "32 heads x 128] interleaved, theta 1e4, N(0,1), seed 16",
+    "rope_pos_video": "standalone RoPE, angles from 3D positions (8x24x32, pairs 10/11/11) "
+                      "on the device, x [1, 6144, 32 heads x 64] split-half, theta 1e4, seed 17",
     "gelu": "tanh-approximated GELU, x [2, 6144, 8192] (LTX-Video feed-forward inner "
             "width), N(0,1) with 1% x50 outliers, seed 12",
     "geglu": "GEGLU value * gelu_tanh(gate), x [2, 6144, 2x8192] -> [2, 6144, 8192], "
@@ -135,11 +139,14 @@ KERNEL_SOURCES = {
              "ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",
              "ltxk_rows_adaln.cu", "ltxk_rows_addnorm.cu"),
     "gelu": ("ltxk_kernels.cuh", "ltxk_launch.h", "ltxk_gelu.cu"),
+    "rope": ("ltxk_kernels.cuh", "ltxk_launch.h", "ltxk_rope.cu"),
 }
 
 
 def kernel_family(kernel):
-    return "gelu" if kernel.startswith(("gelu", "geglu")) else "rows"
+    if kernel.startswith(("gelu", "geglu")):
+        return "gelu"
+    return "rope" if kernel.startswith("rope_kernel") else "rows"
 
 
 def source_digest(family="rows"):
@@ -248,7 +255,10 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
         r = max(1, math.ceil(c.rows * row_frac))
         x = inp["x"][:r]
         t0 = time.perf_counter()
-        if c.kind == "gelu":
+        if c.kind == "rope_pos":
+            oracle.rope(x, c.heads, c.head_dim, c.mode, tuple(c.meta["grid"]),
+                        tuple(c.meta["pairs"]), c.meta["theta"], threads=threads)
+        elif c.kind == "gelu":
             oracle.gelu_tanh(x, threads=threads)
         elif c.kind == "geglu":
             oracle.geglu(x, threads=threads)
@@ -263,8 +273,8 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
             oracle.rms_norm_rope(x, inp["w"], inp["cos"], inp["sin"], c.heads, c.head_dim,
                                  c.mode, c.eps, table_rows=c.seq_len, threads=threads)
         t += time.perf_counter() - t0
-        if c.kind in ("gelu", "geglu"):
-            b += (4 if c.kind == "gelu" else 6) * r * c.hidden
+        if c.kind in ("gelu", "geglu", "rope_pos"):
+            b += (6 if c.kind == "geglu" else 2 * inp["x"].dtype.itemsize) * r * c.hidden
             continue
         e = inp["x"].dtype.itemsize
         b += 2 * e * r * c.hidden + (e * c.hidden if inp["w"] is not None else 0) + (
@@ -381,7 +391,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         if c.kind == "adaln":
             d["scale"] = _tensor(inp["scale"]).to(dev)
             d["shift"] = _tensor(inp["shift"]).to(dev)
-        if c.mode is not None:
+        if c.kind == "rope":
             d["cos"] = torch.from_numpy(inp["cos"]).to(dev)
             d["sin"] = torch.from_numpy(inp["sin"]).to(dev)
         dev_bufs.append(d)
@@ -390,6 +400,10 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         c, d = cases[i], dev_bufs[i]
         x = d["x"] if x is None else x
         wp = None if d["w"] is None else d["w"].data_ptr()
+        if c.kind == "rope_pos":
+            return L.ltxk_rope, (d["y"].data_ptr(), x.data_ptr(), c.rows, c.heads, c.head_dim,
+                                 c.mode, *c.meta["grid"], *c.meta["pairs"], c.meta["theta"],
+                                 DTYPE_CODES[c.dtype], sptr)
         if c.kind == "gelu":
             return L.ltxk_gelu_tanh, (d["y"].data_ptr(), x.data_ptr(), c.rows * c.hidden, sptr)
         if c.kind == "geglu":
@@ -442,6 +456,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         if c.kind in ("gelu", "geglu"):
             plans.append("gelu_vec_kernel" if c.kind == "gelu" else
                          "geglu_vec_kernel<unsigned int>")
+            continue
+        if c.kind == "rope_pos":
+            plans.append(f"rope_kernel<{1 if c.mode == 0 else 2}, {DTYPE_CODES[c.dtype]}, true>")
             continue
         op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
               "adaln": L.OP_RMS_NORM_ADALN, "add_norm": L.OP_ADD_RMS_NORM}[c.kind]

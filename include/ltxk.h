@@ -200,6 +200,38 @@ LTXK_API int ltxk_add_rms_norm_dt(void* out, void* residual_out, const void* x,
                                   ltxk_stream_t stream);
 
 /*
+ * ltxk_rope -- standalone rotary position embedding with the rotation angles
+ * computed on the device from token positions: no cos/sin tables in memory
+ * ("cuda-kernels" skill page, "Kernel-Specific Guidelines / RoPE": 1D text
+ * [batch, seq, heads, head_dim], 3D video [batch, t*h*w, heads, head_dim];
+ * LTX-Video computes its own rotary angles).
+ *   out, x   [rows, heads*head_dim] of element type `dtype`; out == x (in
+ *            place) is allowed, any other overlap returns LTXK_ERR_OVERLAP.
+ *   Row r is token s = r mod (grid_t*grid_h*grid_w) (x is [batch, tokens,
+ *   heads, head_dim] with the token index inner), with coordinates
+ *     (s / (grid_h*grid_w), (s / grid_w) mod grid_h, s mod grid_w).
+ *   The head_dim/2 rotation pairs split into consecutive groups of pairs_t,
+ *   pairs_h, pairs_w pairs (axis t, then h, then w; they must add up to
+ *   head_dim/2).  Pair k of an axis with n pairs turns by
+ *     angle = coordinate * theta^(-k/n),
+ *   and every head's pair (a, b) becomes (a cos - b sin, a sin + b cos),
+ *   rounded once.  mode = LTXK_ROPE_* selects the pairing as for the fused
+ *   form.  1D text: grid (seq_len, 1, 1), pairs (head_dim/2, 0, 0), which is
+ *   the usual theta^(-2k/head_dim).
+ *   head_dim even, at most 512; theta > 0.
+ * Numerics: angles are formed and reduced in fp64, cos/sin in fp32 with a
+ * correction for the reduced angle's fp32 remainder (a few 1e-8 absolute for
+ * coordinates below 2^24), and the rotation uses Kahan's 2x2-determinant
+ * algorithm.  An output is therefore within 1 ulp of the exact value, except
+ * where a' or b' cancels: its error is then bounded by a few fp32 ulps of
+ * |a| + |b|.
+ */
+LTXK_API int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int head_dim,
+                       int mode, int64_t grid_t, int64_t grid_h, int64_t grid_w,
+                       int pairs_t, int pairs_h, int pairs_w, double theta, int dtype,
+                       ltxk_stream_t stream);
+
+/*
  * ltxk_gelu_tanh -- elementwise tanh-approximated GELU, bf16 -> bf16:
  *   y = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
  * ("cuda-kernels" skill page, "Kernel-Specific Guidelines / GEGLU vs GELU":

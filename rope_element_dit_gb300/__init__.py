@@ -54,7 +54,7 @@ EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
            "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
            "ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
-           "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt",
+           "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt", "ltxk_rope",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -107,6 +107,9 @@ def _load():
         getattr(lib, f).restype = I32
     lib.ltxk_plan_launch_dt.argtypes = [I32, I32, I64, I64, I32, I32, I32, ctypes.POINTER(Plan)]
     lib.ltxk_plan_launch_dt.restype = I32
+    lib.ltxk_rope.argtypes = [P, P, I64, I32, I32, I32, I64, I64, I64, I32, I32, I32,
+                              ctypes.c_double, I32, P]
+    lib.ltxk_rope.restype = I32
     lib.ltxk_gelu_tanh.argtypes = [P, P, I64, P]
     lib.ltxk_gelu_tanh.restype = I32
     lib.ltxk_geglu.argtypes = [P, P, I64, I64, P]
@@ -197,6 +200,12 @@ def ltxk_plan_launch_dt(op, dtype, rows, hidden, head_dim, mode, vector_ok):
     st = _lib.ltxk_plan_launch_dt(op, dtype, rows, hidden, head_dim, mode,
                                   1 if vector_ok else 0, ctypes.byref(p))
     return st, p
+
+
+def ltxk_rope(out, x, rows, heads, head_dim, mode, grid_t, grid_h, grid_w, pairs_t, pairs_h,
+              pairs_w, theta, dtype, stream) -> int:
+    return _lib.ltxk_rope(out, x, rows, heads, head_dim, mode, grid_t, grid_h, grid_w, pairs_t,
+                          pairs_h, pairs_w, theta, dtype, stream)
 
 
 def ltxk_gelu_tanh(out, x, n, stream) -> int:
@@ -425,4 +434,30 @@ def geglu(x, out=None, stream=None):
     st = ltxk_geglu(_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
                     rows, hidden, _stream_handle(x, stream))
     _check(st, "ltxk_geglu")
+    return out
+
+
+def rope(x, heads: int, head_dim: int, mode: int = ROPE_INTERLEAVED, grid=None, pairs=None,
+         theta: float = 10000.0, out=None, stream=None):
+    """Standalone RoPE with angles computed on the device from token
+    positions.  ``x``: [..., heads*head_dim] (bfloat16, float16 or float32),
+    rows in token order.  ``grid = (T, H, W)`` and ``pairs = (nt, nh, nw)``;
+    the default is 1D text over the rows' second-to-last axis: grid
+    ``(x.shape[-2] or rows, 1, 1)``, pairs ``(head_dim/2, 0, 0)``."""
+    import torch
+    code = _dtype_code(x)
+    hidden = heads * head_dim
+    if x.shape[-1] != hidden:
+        raise ValueError("last axis of x must be heads*head_dim")
+    rows = x.numel() // hidden if hidden else 0
+    if grid is None:
+        grid = (x.shape[-2] if x.dim() >= 2 else max(1, rows), 1, 1)
+    if pairs is None:
+        pairs = (head_dim // 2, 0, 0)
+    if out is None:
+        out = torch.empty_like(x)
+    st = ltxk_rope(_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype), rows, heads,
+                   head_dim, mode, grid[0], grid[1], grid[2], pairs[0], pairs[1], pairs[2],
+                   float(theta), code, _stream_handle(x, stream))
+    _check(st, "ltxk_rope")
     return out

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libltxk.so")
 
-SOURCES = ["ltxk_abi.cu", "ltxk_noalloc.cu", "ltxk_pipeline.cu", "ltxk_gelu.cu"]
+SOURCES = ["ltxk_abi.cu", "ltxk_noalloc.cu", "ltxk_pipeline.cu", "ltxk_gelu.cu", "ltxk_rope.cu"]
 # Row-kernel instance files, compiled once per element format (LTXK_FMT:
 # 0 bf16, 1 fp16, 2 fp32).
 ROW_SOURCES = ["ltxk_rows_plain.cu", "ltxk_rows_interleaved.cu", "ltxk_rows_split.cu",

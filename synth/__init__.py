@@ -228,7 +228,7 @@ class Case:
     seq_len: int = 0               # positions per batch item (table rows)
     table: str = ""                # "1d" or "3axis"
     meta: dict = field(default_factory=dict)
-    op: str = ""                   # "adaln", "add_norm", "gelu", "geglu"
+    op: str = ""                   # "adaln", "add_norm", "gelu", "geglu", "rope_pos"
     weight: bool = True            # False: no weight (ones)
     rows_per_cond: int = 0         # AdaLN: rows sharing one conditioning row
     dtype: str = "bf16"            # element format of x, w, scale, shift, res
@@ -327,6 +327,20 @@ F16 = [Case(name="rms_norm_f16_4x4096x3072", rows=4 * 4096, hidden=3072, seed=14
 F32 = [Case(name="rms_norm_f32_4x4096x3072", rows=4 * 4096, hidden=3072, seed=15,
             x_dist="normal_outliers", eps=1e-6, dtype="f32", meta={"shape": [4, 4096, 3072]})]
 
+# Standalone RoPE with angles computed on the device from token positions,
+# on the fused configs' shapes: 1D text [2, 4096, 32 x 128] interleaved and
+# 3D video [1, 8x24x32, 32 x 64] split-half, theta 1e4, N(0,1), no weight.
+ROPE_POS_TEXT = [Case(
+    name="rope_pos_text_2x4096x32x128", rows=2 * 4096, hidden=4096, seed=16,
+    x_dist="normal", eps=0.0, mode=INTERLEAVED, heads=32, head_dim=128, op="rope_pos",
+    weight=False, meta={"shape": [2, 4096, 32, 128], "grid": [4096, 1, 1],
+                        "pairs": [64, 0, 0], "theta": 10000.0})]
+ROPE_POS_VIDEO = [Case(
+    name="rope_pos_video_1x6144x32x64", rows=6144, hidden=2048, seed=17,
+    x_dist="normal", eps=0.0, mode=SPLIT_HALF, heads=32, head_dim=64, op="rope_pos",
+    weight=False, meta={"shape": [1, 6144, 32, 64], "grid": [8, 24, 32],
+                        "pairs": [10, 11, 11], "theta": 10000.0})]
+
 WORKLOADS = {
     "small": SMALL,
     "sweep": SWEEP,
@@ -339,6 +353,8 @@ WORKLOADS = {
     "geglu": GEGLU,
     "f16": F16,
     "f32": F32,
+    "rope_pos_text": ROPE_POS_TEXT,
+    "rope_pos_video": ROPE_POS_VIDEO,
 }
 
 STREAM_SCALE = 3
@@ -366,7 +382,7 @@ def make_w(case: Case) -> np.ndarray:
 
 
 def make_tables(case: Case):
-    if case.mode is None:
+    if case.mode is None or case.kind == "rope_pos":
         return None, None
     if case.table == "1d":
         return rope_table_1d(case.seq_len, case.head_dim,
@@ -407,8 +423,8 @@ def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
     fp32 cos/sin tables at their literal size for the fused form, or the
     bf16 scale and shift for the AdaLN form.  GELU reads and writes one
     bf16 per element; GEGLU reads two per output element and writes one."""
-    if case.kind == "gelu":
-        return 4 * case.rows * case.hidden
+    if case.kind in ("gelu", "rope_pos"):
+        return (8 if case.dtype == "f32" else 4) * case.rows * case.hidden
     if case.kind == "geglu":
         return 6 * case.rows * case.hidden
     e = 4 if case.dtype == "f32" else 2

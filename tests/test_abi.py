@@ -339,3 +339,31 @@ def test_dtype_validation(L):
     assert L.ltxk_rms_norm_adaln_dt(A, B, None, A + 124, C, 4, 8, 2, 1e-6, L.DTYPE_F32,
                                     None) == L.ERR_OVERLAP
     assert L.ltxk_status_string(L.ERR_DTYPE) == "unknown element type"
+
+
+def test_rope_validation(L):
+    """Standalone RoPE: argument errors come back before any CUDA call."""
+    f = L.ltxk_rope
+    ok = dict(rows=4, heads=2, head_dim=8, mode=0, g=(4, 1, 1), p=(4, 0, 0), theta=1e4,
+              dtype=L.DTYPE_BF16)
+
+    def call(out=A, x=B, **kw):
+        a = dict(ok, **kw)
+        return f(out, x, a["rows"], a["heads"], a["head_dim"], a["mode"], *a["g"], *a["p"],
+                 a["theta"], a["dtype"], None)
+
+    assert call(dtype=7) == L.ERR_DTYPE
+    assert call(out=None) == L.ERR_NULL and call(x=None) == L.ERR_NULL
+    assert call(mode=2) == L.ERR_MODE
+    assert call(rows=-1) == L.ERR_SHAPE
+    assert call(head_dim=7, p=(3, 0, 0)) == L.ERR_SHAPE
+    assert call(head_dim=1024, p=(512, 0, 0)) == L.ERR_SHAPE         # over 512
+    assert call(p=(3, 0, 0)) == L.ERR_SHAPE                          # pairs must add up
+    assert call(p=(5, -1, 0)) == L.ERR_SHAPE
+    assert call(g=(0, 1, 1)) == L.ERR_SHAPE
+    assert call(theta=0.0) == L.ERR_SHAPE and call(theta=float("nan")) == L.ERR_SHAPE
+    assert call(x=B + 1) == L.ERR_ALIGN
+    assert call(x=B + 2, dtype=L.DTYPE_F32) == L.ERR_ALIGN
+    assert call(out=A, x=A + 16) == L.ERR_OVERLAP
+    assert call(rows=0) == L.OK                                       # nothing launched
+    assert call(rows=0, out=A, x=A) == L.OK

@@ -126,7 +126,7 @@ def gpu_rope(x_dev, w_dev, c_dev, s_dev, rows, heads, D, mode, eps, seq_len=None
 # ---------------------------------------------------------------- workloads --
 
 ALL_CASES = [c for cases in synth.WORKLOADS.values() for c in cases
-             if c.kind not in ("gelu", "geglu")       # those: test_gpu_gelu.py
+             if c.kind not in ("gelu", "geglu", "rope_pos")   # test_gpu_gelu.py, _rope_pos.py
              and c.dtype == "bf16"]                   # fp16 / fp32: test_gpu_dtypes.py
 
 

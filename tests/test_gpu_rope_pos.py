@@ -1,0 +1,155 @@
+"""GPU parity of the standalone RoPE with angles computed on the device from
+token positions ("cuda-kernels" page, "Kernel-Specific Guidelines / RoPE":
+1D text [batch, seq, heads, head_dim], 3D video [batch, t*h*w, heads,
+head_dim]) against the fp64 oracle.
+
+Tolerance: the kernel's cos/sin are its own (fp64 angle and reduction,
+fp32 sincosf with a remainder correction: a few 1e-8 absolute), so an
+element is accepted when it is within 1 ulp of the correctly rounded exact
+value, or within half a spacing plus 8 * 2^-24 * (|a| + |b|), the bound on
+the rotation error of its pair (a, b) -- only where the rotation cancels does
+the second clause matter.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rope_element_dit_gb300 as L
+import synth
+from oracle.compare import compare_bf16_bounded, compare_fmt_bounded
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 64
+U = 2.0 ** -24
+DT = {"bf16": (torch.int16, L.DTYPE_BF16), "f16": (torch.float16, L.DTYPE_F16),
+      "f32": (torch.float32, L.DTYPE_F32)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    assert torch.cuda.is_available(), "GPU parity tests need a CUDA device"
+    torch.cuda.set_device(0)
+    assert torch.cuda.get_device_capability(0) == (10, 3)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
+
+
+def host(t, fmt):
+    a = t.cpu().numpy()
+    return a.view(np.uint16) if fmt == "bf16" else a
+
+
+def pair_mag(xw, heads, D, mode):
+    """|a| + |b| of every element's rotation pair (exact inputs)."""
+    rows = xw.shape[0]
+    a = np.abs(xw).reshape(rows, heads, D)
+    if mode == 0:
+        m = a.reshape(rows, heads, D // 2, 2).sum(-1, keepdims=True)
+        m = np.broadcast_to(m, (rows, heads, D // 2, 2))
+    else:
+        P = D // 2
+        s = a[..., :P] + a[..., P:]
+        m = np.concatenate([s, s], axis=-1)
+    return np.asarray(m).reshape(rows, heads * D)
+
+
+def run(x, heads, D, mode, grid, pairs, theta, fmt, out=None, x_dev=None):
+    rows = x.shape[0]
+    n = x.size
+    tdt, code = DT[fmt]
+    whole = torch.full((n + 2 * GUARD,), 77, dtype=tdt, device="cuda")
+    outv = whole[GUARD:GUARD + n] if out is None else out
+    xd = dev(x) if x_dev is None else x_dev
+    st = L.ltxk_rope(outv.data_ptr(), xd.data_ptr(), rows, heads, D, mode, *grid, *pairs,
+                     float(theta), code, torch.cuda.current_stream().cuda_stream)
+    assert st == L.OK, L.ltxk_status_string(st)
+    torch.cuda.synchronize()
+    if out is None:
+        h = whole.cpu()
+        assert torch.all(h[:GUARD] == 77) and torch.all(h[GUARD + n:] == 77), "wrote outside"
+    return host(outv, fmt)
+
+
+def check(got, x, heads, D, mode, grid, pairs, theta, fmt, what):
+    _, ye = oracle.rope(x, heads, D, mode, grid, pairs, theta, exact=True, threads=16)
+    xw = oracle.widen(x) if fmt != "bf16" else oracle.widen_bf16(x)
+    bound = 8 * U * pair_mag(xw.reshape(x.shape[0], -1), heads, D, mode)
+    if fmt == "bf16":
+        r = compare_bf16_bounded(got, ye, bound)
+    else:
+        r = compare_fmt_bounded(got, ye, bound)
+    assert r["ok"], f"{what}: {r}"
+    return r
+
+
+def make_x(seed, rows, hidden, fmt):
+    return synth.normal_bf16(seed, 0, rows * hidden, fmt=fmt).reshape(rows, hidden)
+
+
+# (rows, heads, head_dim, grid, pairs): 1D text and 3D video, vector and
+# element-wise paths, ragged row counts, positions that wrap
+CASES = [
+    (8192, 32, 128, (4096, 1, 1), (64, 0, 0)),          # text [2, 4096, 32 x 128]
+    (6144, 32, 64, (8, 24, 32), (10, 11, 11)),          # video [1, 8x24x32, 32 x 64]
+    (37, 4, 128, (16, 1, 1), (64, 0, 0)),
+    (300, 3, 64, (2, 5, 7), (10, 11, 11)),
+    (50, 5, 16, (3, 4, 5), (2, 3, 3)),
+    (33, 2, 24, (11, 1, 1), (12, 0, 0)),                # head_dim 24: split-half element-wise
+    (9, 7, 6, (4, 2, 1), (1, 1, 1)),                    # head_dim 6: element-wise both modes
+    (21, 16, 512, (9, 1, 1), (256, 0, 0)),              # largest head_dim
+    (5, 80, 128, (1, 1, 1), (64, 0, 0)),                # every token at position 0
+]
+
+
+@pytest.mark.parametrize("rows,heads,D,grid,pairs", CASES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rope_bf16(rows, heads, D, grid, pairs, mode):
+    x = make_x(9000 + rows + D, rows, heads * D, "bf16")
+    got = run(x, heads, D, mode, grid, pairs, 10000.0, "bf16")
+    r = check(got, x, heads, D, mode, grid, pairs, 10000.0, "bf16", f"{rows}x{heads}x{D}")
+    assert r["exact"] >= 0.98 * r["elements"]   # the bound is for cancelling pairs only
+
+
+@pytest.mark.parametrize("fmt", ["f16", "f32"])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[4], CASES[6]])
+def test_rope_other_formats(fmt, mode, case):
+    rows, heads, D, grid, pairs = case
+    x = make_x(9100 + rows, rows, heads * D, fmt)
+    got = run(x, heads, D, mode, grid, pairs, 10000.0, fmt)
+    check(got, x, heads, D, mode, grid, pairs, 10000.0, fmt, f"{fmt} {rows}x{heads}x{D}")
+
+
+def test_rope_position_zero_is_identity_and_in_place():
+    rows, heads, D = 64, 8, 64
+    x = make_x(9201, rows, heads * D, "bf16")
+    got = run(x, heads, D, 0, (1, 1, 1), (32, 0, 0), 10000.0, "bf16")
+    assert np.array_equal(got.reshape(x.shape), x), "token 0 must be the identity"
+    xd = dev(x)
+    got = run(x, heads, D, 1, (8, 2, 4), (16, 8, 8), 500.0, "bf16", out=xd, x_dev=xd)
+    check(got, x, heads, D, 1, (8, 2, 4), (16, 8, 8), 500.0, "bf16", "in place")
+
+
+def test_rope_unaligned_and_theta():
+    rows, heads, D = 40, 4, 64
+    x = make_x(9202, rows, heads * D, "bf16")
+    xb = dev(np.concatenate([np.zeros(1, np.uint16), x.ravel()]))
+    out = torch.empty(rows * heads * D + 1, dtype=torch.int16, device="cuda")
+    for theta in (10000.0, 1e6, 2.5):
+        got = run(x, heads, D, 0, (40, 1, 1), (32, 0, 0), theta, "bf16", out=out[1:],
+                  x_dev=xb[1:])
+        check(got, x, heads, D, 0, (40, 1, 1), (32, 0, 0), theta, "bf16", f"theta {theta}")
+
+
+def test_rope_torch_helper():
+    x = make_x(9204, 2 * 100, 4 * 32, "bf16").reshape(2, 100, 128)
+    xt = dev(x).view(torch.bfloat16).reshape(2, 100, 128)
+    y = L.rope(xt, 4, 32, L.ROPE_SPLIT_HALF)
+    torch.cuda.synchronize()
+    assert y.shape == xt.shape and y.dtype == torch.bfloat16
+    check(y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(200, 128),
+          x.reshape(200, 128), 4, 32, 1, (100, 1, 1), (16, 0, 0), 10000.0, "bf16", "helper")
