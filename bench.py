@@ -77,6 +77,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="sweep", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--case", type=int, default=None,
+                    help="run only this shape (index) of the workload, e.g. for a profiler "
+                         "capture that should hold one shape on the device")
     ap.add_argument("--impl", default="ltxk", choices=["ltxk", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -618,6 +621,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "io_dtype": cases[0].dtype, "data": "synthetic",
         "config": {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload,
+                   "case": args.case,
                    "timing": "CUDA events around each launch on the launching stream; "
                              "a GPU spin before each launch keeps host launch latency "
                              "out of the events",
@@ -645,6 +649,10 @@ def main():
     args = parse_args()
     world, rank, local = dist_env()
     cases = synth.WORKLOADS[args.workload]
+    if args.case is not None:
+        if not 0 <= args.case < len(cases):
+            raise SystemExit(f"--case must be in [0, {len(cases)})")
+        cases = [cases[args.case]]
     inputs = [synth.make_inputs(c) for c in cases]
     if args.impl == "reference":
         run_reference(args, cases, inputs, world, rank)
