@@ -305,8 +305,16 @@ def cpu_baseline(cases, inputs, seconds):
               f"{frac * 100:.1f}% of the rows of every shape"
               + (f", {reps} repetitions" if reps > 1 else "")
               + f", {tot_t:.1f} s")
+    # the same oracle on one thread, over a sample sized to about a quarter of
+    # the time budget
+    t1, _ = cpu_oracle_time(cases, inputs, 0.001, 1)
+    frac1 = min(1.0, max(0.001, 0.001 * 0.25 * seconds / max(t1, 1e-6)))
+    st, sb = cpu_oracle_time(cases, inputs, frac1, 1)
     return {"value": round(tot_b / tot_t / 1e9, 3), "unit": UNIT, "cores": threads,
-            "kind": "oracle", "sample": sample}
+            "kind": "oracle", "sample": sample,
+            "single_thread": {"value": round(sb / st / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"first {frac1 * 100:.2f}% of the rows of every "
+                                        f"shape, {st:.1f} s"}}
 
 
 def run_reference(args, cases, inputs, world, rank):
