@@ -275,6 +275,12 @@ LTXK_API int ltxk_geglu(void* out, const void* x, int64_t rows, int64_t hidden,
  *                 the caller; split into n_streams slots of at least one row.
  *   streams       n_streams (1 .. LTXK_HOST_MAX_STREAMS) streams, ideally
  *                 distinct non-default streams.
+ * When out_host and x_host are both page-locked host memory the device can
+ * address (cudaHostAlloc, cudaHostRegister, torch pin_memory), the call
+ * instead queues one kernel on streams[0] that reads x and writes y across
+ * the host link directly (zero-copy; on GB300 over NVLink-C2C, both
+ * directions at once); staging is then unused.  out_host may equal x_host
+ * (in place) but must not partly overlap it (LTXK_ERR_OVERLAP).
  * The library allocates nothing.  Returns an ltxk_status; argument errors
  * are reported before any copy is queued.
  */

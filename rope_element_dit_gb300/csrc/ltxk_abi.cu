@@ -466,6 +466,7 @@ int add_norm_fmt(void* out, void* residual_out, const void* x, const void* resid
 
 namespace ltxk {
 void record_cuda_error(int e) { g_last_cuda_error = e; }
+int current_path() { return g_path.load(); }
 }  // namespace ltxk
 
 extern "C" {

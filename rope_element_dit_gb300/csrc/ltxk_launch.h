@@ -40,4 +40,7 @@ const void* rows_tma_split_ptr(int vec_per_lane);
 // Record a cudaError_t for ltxk_last_cuda_error() (calling thread).
 void record_cuda_error(int e);
 
+// The kernel-family setting of ltxk_set_path (LTXK_PATH_*).
+int current_path();
+
 }  // namespace ltxk

@@ -1,6 +1,14 @@
 // ltxk_pipeline.cu -- ltxk_rms_norm_host: RMSNorm of rows held in host
-// memory, pipelined over caller-provided streams and device staging memory.
+// memory.
 //
+// Page-locked host memory that the GPU can address (cudaHostAlloc, torch's
+// pin_memory, cudaHostRegister): one kernel on streams[0] reads x and writes
+// y across the host link itself (zero-copy).  On GB300 the link to the Grace
+// CPU (NVLink-C2C) then carries both directions at once, at the rate of two
+// concurrent copies, with no staging and no copy engine.
+//
+// Any other host memory is pipelined over caller-provided streams and device
+// staging memory:
 // The rows are cut into chunks.  Chunk i goes to stream i % n and staging
 // slot i % n: copy x in (host -> device), normalise in place in the slot,
 // copy y out (device -> host).  Consecutive chunks run on different streams,
@@ -21,6 +29,26 @@ namespace {
 int fail(cudaError_t e) {
   ltxk::record_cuda_error(static_cast<int>(e));
   return LTXK_ERR_CUDA;
+}
+
+// The current device's address of [p, p + bytes) if the whole range is host
+// memory it can access directly (page-locked and mapped, or managed), with
+// the device addresses of both ends the same distance apart; else nullptr.
+void* device_view(const void* p, int64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  cudaPointerAttributes a0, a1;
+  if (cudaPointerGetAttributes(&a0, c) != cudaSuccess ||
+      cudaPointerGetAttributes(&a1, c + bytes - 1) != cudaSuccess) {
+    cudaGetLastError();   // an unknown pointer is not an error here
+    return nullptr;
+  }
+  const bool host0 = a0.type == cudaMemoryTypeHost || a0.type == cudaMemoryTypeManaged;
+  const bool host1 = a1.type == cudaMemoryTypeHost || a1.type == cudaMemoryTypeManaged;
+  if (!host0 || !host1 || a0.devicePointer == nullptr || a1.devicePointer == nullptr)
+    return nullptr;
+  if (static_cast<char*>(a1.devicePointer) - static_cast<char*>(a0.devicePointer) != bytes - 1)
+    return nullptr;
+  return a0.devicePointer;
 }
 
 }  // namespace
@@ -50,7 +78,19 @@ extern "C" int ltxk_rms_norm_host(void* out_host, const void* x_host, const void
   if (w != nullptr && w0 < s0 + static_cast<uint64_t>(staging_bytes) &&
       s0 < w0 + static_cast<uint64_t>(hidden) * 2)
     return LTXK_ERR_OVERLAP;
+  // out may be x exactly (in place), never partly
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x_host), ya = reinterpret_cast<uintptr_t>(out_host);
+  const uint64_t total = static_cast<uint64_t>(rows) * hidden * 2;
+  if (xa != ya && total != 0 && xa < ya + total && ya < xa + total) return LTXK_ERR_OVERLAP;
   if (rows == 0) return LTXK_OK;
+
+  // zero-copy when both buffers are device-accessible host memory (the TMA
+  // ring, selectable for tests, always stages)
+  if (ltxk::current_path() != LTXK_PATH_TMA) {
+    void* yd = device_view(out_host, static_cast<int64_t>(total));
+    const void* xd = yd == nullptr ? nullptr : device_view(x_host, static_cast<int64_t>(total));
+    if (xd != nullptr) return ltxk_rms_norm(yd, xd, w, rows, hidden, eps, streams[0]);
+  }
 
   const char* xh = static_cast<const char*>(x_host);
   char* yh = static_cast<char*>(out_host);

@@ -367,3 +367,12 @@ def test_rope_validation(L):
     assert call(out=A, x=A + 16) == L.ERR_OVERLAP
     assert call(rows=0) == L.OK                                       # nothing launched
     assert call(rows=0, out=A, x=A) == L.OK
+
+
+def test_host_pipeline_rejects_partial_overlap(L):
+    f = L.ltxk_rms_norm_host
+    S = 0x7F0800000000
+    # 4 rows x 8 bf16 = 64 bytes: out 16 bytes into x
+    assert f(A + 16, A, None, 4, 8, 1e-6, S, 1 << 20, [0], 1) == L.ERR_OVERLAP
+    assert f(A, A + 62, None, 4, 8, 1e-6, S, 1 << 20, [0], 1) == L.ERR_OVERLAP
+    assert f(A, A, None, 0, 8, 1e-6, S, 1 << 20, [0], 1) == L.OK      # in place, empty

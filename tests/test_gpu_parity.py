@@ -524,16 +524,22 @@ def test_adaln_binding_helper():
 
 # --------------------------------------------------------- host pipeline --
 
+# pinned: page-locked host buffers take the zero-copy kernel; pageable ones
+# (and pinned ones under the TMA path setting) the staged pipeline
 @pytest.mark.parametrize("rows,hidden,slot_rows,n_streams,pinned", [
     (4099, 3072, 512, 3, True), (1000, 2048, 1, 2, True), (37, 264, 5, 3, False),
-    (16384, 3072, 4096, 3, True), (9, 24, 100, 1, True)])
+    (16384, 3072, 4096, 3, True), (9, 24, 100, 1, True), (4099, 3072, 512, 3, False),
+    (1000, 2048, 1, 2, False), (2049, 2056, 300, 2, "staged")])
 def test_host_pipeline_matches_device_call(rows, hidden, slot_rows, n_streams, pinned):
     x = synth.normal_bf16(61, 0, rows * hidden).reshape(rows, hidden)
     w = synth.normal_bf16(61, 2, hidden, 1.0, 0.1)
     xh = torch.from_numpy(x.view(np.int16).copy())
     yh = torch.full_like(xh, 0x7FC1)
+    old = None
     if pinned:
         xh, yh = xh.pin_memory(), yh.pin_memory()
+    if pinned == "staged":
+        old = L.ltxk_set_path(L.PATH_TMA)
     wd = to_dev(w)
     slot = (slot_rows * hidden * 2 + 255) // 256 * 256
     staging = torch.empty(n_streams * slot, dtype=torch.uint8, device="cuda")
@@ -541,12 +547,33 @@ def test_host_pipeline_matches_device_call(rows, hidden, slot_rows, n_streams, p
     st = L.ltxk_rms_norm_host(yh.data_ptr(), xh.data_ptr(), wd.data_ptr(), rows, hidden,
                               1e-6, staging.data_ptr(), staging.numel(),
                               [s.cuda_stream for s in streams], n_streams)
-    assert st == L.OK
     for s in streams:
         s.synchronize()
+    if old is not None:
+        L.ltxk_set_path(old)
+    assert st == L.OK
     ref = gpu_rms_norm(to_dev(x), wd, rows, hidden, 1e-6)
     torch.cuda.synchronize()
     assert np.array_equal(yh.numpy().view(np.uint16).ravel(), to_host(ref))
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_pipeline_in_place(pinned):
+    """out_host == x_host on both the zero-copy and the staged branch."""
+    rows, hidden = 777, 3072
+    x = synth.normal_bf16(62, 0, rows * hidden).reshape(rows, hidden)
+    xh = torch.from_numpy(x.view(np.int16).copy())
+    if pinned:
+        xh = xh.pin_memory()
+    staging = torch.empty(2 * (4 << 20), dtype=torch.uint8, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    st = L.ltxk_rms_norm_host(xh.data_ptr(), xh.data_ptr(), None, rows, hidden, 1e-6,
+                              staging.data_ptr(), staging.numel(),
+                              [s.cuda_stream for s in streams], 2)
+    for s in streams:
+        s.synchronize()
+    assert st == L.OK
+    assert_parity(xh.numpy().view(np.uint16).ravel(), oracle.rms_norm(x, None, 1e-6), "in place")
 
 
 def test_host_pipeline_helper():
