@@ -29,6 +29,7 @@ std::atomic<int> g_path{LTXK_PATH_AUTO};
 
 constexpr int kMaxVplSlots = 16;   // fp32 rows: 8 (twice the registers per slot)
 constexpr int kGroupChoices[] = {1, 2, 4, 8, 16, 32};
+constexpr int64_t kSmallRows = 2432;   // 152 SMs x 16 two-warp rows
 // Dynamic shared memory a TMA-ring CTA aims for: two CTAs per SM share the
 // 228 KB of an SM, so each keeps about 100 KB of rows in flight.
 #ifndef LTXK_TMA_SMEM_TARGET
@@ -223,6 +224,20 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
         p->rows_per_cta = p->block_threads / (32 * g);
         return LTXK_OK;
       }
+    }
+    // Few rows: when two-warp rows still fit in one wave (about 32 resident
+    // warps per SM on 152 SMs), an exact two-warp split doubles the loads in
+    // flight of a problem too small to fill the GPU.  Measured on GB300 at
+    // hidden 2048: 1024 rows 9.3 -> 8.5 us, 2048 rows 10.7 -> 10.3 us; at
+    // 4096 rows (more than one wave) one warp per row stays faster.
+    if (path != LTXK_PATH_TMA && rows <= kSmallRows && nv % 64 == 0 &&
+        (nv / 64 == 3 || nv / 64 == 4)) {
+      p->kernel = LTXK_KERNEL_ROWS_VEC;
+      p->group_warps = 2;
+      p->vec_per_lane = 4;
+      p->block_threads = block_for_group(2);
+      p->rows_per_cta = p->block_threads / 64;
+      return LTXK_OK;
     }
   }
   if (vec) {

@@ -108,6 +108,11 @@ def test_rope_validation(L):
     # plain RMSNorm: rows that split exactly into 3-4 vectors per lane over
     # g >= 4 warps take that split; others the fewest warps per row
     (0, 16384, 2048, 0, 0, True, 1, 1, 8),
+    (0, 4096, 2048, 0, 0, True, 1, 1, 8),
+    (0, 2048, 2048, 0, 0, True, 1, 2, 4),    # few rows: two warps per row
+    (0, 1024, 2048, 0, 0, True, 1, 2, 4),
+    (0, 2432, 1536, 0, 0, True, 1, 2, 4),
+    (0, 2433, 1536, 0, 0, True, 1, 1, 8),
     (0, 16384, 3072, 0, 0, True, 1, 4, 4),
     (0, 65536, 4096, 0, 0, True, 1, 4, 4),
     (0, 16384, 6144, 0, 0, True, 1, 8, 4),
