@@ -68,6 +68,14 @@ WORKLOAD_TITLES = {
             "width), N(0,1) with 1% x50 outliers, seed 12",
     "geglu": "GEGLU value * gelu_tanh(gate), x [2, 6144, 2x8192] -> [2, 6144, 8192], "
              "N(0,1) with 1% x50 outliers, seed 13",
+    "gelu_f16": "fp16 tanh-approximated GELU, x [2, 6144, 8192], N(0,1) with 1% x50 "
+                "outliers, seed 18",
+    "gelu_f32": "fp32 tanh-approximated GELU, x [2, 6144, 8192], N(0,1) with 1% x50 "
+                "outliers, seed 19",
+    "geglu_f16": "fp16 GEGLU, x [2, 6144, 2x8192] -> [2, 6144, 8192], N(0,1) with 1% x50 "
+                 "outliers, seed 20",
+    "geglu_f32": "fp32 GEGLU, x [2, 6144, 2x8192] -> [2, 6144, 8192], N(0,1) with 1% x50 "
+                 "outliers, seed 21",
 }
 
 
@@ -277,7 +285,7 @@ def cpu_oracle_time(cases, inputs, row_frac, threads):
                                  c.mode, c.eps, table_rows=c.seq_len, threads=threads)
         t += time.perf_counter() - t0
         if c.kind in ("gelu", "geglu", "rope_pos"):
-            b += (6 if c.kind == "geglu" else 2 * inp["x"].dtype.itemsize) * r * c.hidden
+            b += (3 if c.kind == "geglu" else 2) * inp["x"].dtype.itemsize * r * c.hidden
             continue
         e = inp["x"].dtype.itemsize
         b += 2 * e * r * c.hidden + (e * c.hidden if inp["w"] is not None else 0) + (
@@ -417,9 +425,11 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                                  c.mode, *c.meta["grid"], *c.meta["pairs"], c.meta["theta"],
                                  DTYPE_CODES[c.dtype], sptr)
         if c.kind == "gelu":
-            return L.ltxk_gelu_tanh, (d["y"].data_ptr(), x.data_ptr(), c.rows * c.hidden, sptr)
+            return L.ltxk_gelu_tanh_dt, (d["y"].data_ptr(), x.data_ptr(), c.rows * c.hidden,
+                                         DTYPE_CODES[c.dtype], sptr)
         if c.kind == "geglu":
-            return L.ltxk_geglu, (d["y"].data_ptr(), x.data_ptr(), c.rows, c.hidden, sptr)
+            return L.ltxk_geglu_dt, (d["y"].data_ptr(), x.data_ptr(), c.rows, c.hidden,
+                                     DTYPE_CODES[c.dtype], sptr)
         if c.kind == "add_norm":
             return L.ltxk_add_rms_norm, (d["y"].data_ptr(), d["h"].data_ptr(), x.data_ptr(),
                                          d["res"].data_ptr(), wp, c.rows, c.hidden, c.eps,
@@ -466,8 +476,13 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     plans = []
     for c in cases:
         if c.kind in ("gelu", "geglu"):
-            plans.append("gelu_vec_kernel" if c.kind == "gelu" else
-                         "geglu_vec_kernel<unsigned int>")
+            f = DTYPE_CODES[c.dtype]
+            if c.dtype == "f32":
+                plans.append("gelu_chunk_kernel" if c.kind == "gelu" else
+                             "geglu_chunk_kernel<unsigned int>")
+            else:
+                plans.append(f"gelu_vec_kernel<{f}>" if c.kind == "gelu" else
+                             f"geglu_vec_kernel<unsigned int, {f}>")
             continue
         if c.kind == "rope_pos":
             plans.append(f"rope_kernel<{1 if c.mode == 0 else 2}, {DTYPE_CODES[c.dtype]}, true>")

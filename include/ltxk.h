@@ -263,6 +263,26 @@ LTXK_API int ltxk_geglu(void* out, const void* x, int64_t rows, int64_t hidden,
                         ltxk_stream_t stream);
 
 /*
+ * ltxk_gelu_tanh_dt, ltxk_geglu_dt -- ltxk_gelu_tanh and ltxk_geglu for one
+ * element type (LTXK_DTYPE_BF16, _F16 or _F32; input and output share it):
+ * the page's "Supported Data Types" (__half, __nv_bfloat16, float).  Same
+ * arguments, layout and errors; pointers need the element's alignment, and an
+ * unknown dtype returns LTXK_ERR_DTYPE.  bf16 gives exactly the bits of the
+ * calls above.  fp16 is rounded once from the same fp32 evaluation.  The
+ * vector kernels want 16-byte aligned pointers and, for GEGLU, hidden % 8 == 0
+ * (fp32: hidden % 4 == 0); anything else takes the element kernel.  fp32
+ * carries the fp32 evaluation's error:
+ *   |y - gelu| <= 2^-24 (32 + 5 |q| / (1 + 2^q)) |gelu| + 2^-148,
+ * with q = (2 / ln 2) sqrt(2 / pi) (x + 0.044715 x^3) (the |q| term is the
+ * fp32 rounding of q, magnified by 2^q's sensitivity in the left tail).
+ * Bytes per element: 2, 2 or 4 read and written (GEGLU: twice the reads).
+ */
+LTXK_API int ltxk_gelu_tanh_dt(void* out, const void* x, int64_t n, int dtype,
+                               ltxk_stream_t stream);
+LTXK_API int ltxk_geglu_dt(void* out, const void* x, int64_t rows, int64_t hidden,
+                           int dtype, ltxk_stream_t stream);
+
+/*
  * ltxk_rms_norm_host -- ltxk_rms_norm for x and y in HOST memory, pipelined.
  * The rows are cut into chunks; chunk i is copied in on streams[i % n],
  * normalised in place in staging slot i % n, and copied out, so the copy-in,

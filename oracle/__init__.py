@@ -100,10 +100,10 @@ def _load():
             lib.oracle_rope_positions.argtypes = [I32, P, P, I64, I64, I64, I32, I64, I64, I64,
                                                   I64, I64, I64, ctypes.c_double, I64, P]
             lib.oracle_rope_positions.restype = I32
-            lib.oracle_gelu_tanh.argtypes = [P, P, I64, P]
-            lib.oracle_gelu_tanh.restype = None
-            lib.oracle_geglu.argtypes = [P, P, I64, I64, P]
-            lib.oracle_geglu.restype = None
+            lib.oracle_gelu_tanh_fmt.argtypes = [I32, P, P, I64, P]
+            lib.oracle_gelu_tanh_fmt.restype = None
+            lib.oracle_geglu_fmt.argtypes = [I32, P, P, I64, I64, P]
+            lib.oracle_geglu_fmt.restype = None
             _lib = lib
     return _lib
 
@@ -353,8 +353,9 @@ def rope(x, heads, head_dim, mode, grid, pairs, theta=10000.0, *, threads: int =
 
 
 def gelu_tanh(x, *, threads: int = 1, exact: bool = False):
-    """Oracle tanh-approximated GELU, elementwise (uint16 bf16 bits)."""
-    x = _u16(x, "x")
+    """Oracle tanh-approximated GELU, elementwise (uint16 bf16 bits, float16
+    or float32; the result in the same dtype)."""
+    fmt, x = _elems(x, "x")
     flat = x.reshape(-1)
     y = np.empty_like(flat)
     ye = np.empty(flat.shape, np.float64) if exact else None
@@ -362,8 +363,8 @@ def gelu_tanh(x, *, threads: int = 1, exact: bool = False):
 
     def run(block):
         r0, r1 = block
-        lib.oracle_gelu_tanh(_ptr(y[r0:r1]), _ptr(flat[r0:r1]), r1 - r0,
-                             None if ye is None else _ptr(ye[r0:r1]))
+        lib.oracle_gelu_tanh_fmt(fmt, _ptr(y[r0:r1]), _ptr(flat[r0:r1]), r1 - r0,
+                                 None if ye is None else _ptr(ye[r0:r1]))
 
     _run_blocks(run, flat.size, threads)
     y = y.reshape(x.shape)
@@ -372,22 +373,23 @@ def gelu_tanh(x, *, threads: int = 1, exact: bool = False):
 
 def geglu(x, *, threads: int = 1, exact: bool = False):
     """Oracle GEGLU: x [..., 2h] -> [..., h], value * gelu(gate) with the
-    value in the first half of the last axis and the gate in the second."""
-    x = _u16(x, "x")
+    value in the first half of the last axis and the gate in the second
+    (uint16 bf16 bits, float16 or float32; the result in the same dtype)."""
+    fmt, x = _elems(x, "x")
     h2 = x.shape[-1]
     if h2 % 2:
         raise ValueError("last axis must be even")
     h = h2 // 2
     rows = x.size // h2 if h2 else 0
     x2 = x.reshape(rows, h2)
-    y = np.empty((rows, h), np.uint16)
+    y = np.empty((rows, h), x.dtype)
     ye = np.empty((rows, h), np.float64) if exact else None
     lib = _load()
 
     def run(block):
         r0, r1 = block
-        lib.oracle_geglu(_ptr(y[r0:r1]), _ptr(x2[r0:r1]), r1 - r0, h,
-                         None if ye is None else _ptr(ye[r0:r1]))
+        lib.oracle_geglu_fmt(fmt, _ptr(y[r0:r1]), _ptr(x2[r0:r1]), r1 - r0, h,
+                             None if ye is None else _ptr(ye[r0:r1]))
 
     _run_blocks(run, rows, threads)
     shape = x.shape[:-1] + (h,)

@@ -166,3 +166,26 @@ def compare_fmt_bounded(got: np.ndarray, exact: np.ndarray, bound: np.ndarray) -
             "beyond_1ulp_within_bound": int(np.count_nonzero(ok & (d > 1))),
             "over_tolerance": int(bad.size), "first_bad": [int(i) for i in bad[:8]],
             "ok": bad.size == 0}
+
+
+def gelu_f32_bound(gate: np.ndarray, exact: np.ndarray, k0: float = 32.0) -> np.ndarray:
+    """Error bound of an fp32 evaluation of value * gelu(gate) (value = 1
+    for GELU), from the exact gate and the exact result:
+
+        2^-24 (k0 + 5 |q| / (1 + 2^q)) |exact| + 2^-148,   k0 = 32,
+        q = (2 / ln 2) sqrt(2 / pi) (gate + 0.044715 gate^3).
+
+    Terms: q in fp32 carries a relative error of at most 6 * 2^-24 (the two
+    constants' roundings, x^2, the fused multiply-add and the product), which
+    moves s / (1 + s), s = 2^q, by the relative amount
+    ln 2 * (1 - sigma) |dq| <= 4.2 * 2^-24 |q| / (1 + 2^q); the ex2 and rcp
+    approximations and the remaining roundings are about 8 units of 2^-24,
+    taken as k0 = 32 with margin; 2^-148 covers the rounding into the
+    subnormal range (of gelu and then of the product)."""
+    g = np.asarray(gate, dtype=np.float64)
+    e = np.asarray(exact, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        q = (2.0 / np.log(2.0)) * np.sqrt(2.0 / np.pi) * (g + 0.044715 * g ** 3)
+        left = np.exp(-np.logaddexp(0.0, q * np.log(2.0)))    # 1 / (1 + 2^q)
+        rel = np.where(np.isfinite(q), k0 + 5.0 * np.abs(q) * left, np.inf)
+        return np.ldexp(rel, -24) * np.abs(e) + 2.0 ** -148

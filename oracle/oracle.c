@@ -439,22 +439,35 @@ static double gelu_tanh(double x) {
     return x * e / (1.0 + e);
 }
 
-/* y = bf16(gelu(x)) elementwise over n values; y_exact optional. */
-void oracle_gelu_tanh(uint16_t* y, const uint16_t* x, int64_t n, double* y_exact) {
+/* y = round(gelu(x)) elementwise over n values of format fmt (x and y of
+ * that format); y_exact optional. */
+void oracle_gelu_tanh_fmt(int fmt, void* y, const void* x, int64_t n, double* y_exact) {
     for (int64_t i = 0; i < n; ++i) {
-        const double v = gelu_tanh(widen_bf16(x[i]));
+        const double v = gelu_tanh(load_elem(fmt, x, i));
         if (y_exact) y_exact[i] = v;
-        y[i] = round_to_bf16(v);
+        store_elem(fmt, y, i, v);
     }
 }
 
-/* GEGLU: x [rows, 2h] -> y [rows, h], y[r, j] = bf16(x[r, j] * gelu(x[r, h + j])). */
-void oracle_geglu(uint16_t* y, const uint16_t* x, int64_t rows, int64_t h, double* y_exact) {
+void oracle_gelu_tanh(uint16_t* y, const uint16_t* x, int64_t n, double* y_exact) {
+    oracle_gelu_tanh_fmt(FMT_BF16, y, x, n, y_exact);
+}
+
+/* GEGLU: x [rows, 2h] -> y [rows, h], y[r, j] = round(x[r, j] * gelu(x[r, h + j]))
+ * in format fmt. */
+void oracle_geglu_fmt(int fmt, void* y, const void* x, int64_t rows, int64_t h,
+                      double* y_exact) {
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t j = 0; j < h; ++j) {
-            const double v = widen_bf16(x[r * 2 * h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + h + j]));
+            const double value = load_elem(fmt, x, r * 2 * h + j);
+            const double gate = load_elem(fmt, x, r * 2 * h + h + j);
+            const double v = value * gelu_tanh(gate);
             if (y_exact) y_exact[r * h + j] = v;
-            y[r * h + j] = round_to_bf16(v);
+            store_elem(fmt, y, r * h + j, v);
         }
     }
+}
+
+void oracle_geglu(uint16_t* y, const uint16_t* x, int64_t rows, int64_t h, double* y_exact) {
+    oracle_geglu_fmt(FMT_BF16, y, x, rows, h, y_exact);
 }

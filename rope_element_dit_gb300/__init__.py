@@ -55,6 +55,7 @@ EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
            "ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
            "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt", "ltxk_rope",
+           "ltxk_gelu_tanh_dt", "ltxk_geglu_dt",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 
 
@@ -114,6 +115,10 @@ def _load():
     lib.ltxk_gelu_tanh.restype = I32
     lib.ltxk_geglu.argtypes = [P, P, I64, I64, P]
     lib.ltxk_geglu.restype = I32
+    lib.ltxk_gelu_tanh_dt.argtypes = [P, P, I64, I32, P]
+    lib.ltxk_gelu_tanh_dt.restype = I32
+    lib.ltxk_geglu_dt.argtypes = [P, P, I64, I64, I32, P]
+    lib.ltxk_geglu_dt.restype = I32
     lib.ltxk_fault_status.argtypes = []
     lib.ltxk_fault_status.restype = I32
     lib.ltxk_set_path.argtypes = [I32]
@@ -214,6 +219,14 @@ def ltxk_gelu_tanh(out, x, n, stream) -> int:
 
 def ltxk_geglu(out, x, rows, hidden, stream) -> int:
     return _lib.ltxk_geglu(out, x, rows, hidden, stream)
+
+
+def ltxk_gelu_tanh_dt(out, x, n, dtype, stream) -> int:
+    return _lib.ltxk_gelu_tanh_dt(out, x, n, dtype, stream)
+
+
+def ltxk_geglu_dt(out, x, rows, hidden, dtype, stream) -> int:
+    return _lib.ltxk_geglu_dt(out, x, rows, hidden, dtype, stream)
 
 
 def ltxk_fault_status() -> int:
@@ -409,31 +422,34 @@ def add_rms_norm(x, residual, weight=None, eps: float = 1e-6, out=None, residual
 
 
 def gelu_tanh(x, out=None, stream=None):
-    """Tanh-approximated GELU of a bf16 tensor; ``out=x`` works in place."""
+    """Tanh-approximated GELU of a bf16, fp16 or fp32 tensor; ``out=x``
+    works in place."""
     import torch
+    code = _dtype_code(x)
     if out is None:
         out = torch.empty_like(x)
     if out.shape != x.shape:
         raise ValueError("out must have the shape of x")
-    st = ltxk_gelu_tanh(_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
-                        x.numel(), _stream_handle(x, stream))
-    _check(st, "ltxk_gelu_tanh")
+    st = ltxk_gelu_tanh_dt(_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype),
+                           x.numel(), code, _stream_handle(x, stream))
+    _check(st, "ltxk_gelu_tanh_dt")
     return out
 
 
 def geglu(x, out=None, stream=None):
     """GEGLU over the last axis: ``x[..., :h] * gelu_tanh(x[..., h:])`` with
-    ``h = x.shape[-1] // 2`` (bf16)."""
+    ``h = x.shape[-1] // 2`` (bf16, fp16 or fp32)."""
     import torch
+    code = _dtype_code(x)
     if x.shape[-1] % 2:
         raise ValueError("last axis of x must be even")
     hidden = x.shape[-1] // 2
     rows = x.numel() // x.shape[-1] if hidden else 0
     if out is None:
         out = torch.empty(*x.shape[:-1], hidden, dtype=x.dtype, device=x.device)
-    st = ltxk_geglu(_dev_ptr(out, "out", torch.bfloat16), _dev_ptr(x, "x", torch.bfloat16),
-                    rows, hidden, _stream_handle(x, stream))
-    _check(st, "ltxk_geglu")
+    st = ltxk_geglu_dt(_dev_ptr(out, "out", x.dtype), _dev_ptr(x, "x", x.dtype),
+                       rows, hidden, code, _stream_handle(x, stream))
+    _check(st, "ltxk_geglu_dt")
     return out
 
 

@@ -319,6 +319,25 @@ GEGLU = [Case(
     x_dist="normal_outliers", eps=0.0, op="geglu", weight=False,
     meta={"shape": [2, 6144, 16384], "out_shape": [2, 6144, 8192]})]
 
+# GELU and GEGLU in the pages' other two precision modes, on the same
+# feed-forward shapes and recipe.
+GELU_F16 = [Case(
+    name="gelu_tanh_f16_2x6144x8192", rows=2 * 6144, hidden=8192, seed=18,
+    x_dist="normal_outliers", eps=0.0, op="gelu", weight=False, dtype="f16",
+    meta={"shape": [2, 6144, 8192]})]
+GELU_F32 = [Case(
+    name="gelu_tanh_f32_2x6144x8192", rows=2 * 6144, hidden=8192, seed=19,
+    x_dist="normal_outliers", eps=0.0, op="gelu", weight=False, dtype="f32",
+    meta={"shape": [2, 6144, 8192]})]
+GEGLU_F16 = [Case(
+    name="geglu_f16_2x6144x16384", rows=2 * 6144, hidden=8192, seed=20,
+    x_dist="normal_outliers", eps=0.0, op="geglu", weight=False, dtype="f16",
+    meta={"shape": [2, 6144, 16384], "out_shape": [2, 6144, 8192]})]
+GEGLU_F32 = [Case(
+    name="geglu_f32_2x6144x16384", rows=2 * 6144, hidden=8192, seed=21,
+    x_dist="normal_outliers", eps=0.0, op="geglu", weight=False, dtype="f32",
+    meta={"shape": [2, 6144, 16384], "out_shape": [2, 6144, 8192]})]
+
 # The pages' other two precision modes on the largest sweep shape
 # [4, 4096, 3072]: RMSNorm in float16 and in float32, N(0,1) with 1% x50
 # outliers (the sweep's recipe), w ~ N(1, 0.1).
@@ -351,6 +370,10 @@ WORKLOADS = {
     "add_norm": ADD_NORM,
     "gelu": GELU,
     "geglu": GEGLU,
+    "gelu_f16": GELU_F16,
+    "gelu_f32": GELU_F32,
+    "geglu_f16": GEGLU_F16,
+    "geglu_f32": GEGLU_F32,
     "f16": F16,
     "f32": F32,
     "rope_pos_text": ROPE_POS_TEXT,
@@ -422,11 +445,12 @@ def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
     """Bytes one call must move: read x, write y, read w (all bf16), plus the
     fp32 cos/sin tables at their literal size for the fused form, or the
     bf16 scale and shift for the AdaLN form.  GELU reads and writes one
-    bf16 per element; GEGLU reads two per output element and writes one."""
+    element per element; GEGLU reads two per output element and writes one
+    (2 bytes each for bf16 and fp16, 4 for fp32)."""
     if case.kind in ("gelu", "rope_pos"):
         return (8 if case.dtype == "f32" else 4) * case.rows * case.hidden
     if case.kind == "geglu":
-        return 6 * case.rows * case.hidden
+        return (12 if case.dtype == "f32" else 6) * case.rows * case.hidden
     e = 4 if case.dtype == "f32" else 2
     b = 2 * e * case.rows * case.hidden + (e * case.hidden if case.weight else 0)
     if case.kind == "add_norm":

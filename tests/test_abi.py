@@ -308,6 +308,25 @@ def test_geglu_validation(L):
     assert f(A, B, 0, 8, None) == L.OK
 
 
+def test_gelu_geglu_dtype_validation(L):
+    """The per-format entry points: unknown dtypes, the element size's
+    alignment and byte extents, all before any CUDA call."""
+    g, f = L.ltxk_gelu_tanh_dt, L.ltxk_geglu_dt
+    assert g(A, B, 16, 3, None) == L.ERR_DTYPE
+    assert g(None, B, 16, -1, None) == L.ERR_DTYPE         # dtype checked first
+    assert f(A, B, 4, 8, 5, None) == L.ERR_DTYPE
+    assert g(A + 2, B, 16, L.DTYPE_F32, None) == L.ERR_ALIGN    # fp32 wants 4 bytes
+    assert g(A + 1, B, 16, L.DTYPE_F16, None) == L.ERR_ALIGN
+    assert f(A, B + 2, 4, 8, L.DTYPE_F32, None) == L.ERR_ALIGN
+    assert g(A + 60, A, 16, L.DTYPE_F32, None) == L.ERR_OVERLAP  # 64 bytes of fp32
+    assert g(A + 30, A, 16, L.DTYPE_F16, None) == L.ERR_OVERLAP
+    assert f(A + 248, A, 4, 8, L.DTYPE_F32, None) == L.ERR_OVERLAP   # x is 256 bytes
+    assert f(A + 256, A, 0, 8, L.DTYPE_F32, None) == L.OK
+    for dt in (L.DTYPE_BF16, L.DTYPE_F16, L.DTYPE_F32):
+        assert g(A, A, 0, dt, None) == L.OK and f(A, B, 0, 8, dt, None) == L.OK
+        assert g(A, B, -1, dt, None) == L.ERR_SHAPE and f(A, B, 4, 0, dt, None) == L.ERR_SHAPE
+
+
 def test_plans_per_format(L):
     """fp32 rows use at most 8 slots per lane; the TMA ring stays bf16-only."""
     old = L.ltxk_set_path(L.PATH_TMA)

@@ -656,6 +656,14 @@ def test_formats_share_the_arithmetic(oracle_mod, dtype):
     assert np.array_equal(bits(h), bits(oracle_mod.round_to(xf.astype(np.float64) + rf, dtype)))
     _, e_h = oracle_mod.rms_norm(h, cast(wf), 1e-6, exact=True)
     assert np.array_equal(e, e_h) and np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+    _, e_b = oracle_mod.gelu_tanh(xb, exact=True)
+    y, e = oracle_mod.gelu_tanh(cast(xf), exact=True)
+    assert y.dtype == dtype and np.array_equal(e, e_b)
+    assert np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
+    _, e_b = oracle_mod.geglu(xb, exact=True)
+    y, e = oracle_mod.geglu(cast(xf), exact=True)
+    assert y.dtype == dtype and y.shape == (6, 16) and np.array_equal(e, e_b)
+    assert np.array_equal(bits(y), bits(oracle_mod.round_to(e, dtype)))
 
 
 @pytest.mark.parametrize("dtype", [np.float16, np.float32])
@@ -672,6 +680,69 @@ def test_formats_match_torch_rms_norm_fp64(oracle_mod, dtype):
                      torch.from_numpy(w.astype(np.float64)),
                      eps=float(np.float32(1e-6))).numpy()
     np.testing.assert_allclose(ye, ref, rtol=1e-12, atol=1e-300)
+
+
+def _f32_grid(lo, hi, n, seed):
+    """n float32 values in [lo, hi] with full 24-bit significands."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(lo, hi, n).astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_gelu_formats_match_torch_and_numpy_rounding(oracle_mod, dtype):
+    # [-2, 4]: the literal tanh form is accurate there (see the bf16 pin), and
+    # torch's fp64 GELU gives the exact value; the stored result is numpy's
+    # own round-to-nearest-even conversion of it
+    torch = pytest.importorskip("torch")
+    if dtype == np.float16:
+        x = ALL16.view(np.float16)
+        x = x[np.isfinite(x) & (x >= -2) & (x <= 4)]
+    else:
+        x = _f32_grid(-2, 4, 20001, 31)
+    y, g = oracle_mod.gelu_tanh(x, exact=True)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x.astype(np.float64)),
+                                   approximate="tanh").numpy()
+    np.testing.assert_allclose(g, ref, rtol=1e-14, atol=1e-300)
+    assert y.dtype == dtype and np.array_equal(y, g.astype(dtype))
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_gelu_formats_tails_and_specials(oracle_mod, dtype):
+    lim = 60000.0 if dtype == np.float16 else 1e30
+    big = np.array([6, 9.5, 100, 1000, lim], dtype)
+    assert np.array_equal(oracle_mod.gelu_tanh(big), big)          # gelu(x) = x
+    # left tail: log(gelu/x) = 2z - log1p(e^{2z}), accurate where 1 + tanh z cancels
+    x = (np.linspace(-6, -1, 400) if dtype == np.float16 else _f32_grid(-20, -6, 400, 32)).astype(dtype)
+    y, g = oracle_mod.gelu_tanh(x, exact=True)
+    xv = x.astype(np.float64)
+    z = np.sqrt(2 / np.pi) * (xv + 0.044715 * xv ** 3)
+    np.testing.assert_allclose(np.log(g / xv), 2 * z - np.log1p(np.exp(2 * z)), rtol=1e-13)
+    assert np.array_equal(y, g.astype(dtype))        # down into the subnormals and zero
+    inf = np.array([np.inf, -np.inf, np.nan, -lim, 0.0, -0.0], dtype)
+    y = oracle_mod.gelu_tanh(inf)
+    assert y[0] == np.inf and np.isnan(y[1]) and np.isnan(y[2])   # -inf * 0 is NaN
+    assert y[3] == 0 and np.signbit(y[3]) and y[4] == 0 and not np.signbit(y[4])
+    assert np.signbit(y[5])
+
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_geglu_formats_value_times_gelu_of_gate(oracle_mod, dtype):
+    rng = np.random.default_rng(33)
+    rows, h = 5, 24
+    x = (rng.standard_normal((rows, 2 * h)) * 3).astype(dtype)
+    if dtype == np.float32:
+        # huge values on far-tail gates: the product is normal although the
+        # gelu of the gate is below binary32's smallest normal number
+        x[0, :h] = np.float32(2.0 ** 120)
+        x[0, h:] = np.linspace(-11.5, -10.5, h).astype(np.float32)
+    y, ye = oracle_mod.geglu(x, exact=True)
+    _, gate = oracle_mod.gelu_tanh(np.ascontiguousarray(x[:, h:]), exact=True)
+    np.testing.assert_allclose(ye, x[:, :h].astype(np.float64) * gate, rtol=1e-15, atol=1e-300)
+    assert y.dtype == dtype and np.array_equal(y, ye.astype(dtype))
+    if dtype == np.float32:
+        assert np.all(np.abs(gate[0]) < 2.0 ** -126) and np.all(np.abs(y[0]) > 2.0 ** -100)
+    swapped = np.concatenate([x[:, h:], x[:, :h]], axis=1)
+    assert not np.array_equal(oracle_mod.geglu(swapped), y)
 
 
 def test_formats_reject_mixed_dtypes(oracle_mod):

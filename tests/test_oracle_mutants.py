@@ -52,8 +52,8 @@ MUTANTS = [
     ("gelu_exp_sign", "x / (1.0 + exp(-2.0 * z))", "x / (1.0 + exp(2.0 * z))"),
     ("gelu_half_scale", "sqrt(2.0 / M_PI)", "sqrt(1.0 / M_PI)"),
     ("geglu_halves_swapped",
-     "widen_bf16(x[r * 2 * h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + h + j]))",
-     "widen_bf16(x[r * 2 * h + h + j]) * gelu_tanh(widen_bf16(x[r * 2 * h + j]))"),
+     "const double v = value * gelu_tanh(gate);",
+     "const double v = gate * gelu_tanh(value);"),
     ("overflow_kept_finite", "if (r > ldexp(2.0 - ldexp(1.0, 1 - prec), emax)) r = INFINITY;", ""),
     ("f16_exponent_bias", "ldexp((double)(1024 + M), E - 25)", "ldexp((double)(1024 + M), E - 24)"),
     ("f16_subnormal_scale", "v = ldexp((double)M, -24)", "v = ldexp((double)M, -25)"),
