@@ -415,10 +415,12 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             d["sin"] = torch.from_numpy(inp["sin"]).to(dev)
         dev_bufs.append(d)
 
-    def call_args(i, x=None, y=None):
+    def call_args(i, x=None, y=None, res=None, h=None):
         c, d = cases[i], dev_bufs[i]
         x = d["x"] if x is None else x
         d = dict(d, y=d["y"] if y is None else y)
+        if c.kind == "add_norm":
+            d = dict(d, res=d["res"] if res is None else res, h=d["h"] if h is None else h)
         wp = None if d["w"] is None else d["w"].data_ptr()
         if c.kind == "rope_pos":
             return L.ltxk_rope, (d["y"].data_ptr(), x.data_ptr(), c.rows, c.heads, c.head_dim,
@@ -451,8 +453,8 @@ def run_ltxk(args, cases, inputs, world, rank, local):
     # prebuilt calls keep the host side of a launch to one ctypes call
     calls = [call_args(i) for i in range(len(cases))]
 
-    def launch(i, x=None, y=None):
-        fn, a = calls[i] if x is None and y is None else call_args(i, x, y)
+    def launch(i, x=None, y=None, res=None, h=None):
+        fn, a = calls[i] if x is None and y is None else call_args(i, x, y, res, h)
         st = fn(*a)
         if st != L.OK:
             raise L.LtxkError(st, "bench launch")
@@ -580,8 +582,14 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         hx = [_tensor(inp["x"]).reshape(-1).pin_memory() for inp in inputs]
         hy = [torch.empty(c.rows * c.hidden, dtype=d["y"].dtype).pin_memory()
               for c, d in zip(cases, dev_bufs)]
-        h2d = sum(h.numel() * h.element_size() for h in hx)
-        d2h = sum(h.numel() * h.element_size() for h in hy)
+        # the residual add streams its second input and second output (the
+        # new residual stream h) across the host link as well
+        hres = [_tensor(inp["res"]).reshape(-1).pin_memory() if c.kind == "add_norm" else None
+                for c, inp in zip(cases, inputs)]
+        hh = [torch.empty_like(hy[j]).pin_memory() if c.kind == "add_norm" else None
+              for j, c in enumerate(cases)]
+        h2d = sum(h.numel() * h.element_size() for h in hx + hres if h is not None)
+        d2h = sum(h.numel() * h.element_size() for h in hy + hh if h is not None)
         pipelined = all(c.kind == "norm" and c.dtype == "bf16" for c in cases)
         if pipelined:
             pstreams = [torch.cuda.Stream(dev) for _ in range(3)]
@@ -615,7 +623,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                 # the call itself on the pinned host tensors: the kernel reads x
                 # and writes y across the host link (zero-copy)
                 for j in range(n):
-                    launch(j, x=hx[j], y=hy[j])
+                    launch(j, x=hx[j], y=hy[j], res=hres[j], h=hh[j])
             e1.record(stream)
             torch.cuda.synchronize()
             if i >= 3:
@@ -628,9 +636,9 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                         "writes y across the host link (NVLink-C2C on GB300, zero-copy); "
                         "the shapes start on three streams in turn; weight resident"
                         if pipelined else
-                        "the ltxk call on pinned host x and y: the kernel reads x and writes "
-                        "y across the host link (zero-copy); weight, tables and other "
-                        "inputs resident")}
+                        "the ltxk call on pinned host x and y (and, for the residual add, "
+                        "residual and h): the kernel reads and writes them across the host "
+                        "link (zero-copy); weight, tables and conditioning vectors resident")}
 
     clocks = sampler.summary(t0, t1) if not args.no_clocks else None
 

@@ -432,6 +432,21 @@ struct SlotMap {
     }
   }
 
+  // fp32 rows without rotation: slot k of thread t is the two 4-float chunks
+  // c = 2k*GT + t and c + GT, so that every 16-byte access of a warp is one
+  // contiguous 512-byte span (an 8-float slot per lane would leave each
+  // access half of every 32-byte sector).  f(k, element offset of the first
+  // chunk, of the second, first exists, second exists).
+  template <class F>
+  __device__ __forceinline__ void each_chunk_slot(F&& f) const {
+    const int nc = nv * 2;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+      const int c = 2 * k * GT + t;
+      f(k, c * 4, (c + GT) * 4, c < nc, c + GT < nc);
+    }
+  }
+
   // Load this thread's slots of one row (fetch(off) returns one slot).
   template <class Vec, class Fetch>
   __device__ __forceinline__ void load(Vec (&v)[VPL], Fetch&& fetch) const {
@@ -445,6 +460,33 @@ struct SlotMap {
     }
   }
 };
+
+// Whether a row mode and format run on the chunk map above.
+template <int MODE, int FMT>
+struct ChunkMap {
+  static constexpr bool value =
+      FMT == kF32 && (MODE == kPlain || MODE == kAdaLN || MODE == kAddNorm);
+};
+
+// One fp32 slot from two chunks (absent chunks read as zeros), and back.
+__device__ __forceinline__ V32 load_chunks(const void* p, int64_t base, int lo, int hi, bool ok_lo,
+                                           bool ok_hi) {
+  const float* f = static_cast<const float*>(p) + base;
+  return V32{ok_lo ? ld_stream16(f + lo) : make_uint4(0u, 0u, 0u, 0u),
+             ok_hi ? ld_stream16(f + hi) : make_uint4(0u, 0u, 0u, 0u)};
+}
+__device__ __forceinline__ V32 load_chunks_ro(const void* p, int64_t base, int lo, int hi,
+                                              bool ok_lo, bool ok_hi) {
+  const float* f = static_cast<const float*>(p) + base;
+  return V32{ok_lo ? ld_ro16(f + lo) : make_uint4(0u, 0u, 0u, 0u),
+             ok_hi ? ld_ro16(f + hi) : make_uint4(0u, 0u, 0u, 0u)};
+}
+__device__ __forceinline__ void store_chunks(void* p, int64_t base, int lo, int hi, bool ok_lo,
+                                             bool ok_hi, const V32& v) {
+  float* f = static_cast<float*>(p) + base;
+  if (ok_lo) st16(f + lo, v.lo);
+  if (ok_hi) st16(f + hi, v.hi);
+}
 
 template <int FMT, int VPL>
 __device__ __forceinline__ float slots_sumsq(const typename Io<FMT>::Vec (&v)[VPL]) {
@@ -471,7 +513,30 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   const int64_t rb = row * a.hidden;
   const Vec ones = I::ones();
   const float2 inv2 = make_float2(inv_rms, inv_rms);
-  if constexpr (MODE == kPlain || MODE == kAddNorm) {
+  if constexpr (ChunkMap<MODE, FMT>::value) {
+    // the same arithmetic as below, on the chunk map
+    const int64_t cb = MODE == kAdaLN ? div_fast(row, a.rows_per_cond, a.cond_mul) * a.hidden : 0;
+    const float2 one2 = make_float2(1.f, 1.f);
+    m.each_chunk_slot([&](int k, int lo, int hi, bool ok_lo, bool ok_hi) {
+      const Vec wv = has_w ? load_chunks_ro(a.w, 0, lo, hi, ok_lo, ok_hi) : ones;
+      float2 o[4];
+      if constexpr (MODE == kAdaLN) {
+        const Vec sv = load_chunks_ro(a.scale, cb, lo, hi, ok_lo, ok_hi);
+        const Vec tv = load_chunks_ro(a.shift, cb, lo, hi, ok_lo, ok_hi);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 n = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+          o[i] = __ffma2_rn(n, __fadd2_rn(one2, I::pair(sv, i)), I::pair(tv, i));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          o[i] = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+      }
+      store_chunks(a.out, rb, lo, hi, ok_lo, ok_hi, I::pack(o[0], o[1], o[2], o[3]));
+    });
+    return;
+  } else if constexpr (MODE == kPlain || MODE == kAddNorm) {
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
       const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
@@ -659,8 +724,18 @@ rows_vec_kernel(const RowArgs a) {
   int parity = 0;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
   Vec v[VPL];
-  if (kPipe && first < a.rows)
-    m.load(v, [&](int off) { return I::load(a.x, first * a.hidden + off); });
+  // one row of slots of src at element base (the chunk map for fp32 rows
+  // without rotation, the vector map otherwise)
+  auto load_row = [&](Vec (&dst)[VPL], const void* src, int64_t base) {
+    if constexpr (ChunkMap<MODE, FMT>::value) {
+      m.each_chunk_slot([&](int k, int lo, int hi, bool ok_lo, bool ok_hi) {
+        dst[k] = load_chunks(src, base, lo, hi, ok_lo, ok_hi);
+      });
+    } else {
+      m.load(dst, [&](int off) { return I::load(src, base + off); });
+    }
+  };
+  if (kPipe && first < a.rows) load_row(v, a.x, first * a.hidden);
   for (int64_t row = first; row < a.rows; row += row_step) {
     const int64_t rb = row * a.hidden;
     if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
@@ -672,9 +747,9 @@ rows_vec_kernel(const RowArgs a) {
     Vec nv[kPipe ? VPL : 1];
     if constexpr (kPipe) {
       const int64_t next = row + row_step;
-      if (next < a.rows) m.load(nv, [&](int off) { return I::load(a.x, next * a.hidden + off); });
+      if (next < a.rows) load_row(nv, a.x, next * a.hidden);
     } else {
-      m.load(v, [&](int off) { return I::load(a.x, rb + off); });
+      load_row(v, a.x, rb);
     }
     if constexpr ((MODE == kInterleaved || MODE == kSplitHalf) && LTXK_TABLE_PREFETCH > 0) {
       const int64_t pos = row - div_fast(row, a.table_rows, a.table_mul) * a.table_rows;
@@ -685,12 +760,18 @@ rows_vec_kernel(const RowArgs a) {
     if constexpr (MODE == kAddNorm) {
       // h = round(x + res): stored as the new residual stream, then normalised
       Vec rv[VPL];
-      m.load(rv, [&](int off) { return I::load(a.res, rb + off); });
+      load_row(rv, a.res, rb);
 #pragma unroll
       for (int k = 0; k < VPL; ++k) v[k] = add8<FMT>(v[k], rv[k]);
-      m.each_slot([&](int k, int off, int, bool ok) {
-        if (ok) I::store(a.h_out, rb + off, v[k]);
-      });
+      if constexpr (ChunkMap<MODE, FMT>::value) {
+        m.each_chunk_slot([&](int k, int lo, int hi, bool ok_lo, bool ok_hi) {
+          store_chunks(a.h_out, rb, lo, hi, ok_lo, ok_hi, v[k]);
+        });
+      } else {
+        m.each_slot([&](int k, int off, int, bool ok) {
+          if (ok) I::store(a.h_out, rb + off, v[k]);
+        });
+      }
     }
 
     float ss = warp_sum(slots_sumsq<FMT>(v));
