@@ -675,19 +675,31 @@ struct GroupShape {
 // its next row before the epilogue of the current one, so HBM reads keep
 // flowing while rows are scaled and stored (costs one more row of slots in
 // registers).  Not for the residual-add form (two rows of inputs already).
+// Measured on GB300 under the bench protocol: split-half RoPE
+// [6144 x 32x64] 16.1 -> 15.4 us, so it is on there for the 16-bit formats
+// and rows of at most 8 warps (LTXK_PIPELINE_SPLIT; fp32 rows, and the
+// 512- and 1024-thread row groups, would spill the second row of slots);
+// interleaved RoPE unchanged, AdaLN +7 %, plain RMSNorm +1-2 %, so it is
+// off for them (LTXK_PIPELINE turns it on for every mode and format).
 #ifndef LTXK_PIPELINE
 #define LTXK_PIPELINE 0
 #endif
-template <int MODE>
+#ifndef LTXK_PIPELINE_SPLIT
+#define LTXK_PIPELINE_SPLIT 1
+#endif
+template <int MODE, int G, int FMT>
 struct Pipelined {
-  static constexpr bool value = LTXK_PIPELINE != 0 && MODE != kAddNorm;
+  static constexpr bool value =
+      LTXK_PIPELINE != 0
+          ? MODE != kAddNorm
+          : (MODE == kSplitHalf && FMT != kF32 && G <= 8 && LTXK_PIPELINE_SPLIT != 0);
 };
 
-template <int MODE, int VPL, int FMT>
+template <int MODE, int G, int VPL, int FMT>
 struct RegBudget {
   static constexpr int kW = Io<FMT>::kWords;
   static constexpr int kRegs =
-      kW * VPL * (Pipelined<MODE>::value ? 2 : 1) +
+      kW * VPL * (Pipelined<MODE, G, FMT>::value ? 2 : 1) +
                  (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
                   : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
                   : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
@@ -697,7 +709,7 @@ struct RegBudget {
 template <int MODE, int G, int VPL, int FMT>
 struct VecLaunch {
   static constexpr int kBlock = GroupShape<G>::kBlock;
-  static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, VPL, FMT>::kRegs);
+  static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, G, VPL, FMT>::kRegs);
   static constexpr int kMinBlocks = kMin < 1 ? 1 : kMin;
 };
 
@@ -720,7 +732,7 @@ rows_vec_kernel(const RowArgs a) {
   const SlotMap<MODE, VPL, GT> m(a, t);
 
   const int64_t row_step = static_cast<int64_t>(gridDim.x) * S::kGroupsPerCta;
-  constexpr bool kPipe = Pipelined<MODE>::value;
+  constexpr bool kPipe = Pipelined<MODE, G, FMT>::value;
   int parity = 0;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta + group;
   Vec v[VPL];
