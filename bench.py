@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -160,11 +161,27 @@ def kernel_family(kernel):
     return "rope" if kernel.startswith("rope_kernel") else "rows"
 
 
-def source_digest(family="rows"):
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_text(src: str) -> str:
+    """The code of a C++/CUDA source without its comments and with runs of
+    whitespace collapsed, so that a change to a comment alone keeps the
+    digest (string literals in these sources hold no comment markers)."""
+    return " ".join(_COMMENT.sub(" ", src).split())
+
+
+def source_digest(family="rows", read=None):
+    """Digest of the code (comments and layout aside) of a kernel family's
+    sources.  ``read(name)`` returns a source's text (default: the file)."""
     h = hashlib.sha256()
     for fn in KERNEL_SOURCES[family]:
-        with open(os.path.join(CSRC, fn), "rb") as f:
-            h.update(fn.encode() + b"\0" + f.read())
+        if read is None:
+            with open(os.path.join(CSRC, fn), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(fn)
+        h.update(fn.encode() + b"\0" + code_text(text).encode())
     return h.hexdigest()[:16]
 
 

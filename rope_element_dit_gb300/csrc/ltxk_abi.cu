@@ -1,12 +1,15 @@
 // ltxk_abi.cu -- the C ABI declared in include/ltxk.h: argument validation
 // (host only, before any CUDA call), the launch plan, and the launches.
 //
-// Operations: bf16 RMSNorm ("cuda-kernels" skill page, "Kernel-Specific
-// Guidelines / RMSNorm") and the fused RMSNorm + RoPE forms ("ltx-kernels"
-// README, opening list: rms_norm_rope, rms_norm_split_rope).  The launch
-// configuration replaces the page's "Thread Configuration" rule (one block
-// of min(hidden/2, max) threads per row) with persistent grids sized from
-// the SM count and each kernel's occupancy.
+// Operations: RMSNorm ("cuda-kernels" skill page, "Kernel-Specific
+// Guidelines / RMSNorm"), the fused RMSNorm + RoPE forms ("ltx-kernels"
+// README, opening list: rms_norm_rope, rms_norm_split_rope), the AdaLN and
+// residual-add forms, in bf16, fp16 or fp32 ("Supported Data Types").  The
+// launch configuration replaces the page's "Thread Configuration" rule (one
+// block of min(hidden/2, max) threads per row) with warps-per-row and slot
+// counts from a register budget, and grids sized by measurement: one CTA
+// per row group for the row-only forms, persistent CTAs (from the SM count
+// and each kernel's occupancy) for the fused ones.
 #include <cuda_runtime.h>
 
 #include <atomic>
