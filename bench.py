@@ -504,7 +504,13 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                              f"geglu_vec_kernel<unsigned int, {f}>")
             continue
         if c.kind == "rope_pos":
-            plans.append(f"rope_kernel<{1 if c.mode == 0 else 2}, {DTYPE_CODES[c.dtype]}, true>")
+            # the library's block rule: 64 threads when a row's 16-byte units
+            # (lo/hi pairs for split-half) fit one pass of 64 threads
+            units = c.hidden // 8 if c.mode == 0 else c.heads * (c.head_dim // 16)
+            per_thread = (4 if c.mode == 0 else 2) // (2 if c.dtype == "f32" else 1)
+            block = 64 if units <= 64 * per_thread else 128
+            plans.append(f"rope_kernel<{1 if c.mode == 0 else 2}, {DTYPE_CODES[c.dtype]}, true, "
+                         f"{block}>")
             continue
         op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE,
               "adaln": L.OP_RMS_NORM_ADALN, "add_norm": L.OP_ADD_RMS_NORM}[c.kind]

@@ -16,7 +16,9 @@
 //
 // Design.  The angles of a token are shared by all heads of its row, so
 // each CTA computes them once per row into shared memory and every head
-// reuses them (heads-fold reuse).  Persistent 128-thread CTAs:
+// reuses them (heads-fold reuse).  Persistent CTAs of 128 threads (64 when a
+// row is at most 64 threads' units, so that small rows fill every unit slot
+// and twice the rows are in flight per SM):
 //   * the per-pair frequencies theta^(-k/n) are launch constants: the host
 //     evaluates them in fp64, as turns per coordinate unit theta^(-k/n)/(2 pi)
 //     split into two floats th + tl (exact to ~2^-48), and passes them in the
@@ -48,7 +50,12 @@
 
 namespace ltxk {
 
+// Threads per CTA: 128, or 64 when a row is at most 64 threads' units (one
+// pass either way): a small row then fills every unit slot of a thread, and
+// twice the CTAs -- rows in flight -- fit on an SM.
 constexpr int kRopeBlock = 128;
+constexpr int kRopeSmallBlock = 64;
+constexpr int kRopeThreadsPerSm = 1024;
 // 16-byte units per thread per pass over a row: 16 registers of row data
 // (split-half units are two vectors, fp32 vectors two registers wide).
 template <int MODE, int FMT>
@@ -56,7 +63,6 @@ struct RopeUnits {
   static constexpr int value = (MODE == kSplitHalf ? 2 : 4) / (FMT == kF32 ? 2 : 1);
 };
 constexpr int kRopeMaxPairs = 256;    // head_dim <= 512 (frequencies travel as kernel parameters)
-constexpr int kRopeCtasPerSm = 8;
 
 struct RopeArgs {
   void* out;
@@ -123,8 +129,8 @@ __device__ __forceinline__ float2 angle_cs_turns(float c, float2 t) {
 
 // VEC: 16-byte slots (interleaved: head_dim % 8 == 0, split-half: % 16 == 0,
 // 16-byte aligned pointers); otherwise one thread per rotation pair.
-template <int MODE, int FMT, bool VEC>
-__global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const RopeArgs a) {
+template <int MODE, int FMT, bool VEC, int BLOCK>
+__global__ void __launch_bounds__(BLOCK, kRopeThreadsPerSm / BLOCK) rope_kernel(const RopeArgs a) {
   using I = Io<FMT>;
   using Vec = typename I::Vec;
   constexpr int kU = RopeUnits<MODE, FMT>::value;
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
     const int64_t rem = s - ct * a.hw;
     const int64_t ch = div_fast(rem, a.w, a.w_mul);
     const int64_t coord[3] = {ct, ch, rem - ch * a.w};
-    for (int k = tid; k < P; k += kRopeBlock) {
+    for (int k = tid; k < P; k += BLOCK) {
       int axis, kk, n;
       pair_axis(a, k, &axis, &kk, &n);
       const int64_t c = coord[axis];
@@ -157,14 +163,14 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
   const int64_t HD = static_cast<int64_t>(a.heads) * D;
   // Units of a row: 16-byte vectors (interleaved), (lo, hi) vector pairs of a
   // head (split-half), or single rotation pairs (element-wise).  Unit u of a
-  // pass is u0 + i * kRopeBlock; its column in the head (interleaved) or its
+  // pass is u0 + i * BLOCK; its column in the head (interleaved) or its
   // (head, vector pair) (split-half) advance by fixed steps, no division.
   const int qph = D >> 4;   // split-half: vector pairs per head
   const int units = VEC ? (MODE == kInterleaved ? static_cast<int>(HD >> 3) : a.heads * qph)
                         : a.heads * P;
-  const int step_col = (kRopeBlock * 8) % D;
-  const int step_head = qph > 0 ? kRopeBlock / qph : 0;
-  const int step_jv = qph > 0 ? kRopeBlock % qph : 0;
+  const int step_col = (BLOCK * 8) % D;
+  const int step_head = qph > 0 ? BLOCK / qph : 0;
+  const int step_jv = qph > 0 ? BLOCK % qph : 0;
 
   int buf = 0;
   if (static_cast<int64_t>(blockIdx.x) < a.rows) fill_table(blockIdx.x, 0);
@@ -176,14 +182,14 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
         if constexpr (MODE == kInterleaved) {
 #pragma unroll
           for (int i = 0; i < kU; ++i) {
-            const int u = base + tid + i * kRopeBlock;
+            const int u = base + tid + i * BLOCK;
             if (u < units) lo[i] = I::load(a.x, rb + static_cast<int64_t>(u) * 8);
           }
         } else {
           int head = (base + tid) / qph, jv = (base + tid) - head * qph;
 #pragma unroll
           for (int i = 0; i < kU; ++i) {
-            const int u = base + tid + i * kRopeBlock;
+            const int u = base + tid + i * BLOCK;
             if (u < units) {
               const int64_t off = static_cast<int64_t>(head) * D + jv * 8;
               lo[i] = I::load(a.x, rb + off);
@@ -208,13 +214,13 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
     const float* ct = cosv[buf];
     const float* st = sinv[buf];
     if constexpr (VEC) {
-      for (int base = 0; base < units; base += kRopeBlock * kU) {
+      for (int base = 0; base < units; base += BLOCK * kU) {
         if (base > 0) load_pass(base);
         if constexpr (MODE == kInterleaved) {
           int col = ((base + tid) * 8) % D;   // element column of unit i in its head
 #pragma unroll
           for (int i = 0; i < kU; ++i) {
-            const int u = base + tid + i * kRopeBlock;
+            const int u = base + tid + i * BLOCK;
             if (u < units) {
               const int p0 = col >> 1;   // rotation pairs p0 .. p0 + 3 (p0 % 4 == 0)
               const float4 c4 = *reinterpret_cast<const float4*>(ct + p0);
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
           int head = (base + tid) / qph, jv = (base + tid) - head * qph;
 #pragma unroll
           for (int i = 0; i < kU; ++i) {
-            const int u = base + tid + i * kRopeBlock;
+            const int u = base + tid + i * BLOCK;
             if (u < units) {
               const int64_t off = static_cast<int64_t>(head) * D + jv * 8;
               const float4 c0 = *reinterpret_cast<const float4*>(ct + jv * 8);
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(kRopeBlock, kRopeCtasPerSm) rope_kernel(const 
         }
       }
     } else {
-      for (int q = tid; q < units; q += kRopeBlock) {
+      for (int q = tid; q < units; q += BLOCK) {
         const int head = q / P, p = q - head * P;
         const int64_t ia = MODE == kInterleaved ? static_cast<int64_t>(head) * D + 2 * p
                                                 : static_cast<int64_t>(head) * D + p;
@@ -326,16 +332,32 @@ cudaError_t sm_count(int* sms) {
 }
 
 template <int MODE, int FMT>
-const void* rope_fn(bool vec) {
-  return vec ? reinterpret_cast<const void*>(&ltxk::rope_kernel<MODE, FMT, true>)
-             : reinterpret_cast<const void*>(&ltxk::rope_kernel<MODE, FMT, false>);
+const void* rope_fn(bool vec, bool small) {
+  if (!vec) return reinterpret_cast<const void*>(&ltxk::rope_kernel<MODE, FMT, false, ltxk::kRopeBlock>);
+  return small ? reinterpret_cast<const void*>(&ltxk::rope_kernel<MODE, FMT, true, ltxk::kRopeSmallBlock>)
+               : reinterpret_cast<const void*>(&ltxk::rope_kernel<MODE, FMT, true, ltxk::kRopeBlock>);
 }
 
 template <int MODE>
-const void* rope_fn_fmt(int fmt, bool vec) {
-  if (fmt == ltxk::kF16) return rope_fn<MODE, ltxk::kF16>(vec);
-  if (fmt == ltxk::kF32) return rope_fn<MODE, ltxk::kF32>(vec);
-  return rope_fn<MODE, ltxk::kBf16>(vec);
+const void* rope_fn_fmt(int fmt, bool vec, bool small) {
+  if (fmt == ltxk::kF16) return rope_fn<MODE, ltxk::kF16>(vec, small);
+  if (fmt == ltxk::kF32) return rope_fn<MODE, ltxk::kF32>(vec, small);
+  return rope_fn<MODE, ltxk::kBf16>(vec, small);
+}
+
+// Units of a row of the vector kernel (16-byte vectors, or lo/hi vector
+// pairs for split-half), and units per thread per pass.
+int64_t row_units(int mode, int heads, int head_dim) {
+  return mode == LTXK_ROPE_INTERLEAVED ? static_cast<int64_t>(heads) * head_dim / 8
+                                       : static_cast<int64_t>(heads) * (head_dim / 16);
+}
+int units_per_thread(int mode, int fmt) {
+  using ltxk::RopeUnits;
+  if (mode == LTXK_ROPE_INTERLEAVED)
+    return fmt == ltxk::kF32 ? RopeUnits<ltxk::kInterleaved, ltxk::kF32>::value
+                             : RopeUnits<ltxk::kInterleaved, ltxk::kBf16>::value;
+  return fmt == ltxk::kF32 ? RopeUnits<ltxk::kSplitHalf, ltxk::kF32>::value
+                           : RopeUnits<ltxk::kSplitHalf, ltxk::kBf16>::value;
 }
 
 }  // namespace
@@ -389,13 +411,17 @@ extern "C" int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int 
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return fail(e);
-  const int64_t cap = static_cast<int64_t>(sms) * ltxk::kRopeCtasPerSm;
+  const bool small = vec && row_units(mode, heads, head_dim) <=
+                               static_cast<int64_t>(ltxk::kRopeSmallBlock) *
+                                   units_per_thread(mode, fmt);
+  const int block = small ? ltxk::kRopeSmallBlock : ltxk::kRopeBlock;
+  const int64_t cap = static_cast<int64_t>(sms) * (ltxk::kRopeThreadsPerSm / block);
   const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
   const void* fn = mode == LTXK_ROPE_INTERLEAVED
-                       ? rope_fn_fmt<ltxk::kInterleaved>(fmt, vec)
-                       : rope_fn_fmt<ltxk::kSplitHalf>(fmt, vec);
+                       ? rope_fn_fmt<ltxk::kInterleaved>(fmt, vec, small)
+                       : rope_fn_fmt<ltxk::kSplitHalf>(fmt, vec, small);
   void* params[] = {&a};
-  e = cudaLaunchKernel(fn, dim3(grid), dim3(ltxk::kRopeBlock), params, 0,
+  e = cudaLaunchKernel(fn, dim3(grid), dim3(block), params, 0,
                        reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(e);
   return LTXK_OK;
