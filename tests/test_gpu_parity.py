@@ -309,6 +309,7 @@ ROPE_SHAPES = [  # (rows, heads, head_dim, seq_len)
     (5, 1, 2, 5), (6, 1, 4, 3), (10, 2, 8, 4), (33, 3, 16, 11), (70, 4, 64, 24),
     (16, 32, 128, 8), (9, 2, 6, 9), (21, 5, 48, 7), (13, 2, 40, 13),
     (4, 64, 256, 2), (3, 80, 128, 1),
+    (5003, 8, 64, 61),   # several rows per warp of the persistent (pipelined) grid
 ]
 
 
