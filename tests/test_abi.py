@@ -400,3 +400,22 @@ def test_host_pipeline_rejects_partial_overlap(L):
     assert f(A + 16, A, None, 4, 8, 1e-6, S, 1 << 20, [0], 1) == L.ERR_OVERLAP
     assert f(A, A + 62, None, 4, 8, 1e-6, S, 1 << 20, [0], 1) == L.ERR_OVERLAP
     assert f(A, A, None, 0, 8, 1e-6, S, 1 << 20, [0], 1) == L.OK      # in place, empty
+
+
+def test_helpers_reject_host_tensors(L):
+    """The torch helpers take device tensors only: a host tensor is an error
+    before any CUDA call, never a CPU computation."""
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    cos = torch.zeros(4, 8)
+    for call in (lambda: L.rms_norm(x),
+                 lambda: L.rms_norm_rope(x, None, cos, cos, 4, 16, L.ROPE_INTERLEAVED, 1e-6),
+                 lambda: L.rms_norm_adaln(x, None, x[:1], x[:1]),
+                 lambda: L.add_rms_norm(x, x),
+                 lambda: L.gelu_tanh(x),
+                 lambda: L.geglu(x),
+                 lambda: L.rope(x, 4, 16, L.ROPE_INTERLEAVED)):
+        with pytest.raises(TypeError):
+            call()
+    with pytest.raises(TypeError):
+        L.rms_norm(torch.zeros(4, 64, dtype=torch.float64))
