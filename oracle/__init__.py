@@ -1,4 +1,6 @@
-"""fp64 CPU oracle for bf16 RMSNorm and fused RMSNorm+RoPE -- TEST INFRASTRUCTURE.
+"""fp64 CPU oracle for the RMSNorm family (plain, fused with RoPE, AdaLN,
+residual add), standalone RoPE from positions, and tanh GELU / GEGLU --
+TEST INFRASTRUCTURE.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product path (the CUDA library and
@@ -7,9 +9,9 @@ the product path: the two share no code.
 
 The arithmetic lives in ``oracle.c`` (plain C, binary64, sequential sums); this
 module only compiles it with gcc and marshals numpy arrays through ctypes.
-bfloat16 tensors travel as ``numpy.uint16`` arrays of bit patterns; the row
-operations also take ``numpy.float16`` (IEEE binary16) and ``numpy.float32``
-arrays, the pages' other two precision modes, and answer in the same type.
+bfloat16 tensors travel as ``numpy.uint16`` arrays of bit patterns; every
+operation also takes ``numpy.float16`` (IEEE binary16) and ``numpy.float32``
+arrays, the pages' other two precision modes, and answers in the same type.
 
 Definition followed (the pages print no formula; see ``oracle.c`` for the
 page sections cited):

@@ -1,6 +1,8 @@
 /*
- * oracle.c -- plain, slow, fp64 CPU oracle for bf16 RMSNorm and the fused
- * RMSNorm + rotary-embedding (RoPE) forms.
+ * oracle.c -- plain, slow, fp64 CPU oracle for RMSNorm, the fused RMSNorm +
+ * rotary-embedding (RoPE) forms, the AdaLN and residual-add norms, the
+ * standalone RoPE with angles from token positions, and the tanh GELU and
+ * GEGLU, each in bfloat16, IEEE binary16 and binary32.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the independent definition that the
  * CUDA path is checked against.  Only the test suite, the smoke check and the
@@ -53,12 +55,27 @@
  * Every exported function is re-entrant (no global state), so callers may run
  * disjoint row ranges on several threads at once.
  *
- * Parity pins (tests in tests/test_oracle.py): brute force over all 65536
- * bfloat16 patterns for the rounding, hand-computed cases at hidden = 4, the
- * unit-RMS closed form, exact power-of-two scale invariance, the fp64
- * library RMSNorm of PyTorch, identity / quarter-turn / half-turn rotations,
- * pair-norm preservation and the permutation that maps split-half pairing to
- * interleaved pairing.  No function here is left unpinned.
+ * Parity pins (tests in tests/test_oracle.py; tests/test_oracle_mutants.py
+ * checks that a plausible mistake in each part fails one of them):
+ *   - rounding: brute force over all 65536 bfloat16 and binary16 patterns,
+ *     ties to even, specials, numpy's and the hardware's own conversions;
+ *   - RMSNorm: hand-computed cases at hidden = 4, the unit-RMS closed form,
+ *     exact power-of-two scale invariance, the fp64 library RMSNorm of
+ *     PyTorch;
+ *   - RoPE on tables: identity / quarter-turn / half-turn rotations,
+ *     pair-norm preservation, the permutation that maps split-half pairing
+ *     to interleaved pairing, the table row of each row;
+ *   - AdaLN and the residual add: hand cases, the reductions to plain
+ *     RMSNorm, affinity in scale and shift, h as the rounded sum;
+ *   - RoPE from positions: identity at token 0, the closed-form
+ *     frequencies, the 3-axis coordinates, additivity of the angle in the
+ *     position, norms and the pairing permutation;
+ *   - GELU / GEGLU: the odd-part identity gelu(x) - gelu(-x) = x, PyTorch's
+ *     fp64 tanh form, the log-sigmoid form of the far tail, value times
+ *     gelu(gate), in every format;
+ *   - formats: inputs every format holds exactly give the same exact
+ *     results in every format.
+ * No function here is left unpinned.
  */
 #define _DEFAULT_SOURCE 1
 #include <math.h>
