@@ -54,6 +54,9 @@ MUTANTS = [
     ("geglu_halves_swapped",
      "const double v = value * gelu_tanh(gate);",
      "const double v = gate * gelu_tanh(value);"),
+    ("gelu_stored_as_bf16", "        store_elem(fmt, y, i, v);\n", "        store_elem(FMT_BF16, y, i, v);\n"),
+    ("geglu_gate_shifted", "load_elem(fmt, x, r * 2 * h + h + j)",
+     "load_elem(fmt, x, r * 2 * h + h + (j + 1) % h)"),
     ("overflow_kept_finite", "if (r > ldexp(2.0 - ldexp(1.0, 1 - prec), emax)) r = INFINITY;", ""),
     ("f16_exponent_bias", "ldexp((double)(1024 + M), E - 25)", "ldexp((double)(1024 + M), E - 24)"),
     ("f16_subnormal_scale", "v = ldexp((double)M, -24)", "v = ldexp((double)M, -25)"),
@@ -118,6 +121,11 @@ def _pin_calls():
         ("gelu_torch", pins.test_gelu_matches_tanh_form_and_torch, ()),
         ("gelu_tails", pins.test_gelu_tails, ()),
         ("geglu", pins.test_geglu_value_times_gelu_of_gate, ()),
+        ("gelu_fmt_f16", pins.test_gelu_formats_match_torch_and_numpy_rounding, (np.float16,)),
+        ("gelu_fmt_f32", pins.test_gelu_formats_match_torch_and_numpy_rounding, (np.float32,)),
+        ("gelu_tails_f32", pins.test_gelu_formats_tails_and_specials, (np.float32,)),
+        ("geglu_fmt_f16", pins.test_geglu_formats_value_times_gelu_of_gate, (np.float16,)),
+        ("geglu_fmt_f32", pins.test_geglu_formats_value_times_gelu_of_gate, (np.float32,)),
         ("f16_widen", pins.test_f16_widen_all_patterns, ()),
         ("f16_midpoints", pins.test_f16_round_identity_and_midpoints, ()),
         ("f16_specials", pins.test_f16_round_specials, ()),
