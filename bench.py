@@ -320,7 +320,7 @@ def cpu_baseline(cases, inputs, seconds):
     reps = 1
     if frac >= 1.0:
         t_full, _ = cpu_oracle_time(cases, inputs, 1.0, threads)
-        reps = max(1, int(seconds / max(t_full, 1e-6)))
+        reps = max(1, math.ceil(seconds / max(t_full, 1e-6)))   # at least `seconds`
     tot_t, tot_b = 0.0, 0
     for _ in range(reps):
         tt, bb = cpu_oracle_time(cases, inputs, frac, threads)
