@@ -1,5 +1,6 @@
-// ltxk_kernels.cuh -- device code for RMSNorm and fused RMSNorm + RoPE on
-// sm_103a (GB300), for bf16, fp16 and fp32 rows.
+// ltxk_kernels.cuh -- device code for RMSNorm, fused RMSNorm + RoPE, the
+// AdaLN-modulated norm and the fused residual add + RMSNorm on sm_103a
+// (GB300), for bf16, fp16 and fp32 rows.
 //
 // The operation (no formula is printed on the pages; this is the definition
 // the library implements):
@@ -16,7 +17,10 @@
 // The path is bound by HBM bandwidth (4 bytes moved per element against a
 // handful of fp32 operations), so it uses no tensor cores.  Design:
 //   * Each row is read from HBM exactly once, as 16-byte vectors, into
-//     registers; a group of G warps owns one row (G = 1 for hidden <= 4096).
+//     registers; a group of G warps owns one row, with G and the slots per
+//     lane chosen by the host planner (e.g. G = 4 for hidden 3072 and 4096).
+//     fp32 rows without rotation use a chunk map (two 4-float chunks per
+//     slot) so that every warp access is one contiguous span.
 //   * fp32 sum of squares: per-lane partials, an xor-butterfly over the
 //     warp, then (G > 1) a fixed-order sum of the G warp totals through
 //     shared memory.  Every thread ends with the same bit-identical total.
@@ -31,8 +35,11 @@
 //     computation of 2x2 determinants", Math. Comp. 82, 2013), which keeps
 //     the relative error of a rotated value at a few fp32 ulps even when the
 //     two products nearly cancel.
-//   * Persistent grid: CTAs stride over rows, so any row count (ragged
-//     tails included) is spread over all SMs.
+//   * CTAs stride over rows, so any grid covers any row count: the host
+//     launches one CTA per row group for the row-only forms and persistent
+//     grids for the fused ones; split-half rows of the 16-bit formats are
+//     software-pipelined (a warp loads its next row before this row's
+//     epilogue).
 #pragma once
 
 #include <cuda_bf16.h>
