@@ -1,6 +1,9 @@
 /*
- * ltxk.h -- C ABI of libltxk.so: bf16 RMSNorm and fused RMSNorm + rotary
- * position embedding (RoPE) on one NVIDIA GB300 GPU (sm_103a).
+ * ltxk.h -- C ABI of libltxk.so: RMSNorm and fused RMSNorm + rotary position
+ * embedding (RoPE) on one NVIDIA GB300 GPU (sm_103a), with the AdaLN and
+ * residual-add norms, standalone RoPE from token positions and the tanh
+ * GELU / GEGLU, in bfloat16 (the calls without a dtype), fp16 and fp32 (the
+ * _dt calls).
  *
  * Where the operations come from
  *   RMSNorm: "cuda-kernels" skill page (Hugging Face), sections "Kernel-
@@ -25,6 +28,10 @@
  *   - Tensor pointers are DEVICE pointers (or managed memory) of the current
  *     CUDA device.  bfloat16 data travel as void* (IEEE-754 binary32 upper
  *     halves, little-endian).  All tensors are dense and row-major.
+ *     Page-locked host memory the device can address (cudaHostAlloc or
+ *     cudaHostRegister; on GB300 through NVLink-C2C) may be passed as well:
+ *     the kernels then read and write it across the host link themselves
+ *     (zero-copy), with the same results.
  *   - The caller owns and allocates every buffer (the out-variant convention
  *     of the pages' `Tensor! out` ops); the library allocates no device
  *     memory and keeps no per-call state.
