@@ -80,3 +80,44 @@ def test_captured_calls_replay_with_new_inputs():
             assert np.array_equal(a, b), f"call {i}, inputs {seed}"
         # and the replayed norm is the oracle's
         assert compare_bf16(replayed[0], oracle.rms_norm(xn, bits(w), 1e-6))["ok"]
+
+
+def test_concurrent_host_threads_on_separate_streams():
+    """Calls from several host threads at once, each on its own stream:
+    the per-device caches are shared under a lock and the last CUDA error is
+    per thread, so every thread gets the results of a lone caller."""
+    import threading
+    heads, D, S = 8, 64, 48
+    H = heads * D
+    w = dev(synth.normal_bf16(411, 2, H, 1.0, 0.1))
+    cos, sin = (torch.from_numpy(t).cuda() for t in synth.rope_table_1d(S, D))
+    sc = dev(synth.normal_bf16(411, 3, 2 * H, 0.0, 0.5).reshape(2, H))
+    sh = dev(synth.normal_bf16(411, 4, 2 * H, 0.0, 0.5).reshape(2, H))
+    data = [tuple(dev(a) for a in inputs(420 + i)) for i in range(4)]
+    expect = []
+    for x, r in data:                      # one at a time
+        expect.append([bits(o) for o in run_all(x, r, w, cos, sin, sc, sh, heads, D, S)])
+    torch.cuda.synchronize()
+    got, errors = [None] * len(data), []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                x, r = data[i]
+                for _ in range(20):
+                    outs = run_all(x, r, w, cos, sin, sc, sh, heads, D, S)
+                s.synchronize()
+                got[i] = [bits(o) for o in outs]
+        except Exception as e:             # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(data))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(len(data)):
+        for a, b in zip(got[i], expect[i]):
+            assert np.array_equal(a, b), f"thread {i}"
