@@ -48,6 +48,19 @@ KERNEL_ROWS_VEC = 1
 KERNEL_ROWS_ELEM = 2
 KERNEL_ROWS_TMA = 3
 
+__all__ = [
+    # torch helpers (device tensors in, device tensors out)
+    "rms_norm", "rms_norm_rope", "rms_norm_adaln", "add_rms_norm", "rope", "gelu_tanh",
+    "geglu", "rms_norm_host",
+    # errors and constants
+    "LtxkError", "Plan", "LIB_PATH", "EXPORTS",
+    "OK", "ERR_NULL", "ERR_SHAPE", "ERR_ALIGN", "ERR_MODE", "ERR_OVERLAP", "ERR_CUDA",
+    "ERR_TIMEOUT", "ERR_DTYPE", "ROPE_INTERLEAVED", "ROPE_SPLIT_HALF",
+    "DTYPE_BF16", "DTYPE_F16", "DTYPE_F32", "PATH_AUTO", "PATH_REGISTERS", "PATH_TMA",
+    "OP_RMS_NORM", "OP_RMS_NORM_ROPE", "OP_RMS_NORM_ADALN", "OP_ADD_RMS_NORM",
+    "KERNEL_NONE", "KERNEL_ROWS_VEC", "KERNEL_ROWS_TMA", "KERNEL_ROWS_ELEM",
+]
+
 # Every entry point include/ltxk.h declares.
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_adaln", "ltxk_rms_norm_host", "ltxk_add_rms_norm",
@@ -57,6 +70,7 @@ EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt", "ltxk_rope",
            "ltxk_gelu_tanh_dt", "ltxk_geglu_dt",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
+__all__ += list(EXPORTS)
 
 
 class LtxkError(RuntimeError):
