@@ -239,6 +239,23 @@ LTXK_API int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int he
                        ltxk_stream_t stream);
 
 /*
+ * ltxk_rope_tables -- the cos and sin tables of the fused RMSNorm + RoPE
+ * (ltxk_rms_norm_rope_seq's cos/sin inputs) for token positions, computed on
+ * the device with ltxk_rope's angles: row s of each table holds, for the
+ * head_dim/2 pairs, cos and sin of the angle ltxk_rope gives token
+ * s mod (T*H*W) (same coordinates, pair split and frequencies).
+ *   cos_out, sin_out  [tokens, head_dim/2] fp32 on the device, 4-byte
+ *                     aligned; they must not overlap (LTXK_ERR_OVERLAP).
+ *   tokens >= 0 (0 is a no-op); tokens * head_dim <= 2^40.
+ *   head_dim, grid_*, pairs_*, theta  as for ltxk_rope (head_dim <= 512).
+ * Each value is within about 2 * 2^-24 of the exact cos / sin for
+ * coordinates below 2^24.  Writes 8 bytes per pair and token.
+ */
+LTXK_API int ltxk_rope_tables(float* cos_out, float* sin_out, int64_t tokens, int head_dim,
+                              int64_t grid_t, int64_t grid_h, int64_t grid_w, int pairs_t,
+                              int pairs_h, int pairs_w, double theta, ltxk_stream_t stream);
+
+/*
  * ltxk_gelu_tanh -- elementwise tanh-approximated GELU, bf16 -> bf16:
  *   y = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
  * ("cuda-kernels" skill page, "Kernel-Specific Guidelines / GEGLU vs GELU":

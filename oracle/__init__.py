@@ -102,6 +102,9 @@ def _load():
             lib.oracle_rope_positions.argtypes = [I32, P, P, I64, I64, I64, I32, I64, I64, I64,
                                                   I64, I64, I64, ctypes.c_double, I64, P]
             lib.oracle_rope_positions.restype = I32
+            lib.oracle_rope_tables.argtypes = [P, P, I64, I64, I64, I64, I64, I64, I64, I64,
+                                               ctypes.c_double]
+            lib.oracle_rope_tables.restype = I32
             lib.oracle_gelu_tanh_fmt.argtypes = [I32, P, P, I64, P]
             lib.oracle_gelu_tanh_fmt.restype = None
             lib.oracle_geglu_fmt.argtypes = [I32, P, P, I64, I64, P]
@@ -352,6 +355,21 @@ def rope(x, heads, head_dim, mode, grid, pairs, theta=10000.0, *, threads: int =
     _run_blocks(run, rows, threads)
     y = y.reshape(x.shape)
     return (y, ye.reshape(x.shape)) if exact else y
+
+
+def rope_tables(tokens, head_dim, grid, pairs, theta=10000.0):
+    """Oracle cos / sin tables ``[tokens, head_dim/2]`` (float64) of the
+    angles of ``rope``: row s is token ``s mod (T*H*W)``."""
+    P = head_dim // 2
+    c = np.empty((tokens, P), np.float64)
+    s = np.empty((tokens, P), np.float64)
+    T, H, W = grid
+    nt, nh, nw = pairs
+    rc = _load().oracle_rope_tables(_ptr(c), _ptr(s), tokens, head_dim, T, H, W, nt, nh, nw,
+                                    float(theta))
+    if rc != 0:
+        raise ValueError(f"oracle_rope_tables failed ({rc})")
+    return c, s
 
 
 def gelu_tanh(x, *, threads: int = 1, exact: bool = False):

@@ -407,6 +407,22 @@ static void rope_angles(int64_t s, int64_t T, int64_t H, int64_t W,
     }
 }
 
+/* cos and sin tables [tokens, head_dim/2] of the same angles: row s holds
+ * token s mod (T*H*W).  Returns 0, or -2 on an invalid argument. */
+int oracle_rope_tables(double* cos_out, double* sin_out, int64_t tokens, int64_t head_dim,
+                       int64_t T, int64_t H, int64_t W, int64_t nt, int64_t nh, int64_t nw,
+                       double theta) {
+    if (tokens < 0 || head_dim <= 0 || head_dim % 2 != 0) return -2;
+    if (T <= 0 || H <= 0 || W <= 0 || nt < 0 || nh < 0 || nw < 0 ||
+        nt + nh + nw != head_dim / 2 || !(theta > 0.0))
+        return -2;
+    const int64_t P = head_dim / 2;
+    for (int64_t s = 0; s < tokens; ++s)
+        rope_angles(s % (T * H * W), T, H, W, nt, nh, nw, theta, cos_out + s * P,
+                    sin_out + s * P);
+    return 0;
+}
+
 /* x, y: [rows, heads*head_dim] in format fmt; row r is token
  * (first_row + r) mod (T*H*W).  Returns 0, -1 on allocation failure, -2 on
  * an invalid argument. */

@@ -50,8 +50,8 @@ KERNEL_ROWS_TMA = 3
 
 __all__ = [
     # torch helpers (device tensors in, device tensors out)
-    "rms_norm", "rms_norm_rope", "rms_norm_adaln", "add_rms_norm", "rope", "gelu_tanh",
-    "geglu", "rms_norm_host",
+    "rms_norm", "rms_norm_rope", "rms_norm_adaln", "add_rms_norm", "rope", "rope_tables",
+    "gelu_tanh", "geglu", "rms_norm_host",
     # errors and constants
     "LtxkError", "Plan", "LIB_PATH", "EXPORTS",
     "OK", "ERR_NULL", "ERR_SHAPE", "ERR_ALIGN", "ERR_MODE", "ERR_OVERLAP", "ERR_CUDA",
@@ -68,7 +68,7 @@ EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
            "ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
            "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt", "ltxk_rope",
-           "ltxk_gelu_tanh_dt", "ltxk_geglu_dt",
+           "ltxk_gelu_tanh_dt", "ltxk_geglu_dt", "ltxk_rope_tables",
            "ltxk_status_string", "ltxk_last_cuda_error", "ltxk_plan_launch")
 __all__ += list(EXPORTS)
 
@@ -129,6 +129,9 @@ def _load():
     lib.ltxk_gelu_tanh.restype = I32
     lib.ltxk_geglu.argtypes = [P, P, I64, I64, P]
     lib.ltxk_geglu.restype = I32
+    lib.ltxk_rope_tables.argtypes = [P, P, I64, I32, I64, I64, I64, I32, I32, I32,
+                                     ctypes.c_double, P]
+    lib.ltxk_rope_tables.restype = I32
     lib.ltxk_gelu_tanh_dt.argtypes = [P, P, I64, I32, P]
     lib.ltxk_gelu_tanh_dt.restype = I32
     lib.ltxk_geglu_dt.argtypes = [P, P, I64, I64, I32, P]
@@ -233,6 +236,12 @@ def ltxk_gelu_tanh(out, x, n, stream) -> int:
 
 def ltxk_geglu(out, x, rows, hidden, stream) -> int:
     return _lib.ltxk_geglu(out, x, rows, hidden, stream)
+
+
+def ltxk_rope_tables(cos_out, sin_out, tokens, head_dim, grid_t, grid_h, grid_w, pairs_t,
+                     pairs_h, pairs_w, theta, stream) -> int:
+    return _lib.ltxk_rope_tables(cos_out, sin_out, tokens, head_dim, grid_t, grid_h, grid_w,
+                                 pairs_t, pairs_h, pairs_w, theta, stream)
 
 
 def ltxk_gelu_tanh_dt(out, x, n, dtype, stream) -> int:
@@ -491,3 +500,25 @@ def rope(x, heads: int, head_dim: int, mode: int = ROPE_INTERLEAVED, grid=None, 
                    float(theta), code, _stream_handle(x, stream))
     _check(st, "ltxk_rope")
     return out
+
+
+def rope_tables(head_dim: int, grid, pairs=None, theta: float = 10000.0, tokens=None,
+                device=None, stream=None):
+    """cos and sin tables ``[tokens, head_dim/2]`` (float32, on the device)
+    for ``rms_norm_rope(..., seq_len=tokens)``, with ``rope``'s angles: row s
+    is token ``s mod (T*H*W)`` of ``grid = (T, H, W)``; ``pairs`` defaults to
+    1D ``(head_dim/2, 0, 0)`` and ``tokens`` to ``T*H*W``."""
+    import torch
+    T, H, W = grid
+    if pairs is None:
+        pairs = (head_dim // 2, 0, 0)
+    if tokens is None:
+        tokens = T * H * W
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    cos = torch.empty(tokens, head_dim // 2, dtype=torch.float32, device=device)
+    sin = torch.empty_like(cos)
+    st = ltxk_rope_tables(_dev_ptr(cos, "cos", torch.float32), _dev_ptr(sin, "sin", torch.float32),
+                          tokens, head_dim, T, H, W, pairs[0], pairs[1], pairs[2], float(theta),
+                          _stream_handle(cos, stream))
+    _check(st, "ltxk_rope_tables")
+    return cos, sin

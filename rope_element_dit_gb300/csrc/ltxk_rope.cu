@@ -127,6 +127,47 @@ __device__ __forceinline__ float2 angle_cs_turns(float c, float2 t) {
   return make_float2(__fmaf_rn(-sn, d, cs), __fmaf_rn(cs, d, sn));
 }
 
+// The coordinates (t, h, w) of token s (taken mod T*H*W).
+__device__ __forceinline__ void token_coords(const RopeArgs& a, int64_t r, int64_t coord[3]) {
+  const int64_t s = r - div_fast(r, a.thw, a.thw_mul) * a.thw;
+  const int64_t ct = div_fast(s, a.hw, a.hw_mul);
+  const int64_t rem = s - ct * a.hw;
+  const int64_t ch = div_fast(rem, a.w, a.w_mul);
+  coord[0] = ct;
+  coord[1] = ch;
+  coord[2] = rem - ch * a.w;
+}
+
+// (cos, sin) of pair k of a token with coordinates coord.
+__device__ __forceinline__ float2 pair_angle(const RopeArgs& a, const int64_t coord[3], int k) {
+  int axis, kk, n;
+  pair_axis(a, k, &axis, &kk, &n);
+  const int64_t c = coord[axis];
+  const float2 t = a.turns[k];
+  return c < (int64_t{1} << 24)
+             ? angle_cs_turns(static_cast<float>(c), t)
+             : angle_cs(c, 6.283185307179586 * (static_cast<double>(t.x) + t.y));
+}
+
+// cos and sin tables [tokens, head_dim/2] (fp32) of tokens 0 .. tokens-1,
+// token s at position s mod T*H*W: the inputs of the fused RMSNorm + RoPE,
+// with the angles of the standalone kernel.  One thread per (token, pair).
+__global__ void __launch_bounds__(256) rope_tables_kernel(float* cos_out, float* sin_out,
+                                                          int64_t tokens, const RopeArgs a) {
+  const int P = a.head_dim >> 1;
+  const int64_t n = tokens * P;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const int64_t s = i / P;
+    int64_t coord[3];
+    token_coords(a, s, coord);
+    const float2 v = pair_angle(a, coord, static_cast<int>(i - s * P));
+    cos_out[i] = v.x;
+    sin_out[i] = v.y;
+  }
+}
+
 // VEC: 16-byte slots (interleaved: head_dim % 8 == 0, split-half: % 16 == 0,
 // 16-byte aligned pointers); otherwise one thread per rotation pair.
 template <int MODE, int FMT, bool VEC, int BLOCK>
@@ -142,19 +183,10 @@ __global__ void __launch_bounds__(BLOCK, kRopeThreadsPerSm / BLOCK) rope_kernel(
 
   // the angles of row r's token into buffer b
   auto fill_table = [&](int64_t r, int b) {
-    const int64_t s = r - div_fast(r, a.thw, a.thw_mul) * a.thw;
-    const int64_t ct = div_fast(s, a.hw, a.hw_mul);
-    const int64_t rem = s - ct * a.hw;
-    const int64_t ch = div_fast(rem, a.w, a.w_mul);
-    const int64_t coord[3] = {ct, ch, rem - ch * a.w};
+    int64_t coord[3];
+    token_coords(a, r, coord);
     for (int k = tid; k < P; k += BLOCK) {
-      int axis, kk, n;
-      pair_axis(a, k, &axis, &kk, &n);
-      const int64_t c = coord[axis];
-      const float2 t = a.turns[k];
-      const float2 v = c < (int64_t{1} << 24)
-                           ? angle_cs_turns(static_cast<float>(c), t)
-                           : angle_cs(c, 6.283185307179586 * (static_cast<double>(t.x) + t.y));
+      const float2 v = pair_angle(a, coord, k);
       cosv[b][k] = v.x;
       sinv[b][k] = v.y;
     }
@@ -360,6 +392,41 @@ int units_per_thread(int mode, int fmt) {
                            : RopeUnits<ltxk::kSplitHalf, ltxk::kBf16>::value;
 }
 
+// Validates the position grid, the pair split and theta, and fills the
+// position fields of a: T*H*W, H*W, W and their division multipliers, the
+// pairs per axis, and the frequencies as turns per coordinate unit.
+int position_args(ltxk::RopeArgs* a, int head_dim, int64_t grid_t, int64_t grid_h,
+                  int64_t grid_w, int pairs_t, int pairs_h, int pairs_w, double theta) {
+  if (grid_t < 1 || grid_h < 1 || grid_w < 1 || grid_t > (int64_t{1} << 31) ||
+      grid_h > (int64_t{1} << 31) || grid_w > (int64_t{1} << 31) ||
+      grid_t * grid_h > (int64_t{1} << 62) / grid_w)
+    return LTXK_ERR_SHAPE;
+  if (pairs_t < 0 || pairs_h < 0 || pairs_w < 0 ||
+      static_cast<int64_t>(pairs_t) + pairs_h + pairs_w != head_dim / 2)
+    return LTXK_ERR_SHAPE;
+  if (!(theta > 0.0) || !(theta < 1e300)) return LTXK_ERR_SHAPE;
+  a->head_dim = head_dim;
+  a->thw = grid_t * grid_h * grid_w;
+  a->hw = grid_h * grid_w;
+  a->w = grid_w;
+  a->thw_mul = div_mul(a->thw);
+  a->hw_mul = div_mul(a->hw);
+  a->w_mul = div_mul(grid_w);
+  a->nt = pairs_t;
+  a->nh = pairs_h;
+  a->nw = pairs_w;
+  // pair k of an axis with n pairs: theta^(-k/n), in fp64
+  const int per_axis[3] = {pairs_t, pairs_h, pairs_w};
+  for (int axis = 0, k = 0; axis < 3; ++axis)
+    for (int j = 0; j < per_axis[axis]; ++j, ++k) {
+      const double tpu = pow(theta, -static_cast<double>(j) / per_axis[axis]) *
+                         0.15915494309189535;   // turns per coordinate unit
+      const float th = static_cast<float>(tpu);
+      a->turns[k] = make_float2(th, static_cast<float>(tpu - static_cast<double>(th)));
+    }
+  return LTXK_OK;
+}
+
 }  // namespace
 
 extern "C" int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int head_dim,
@@ -377,14 +444,10 @@ extern "C" int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int 
     return LTXK_ERR_SHAPE;
   const int64_t hd = static_cast<int64_t>(heads) * head_dim;
   if (hd > LTXK_MAX_HIDDEN || (rows > 0 && rows > INT64_MAX / 8 / hd)) return LTXK_ERR_SHAPE;
-  if (grid_t < 1 || grid_h < 1 || grid_w < 1 || grid_t > (int64_t{1} << 31) ||
-      grid_h > (int64_t{1} << 31) || grid_w > (int64_t{1} << 31) ||
-      grid_t * grid_h > (int64_t{1} << 62) / grid_w)
-    return LTXK_ERR_SHAPE;
-  if (pairs_t < 0 || pairs_h < 0 || pairs_w < 0 ||
-      static_cast<int64_t>(pairs_t) + pairs_h + pairs_w != head_dim / 2)
-    return LTXK_ERR_SHAPE;
-  if (!(theta > 0.0) || !(theta < 1e300)) return LTXK_ERR_SHAPE;
+  ltxk::RopeArgs a{};
+  const int st = position_args(&a, head_dim, grid_t, grid_h, grid_w, pairs_t, pairs_h, pairs_w,
+                               theta);
+  if (st != LTXK_OK) return st;
   const int esz = fmt == ltxk::kF32 ? 4 : 2;
   if (!aligned_to(out, esz) || !aligned_to(x, esz)) return LTXK_ERR_ALIGN;
   const uint64_t bytes = static_cast<uint64_t>(rows) * hd * esz;
@@ -394,20 +457,10 @@ extern "C" int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int 
   const bool vec = aligned_to(out, 16) && aligned_to(x, 16) &&
                    head_dim % (mode == LTXK_ROPE_INTERLEAVED ? 8 : 16) == 0 &&
                    hd / 8 <= static_cast<int64_t>(1) << 30;
-  ltxk::RopeArgs a{out, x, rows, heads, head_dim,
-                   grid_t * grid_h * grid_w, grid_h * grid_w, grid_w,
-                   div_mul(grid_t * grid_h * grid_w), div_mul(grid_h * grid_w), div_mul(grid_w),
-                   pairs_t, pairs_h, pairs_w, {}};
-  // pair k of an axis with n pairs: theta^(-k/n), in fp64
-  const int per_axis[3] = {pairs_t, pairs_h, pairs_w};
-  for (int axis = 0, k = 0; axis < 3; ++axis)
-    for (int j = 0; j < per_axis[axis]; ++j, ++k)
-    {
-      const double tpu = pow(theta, -static_cast<double>(j) / per_axis[axis]) *
-                         0.15915494309189535;   // turns per coordinate unit
-      const float th = static_cast<float>(tpu);
-      a.turns[k] = make_float2(th, static_cast<float>(tpu - static_cast<double>(th)));
-    }
+  a.out = out;
+  a.x = x;
+  a.rows = rows;
+  a.heads = heads;
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return fail(e);
@@ -423,6 +476,33 @@ extern "C" int ltxk_rope(void* out, const void* x, int64_t rows, int heads, int 
   void* params[] = {&a};
   e = cudaLaunchKernel(fn, dim3(grid), dim3(block), params, 0,
                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(e);
+  return LTXK_OK;
+}
+
+extern "C" int ltxk_rope_tables(float* cos_out, float* sin_out, int64_t tokens, int head_dim,
+                                int64_t grid_t, int64_t grid_h, int64_t grid_w, int pairs_t,
+                                int pairs_h, int pairs_w, double theta, ltxk_stream_t stream) {
+  if (cos_out == nullptr || sin_out == nullptr) return LTXK_ERR_NULL;
+  if (tokens < 0 || head_dim < 2 || head_dim % 2 != 0 || head_dim / 2 > ltxk::kRopeMaxPairs ||
+      (tokens > 0 && tokens > (int64_t{1} << 40) / head_dim))
+    return LTXK_ERR_SHAPE;
+  ltxk::RopeArgs a{};
+  const int st = position_args(&a, head_dim, grid_t, grid_h, grid_w, pairs_t, pairs_h, pairs_w,
+                               theta);
+  if (st != LTXK_OK) return st;
+  if (!aligned_to(cos_out, 4) || !aligned_to(sin_out, 4)) return LTXK_ERR_ALIGN;
+  const int64_t n = tokens * (head_dim / 2);
+  if (overlaps(cos_out, static_cast<uint64_t>(n) * 4, sin_out, static_cast<uint64_t>(n) * 4))
+    return LTXK_ERR_OVERLAP;
+  if (tokens == 0) return LTXK_OK;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return fail(e);
+  const int64_t blocks = (n + 255) / 256, cap = static_cast<int64_t>(sms) * 8;
+  ltxk::rope_tables_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(cos_out, sin_out, tokens, a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return fail(e);
   return LTXK_OK;
 }

@@ -419,3 +419,19 @@ def test_helpers_reject_host_tensors(L):
             call()
     with pytest.raises(TypeError):
         L.rms_norm(torch.zeros(4, 64, dtype=torch.float64))
+
+
+def test_rope_tables_validation(L):
+    f = L.ltxk_rope_tables
+    args = (4096, 128, 4096, 1, 1, 64, 0, 0, 10000.0, None)
+    assert f(None, B, *args) == L.ERR_NULL
+    assert f(A, None, *args) == L.ERR_NULL
+    assert f(A, B, -1, 128, 4096, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_SHAPE
+    assert f(A, B, 16, 127, 16, 1, 1, 63, 0, 0, 1e4, None) == L.ERR_SHAPE      # odd head_dim
+    assert f(A, B, 16, 1026, 16, 1, 1, 513, 0, 0, 1e4, None) == L.ERR_SHAPE    # > 256 pairs
+    assert f(A, B, 16, 128, 16, 1, 1, 63, 0, 0, 1e4, None) == L.ERR_SHAPE      # pairs != D/2
+    assert f(A, B, 16, 128, 0, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_SHAPE       # empty grid
+    assert f(A, B, 16, 128, 16, 1, 1, 64, 0, 0, -1.0, None) == L.ERR_SHAPE     # theta <= 0
+    assert f(A + 2, B, 16, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_ALIGN
+    assert f(A, A + 64, 16, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_OVERLAP  # 16 x 64 x 4 B
+    assert f(A, B, 0, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.OK              # no tokens

@@ -853,3 +853,24 @@ def test_rope_positions_rejects_bad_arguments(oracle_mod):
                                ((2, 1, 1), (4, 0, 0), 0.0), ((2, 1, 1), (5, -1, 0), 1e4)):
         with pytest.raises(RuntimeError):
             oracle_mod.rope(x, 2, 8, 0, grid, pairs, theta)
+
+
+def test_rope_tables_are_the_fused_forms_table_recipe(oracle_mod):
+    """The positional angles, written as tables, are the tables the fused
+    form's workloads are generated with (the generator's own fp64 code, cast
+    to fp32): the standalone and fused RoPE agree on what a position means."""
+    c, s = oracle_mod.rope_tables(6144, 64, (8, 24, 32), (10, 11, 11))
+    ct, st = synth.rope_table_3axis(8, 24, 32, 64, (10, 11, 11), 10000.0)
+    assert np.abs(c - ct).max() <= 2.0 ** -24 and np.abs(s - st).max() <= 2.0 ** -24
+    c, s = oracle_mod.rope_tables(4096, 128, (4096, 1, 1), (64, 0, 0))
+    ct, st = synth.rope_table_1d(4096, 128)
+    assert np.abs(c - ct).max() <= 2.0 ** -24 and np.abs(s - st).max() <= 2.0 ** -24
+
+
+def test_rope_tables_identity_wrap_and_norms(oracle_mod):
+    c, s = oracle_mod.rope_tables(2 * 96 + 5, 64, (2, 6, 8), (10, 11, 11))
+    assert np.all(c[0] == 1.0) and np.all(s[0] == 0.0)                 # token 0: no turn
+    assert np.array_equal(c[:96 + 5], c[96:2 * 96 + 5])                # row s is token s mod THW
+    np.testing.assert_allclose(c * c + s * s, 1.0, rtol=1e-15)
+    with pytest.raises(ValueError):
+        oracle_mod.rope_tables(4, 64, (2, 6, 8), (10, 11, 10))          # pairs must sum to D/2
