@@ -57,6 +57,8 @@ MUTANTS = [
     ("gelu_stored_as_bf16", "        store_elem(fmt, y, i, v);\n", "        store_elem(FMT_BF16, y, i, v);\n"),
     ("geglu_gate_shifted", "load_elem(fmt, x, r * 2 * h + h + j)",
      "load_elem(fmt, x, r * 2 * h + h + (j + 1) % h)"),
+    ("rope_tables_no_wrap", "rope_angles(s % (T * H * W), T, H, W, nt, nh, nw, theta, cos_out",
+     "rope_angles(s, T, H, W, nt, nh, nw, theta, cos_out"),
     ("overflow_kept_finite", "if (r > ldexp(2.0 - ldexp(1.0, 1 - prec), emax)) r = INFINITY;", ""),
     ("f16_exponent_bias", "ldexp((double)(1024 + M), E - 25)", "ldexp((double)(1024 + M), E - 24)"),
     ("f16_subnormal_scale", "v = ldexp((double)M, -24)", "v = ldexp((double)M, -25)"),
@@ -141,6 +143,8 @@ def _pin_calls():
         ("rpos_3axis", pins.test_rope_positions_three_axis_coordinates, ()),
         ("rpos_additive", pins.test_rope_positions_angle_is_additive_in_position, ()),
         ("rpos_norms", pins.test_rope_positions_norms_wrap_and_permutation, ()),
+        ("rtab_recipe", pins.test_rope_tables_are_the_fused_forms_table_recipe, ()),
+        ("rtab_wrap", pins.test_rope_tables_identity_wrap_and_norms, ()),
     ]
     return calls
 
