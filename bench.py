@@ -1,19 +1,25 @@
 """Benchmark: achieved HBM GB/s and us/call of bf16 RMSNorm / fused
 RMSNorm+RoPE on GB300, through the C ABI of libltxk.so.
 
-One step = one call per shape of the chosen workload (default: the bf16
-RMSNorm shape sweep [2x1024x2048], [4x1024x2048], [2x4096x3072],
-[4x4096x3072]).  Inputs are seeded, synthetic and resident in HBM before the
-timed region; L2 is flushed (a 2x-L2 write) between steps, outside the
-events.  Prints ONE JSON line (rank 0).
+One step = one call per shape of the chosen workload.  The default,
+``five_configs``, is the five configurations in one step: bf16 RMSNorm
+[1x1024x2048], the shape sweep [2x1024x2048] .. [4x4096x3072], fused
+RMSNorm + interleaved RoPE [2x4096, 32x128], fused RMSNorm + split-half RoPE
+[6144, 32x64], and the bandwidth stress shapes [4x16384x4096],
+[262143x2560], [65536x5120] (the largest problems, which dominate the
+step's bytes and time).  Inputs are seeded, synthetic and resident in HBM
+before the timed region; L2 is flushed (a 2x-L2 write, then a 2x-L2 read)
+before every launch, outside the events.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ltxk|reference]
 
 --impl reference times the fp64 CPU oracle on this host's cores on a bounded
 row sample of the same workload (the method's plain definition, not a GPU
-implementation).  Under torchrun (N > 1) every rank runs the workload on its
-own GPU (weak scaling, no data exchange); the time is the max over ranks.
+implementation).  Under torchrun (N > 1) the batch is N times the
+workload's rows and every rank normalises its contiguous shard of the rows
+(weak scaling: fixed rows per GPU, no data exchange); the time is the max
+over ranks.
 """
 from __future__ import annotations
 
@@ -43,6 +49,13 @@ FALLBACK_HBM_GBS = 6800.0
 CSRC = os.path.join(ROOT, "rope_element_dit_gb300", "csrc")
 
 WORKLOAD_TITLES = {
+    "five_configs": "bf16 RMSNorm bandwidth stress [4x16384x4096], [262143x2560], "
+                    "[65536x5120] (U(-4,4), eps 1e-5, seeds 7-9), timed in one step with "
+                    "RMSNorm [1x1024x2048] (seed 0), the shape sweep [2x1024x2048], "
+                    "[4x1024x2048], [2x4096x3072], [4x4096x3072] (1% x50 outliers, seeds "
+                    "1-4), fused RMSNorm + interleaved RoPE [2x4096, 32x128] (seed 5) and "
+                    "fused RMSNorm + split-half RoPE [6144, 32x64], 3-axis positions "
+                    "(seed 6); w ~ N(1,0.1)",
     "sweep": "bf16 RMSNorm shape sweep [2x1024x2048], [4x1024x2048], "
              "[2x4096x3072], [4x4096x3072]; N(0,1) with 1% x50 outliers, "
              "w ~ N(1,0.1), eps 1e-6, seeds 1-4",
@@ -85,7 +98,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="sweep", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="five_configs", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--case", type=int, default=None,
                     help="run only this shape (index) of the workload, e.g. for a profiler "
                          "capture that should hold one shape on the device")
@@ -110,12 +123,8 @@ def dist_env():
     return world, rank, local
 
 
-def shard_rows(rows, world, rank):
-    """Rows [r0, r1) of a batch that rank `rank` of `world` normalises: rows
-    are independent, so a contiguous split needs no exchange."""
-    base, extra = divmod(rows, world)
-    r0 = rank * base + min(rank, extra)
-    return r0, r0 + base + (1 if rank < extra else 0)
+# Rows [r0, r1) of a batch that rank `rank` of `world` normalises.
+shard_rows = synth.shard_rows
 
 
 def max_over_ranks(seconds, world, device=None):
@@ -185,9 +194,9 @@ def source_digest(family="rows", read=None):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload, digest):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def recorded_traffic(kernel, case, digest):
+    """DRAM bytes per launch of one case (shape) from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -196,7 +205,7 @@ def recorded_traffic(kernel, workload, digest):
         if not line or line.startswith("#"):
             continue
         parts = line.split("\t")
-        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload \
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == case \
                 and parts[2] == digest:
             return int(parts[3])
     return None
@@ -366,7 +375,7 @@ def run_reference(args, cases, inputs, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TITLES[args.workload], "row_fraction": frac},
+        "config": config_keys(args, cases) | {"row_fraction": frac},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -374,6 +383,15 @@ def run_reference(args, cases, inputs, world, rank):
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+def config_keys(args, cases):
+    """The keys that name the workload, the same in both arms."""
+    d = {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload, "case": args.case,
+         "shapes": [c.name for c in cases]}
+    if args.workload == "five_configs":
+        d["headline"] = WORKLOAD_TITLES["stress"]
+    return d
 
 
 # ------------------------------------------------------------- GPU timing --
@@ -572,29 +590,37 @@ def run_ltxk(args, cases, inputs, world, rank, local):
 
     # dominant kernel: the kernel instance with the largest share of time
     by_kernel = {}
-    for j, name in enumerate(plans):
-        k = by_kernel.setdefault(name, {"bytes": 0, "ms": 0.0, "launches": 0})
-        k["bytes"] += bytes_per_launch[j] * args.steps
-        k["ms"] += per_launch[:, j].sum()
-        k["launches"] += args.steps
-    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
     peak, peak_kind = measured_peak()
-    achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
-    digest = source_digest(kernel_family(dom_name))
-    traffic = recorded_traffic(dom_name, args.workload, digest)
-
     per_shape = []
     for j, c in enumerate(cases):
         us = per_launch[:, j] * 1e3
         med = float(np.median(us))
         mean = float(us.mean())
+        dram = recorded_traffic(plans[j], c.name, source_digest(kernel_family(plans[j])))
+        k = by_kernel.setdefault(plans[j], {"bytes": 0, "ms": 0.0, "launches": 0, "dram": 0,
+                                            "dram_known": True})
+        k["bytes"] += bytes_per_launch[j] * args.steps
+        k["ms"] += per_launch[:, j].sum()
+        k["launches"] += args.steps
+        if dram is None:
+            k["dram_known"] = False
+        else:
+            k["dram"] += dram * args.steps
         per_shape.append({
             "case": c.name, "kernel": plans[j], "bytes": bytes_per_launch[j],
             "us_mean": round(mean, 3), "gbps_mean": round(bytes_per_launch[j] / mean / 1e3, 1),
             "us_median": round(med, 3), "us_p10": round(float(np.percentile(us, 10)), 3),
             "us_p90": round(float(np.percentile(us, 90)), 3),
             "gbps_median": round(bytes_per_launch[j] / med / 1e3, 1),
-            "frac_of_peak": round(bytes_per_launch[j] / med / 1e3 / peak, 4)})
+            "frac_of_peak": round(bytes_per_launch[j] / med / 1e3 / peak, 4),
+            # DRAM bytes of one ncu capture of this shape over the live time
+            "dram_bytes": dram,
+            "dram_frac_of_peak": None if dram is None else round(dram / med / 1e3 / peak, 4)})
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+    achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
+    digest = source_digest(kernel_family(dom_name))
+    traffic = dom["dram"] // dom["launches"] if dom["dram_known"] else None
+    achieved_dram = None if traffic is None else traffic * dom["launches"] / (dom["ms"] / 1e3) / 1e9
 
     # e2e: host (pinned) x -> host y through the public API.  bf16 RMSNorm
     # goes through the host call ltxk_rms_norm_host; the other workloads call
@@ -613,13 +639,15 @@ def run_ltxk(args, cases, inputs, world, rank, local):
               for j, c in enumerate(cases)]
         h2d = sum(h.numel() * h.element_size() for h in hx + hres if h is not None)
         d2h = sum(h.numel() * h.element_size() for h in hy + hh if h is not None)
-        pipelined = all(c.kind == "norm" and c.dtype == "bf16" for c in cases)
-        if pipelined:
-            pstreams = [torch.cuda.Stream(dev) for _ in range(3)]
-            # one staging buffer per shape: calls on rotated streams never share
-            # slots, whichever branch (zero-copy or staged) a call takes
-            staging = [torch.empty(3 * (16 << 20), dtype=torch.uint8, device=dev) for _ in cases]
-            handles = [ps.cuda_stream for ps in pstreams]
+        # bf16 RMSNorm shapes go through the host call, the others through
+        # their entry point on the pinned tensors
+        host_call = [c.kind == "norm" and c.dtype == "bf16" for c in cases]
+        pstreams = [torch.cuda.Stream(dev) for _ in range(3)]
+        handles = [ps.cuda_stream for ps in pstreams]
+        # one staging buffer per host-call shape: calls on rotated streams
+        # never share slots, whichever branch (zero-copy or staged) a call takes
+        staging = [torch.empty(3 * (16 << 20), dtype=torch.uint8, device=dev) if hc else None
+                   for hc in host_call]
         e_ms = []
         for i in range(args.e2e_steps + 3):
             flush_l2(i)
@@ -627,41 +655,43 @@ def run_ltxk(args, cases, inputs, world, rank, local):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            if pipelined:
-                for ps in pstreams:
-                    ps.wait_stream(stream)
-                for j, c in enumerate(cases):
-                    wp = None if dev_bufs[j]["w"] is None else dev_bufs[j]["w"].data_ptr()
-                    # independent shapes start on different streams, so their
-                    # fixed latencies overlap
-                    rot = handles[j % len(handles):] + handles[:j % len(handles)]
-                    st = L.ltxk_rms_norm_host(hy[j].data_ptr(), hx[j].data_ptr(), wp, c.rows,
-                                              c.hidden, c.eps, staging[j].data_ptr(),
-                                              staging[j].numel(), rot, len(rot))
-                    if st != L.OK:
-                        raise L.LtxkError(st, "bench e2e")
-                for ps in pstreams:
-                    stream.wait_stream(ps)
-            else:
-                # the call itself on the pinned host tensors: the kernel reads x
-                # and writes y across the host link (zero-copy)
-                for j in range(n):
+            for ps in pstreams:
+                ps.wait_stream(stream)
+            for j, c in enumerate(cases):
+                if not host_call[j]:
+                    # the call itself on the pinned host tensors: the kernel
+                    # reads x and writes y across the host link (zero-copy)
                     launch(j, x=hx[j], y=hy[j], res=hres[j], h=hh[j])
+                    continue
+                wp = None if dev_bufs[j]["w"] is None else dev_bufs[j]["w"].data_ptr()
+                # independent shapes start on different streams, so their
+                # fixed latencies overlap
+                rot = handles[j % len(handles):] + handles[:j % len(handles)]
+                st = L.ltxk_rms_norm_host(hy[j].data_ptr(), hx[j].data_ptr(), wp, c.rows,
+                                          c.hidden, c.eps, staging[j].data_ptr(),
+                                          staging[j].numel(), rot, len(rot))
+                if st != L.OK:
+                    raise L.LtxkError(st, "bench e2e")
+            for ps in pstreams:
+                stream.wait_stream(ps)
             e1.record(stream)
             torch.cuda.synchronize()
             if i >= 3:
                 e_ms.append(e0.elapsed_time(e1))
         e2e_s = max_over_ranks(sum(e_ms) / 1e3, world, dev)
+        notes = []
+        if any(host_call):
+            notes.append("bf16 RMSNorm shapes: ltxk_rms_norm_host on pinned host x and y, one "
+                         "kernel reads x and writes y across the host link (NVLink-C2C on "
+                         "GB300, zero-copy), the shapes start on three streams in turn")
+        if not all(host_call):
+            notes.append("other shapes: the ltxk call on pinned host x and y (and, for the "
+                         "residual add, residual and h), the kernel reads and writes them "
+                         "across the host link (zero-copy)")
+        notes.append("weight, tables and conditioning vectors resident")
         e2e = {"value": round(aggregate_gbps(bytes_per_step, len(e_ms), world, e2e_s), 2),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s / len(e_ms) * 1e3, 4),
-               "note": ("ltxk_rms_norm_host on pinned host x and y: one kernel reads x and "
-                        "writes y across the host link (NVLink-C2C on GB300, zero-copy); "
-                        "the shapes start on three streams in turn; weight resident"
-                        if pipelined else
-                        "the ltxk call on pinned host x and y (and, for the residual add, "
-                        "residual and h): the kernel reads and writes them across the host "
-                        "link (zero-copy); weight, tables and conditioning vectors resident")}
+               "ms_per_step": round(e2e_s / len(e_ms) * 1e3, 4), "note": "; ".join(notes)}
 
     clocks = sampler.summary(t0, t1) if not args.no_clocks else None
 
@@ -680,8 +710,7 @@ def run_ltxk(args, cases, inputs, world, rank, local):
         "ms_per_step": round(float(step_ms.mean()), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "io_dtype": cases[0].dtype, "data": "synthetic",
-        "config": {"workload": WORKLOAD_TITLES[args.workload], "name": args.workload,
-                   "case": args.case,
+        "config": config_keys(args, cases) | {
                    "timing": "CUDA events around each launch on the launching stream; "
                              "a GPU spin before each launch keeps host launch latency "
                              "out of the events",
@@ -691,11 +720,16 @@ def run_ltxk(args, cases, inputs, world, rank, local):
                          "another buffer (cold and clean L2 at kernel start)",
                    "path": args.path,
                    "bytes_per_step": bytes_per_step, "per_shape": per_shape,
-                   "parallelism": f"{world} independent GPU(s), rows of a batch per GPU"},
+                   "parallelism": (f"rows of one batch of {world} x the workload's rows "
+                                   f"split over {world} GPUs, no exchange"
+                                   if world > 1 else "1 GPU")},
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
+                     # the same launches' DRAM bytes (ncu) over their live time
+                     "achieved_dram": None if achieved_dram is None else round(achieved_dram, 1),
+                     "frac_dram": None if achieved_dram is None else round(achieved_dram / peak, 4),
                      "algorithmic_bytes_per_launch": int(dom["bytes"] / dom["launches"]),
                      "launches": dom["launches"], "source_digest": digest},
         "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu,
@@ -713,6 +747,8 @@ def main():
         if not 0 <= args.case < len(cases):
             raise SystemExit(f"--case must be in [0, {len(cases)})")
         cases = [cases[args.case]]
+    if args.impl == "ltxk" and world > 1:
+        cases = [synth.shard_case(c, world, rank) for c in cases]
     inputs = [synth.make_inputs(c) for c in cases]
     if args.impl == "reference":
         run_reference(args, cases, inputs, world, rank)

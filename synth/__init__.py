@@ -127,13 +127,15 @@ def _chunked(n: int, fn, threads: int | None, fmt: str = "bf16") -> np.ndarray:
 
 
 def normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0,
-                std: float = 1.0, threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
+                std: float = 1.0, threads: int | None = None, fmt: str = "bf16",
+                start: int = 0) -> np.ndarray:
     """n draws of N(mean, std^2), rounded to bfloat16 (bit patterns), or to
-    float16 / float32 with ``fmt``."""
+    float16 / float32 with ``fmt``: elements start .. start+n-1 of the
+    stream (the stream is counter-based, so any slice is generated alone)."""
     key = stream_key(seed, stream)
 
     def fn(s, c):
-        z = raw(key, 2 * s, 2 * c)
+        z = raw(key, 2 * (start + s), 2 * c)
         u0 = _unit_open_right(z[0::2])
         u1 = _unit_open_left(z[1::2])
         g = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u0)
@@ -143,31 +145,33 @@ def normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0,
 
 
 def uniform_bf16(seed: int, stream: int, n: int, lo: float, hi: float,
-                 threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
+                 threads: int | None = None, fmt: str = "bf16", start: int = 0) -> np.ndarray:
     """n draws of U[lo, hi), rounded to bfloat16 (bit patterns), or to
-    float16 / float32 with ``fmt``."""
+    float16 / float32 with ``fmt``: elements start .. start+n-1 of the stream."""
     key = stream_key(seed, stream)
 
     def fn(s, c):
-        u = _unit_open_right(raw(key, s, c))
+        u = _unit_open_right(raw(key, start + s, c))
         return to_format(lo + (hi - lo) * u, fmt)
 
     return _chunked(n, fn, threads, fmt)
 
 
 def normal_with_outliers_bf16(seed: int, n: int, frac: float, scale: float,
-                              threads: int | None = None, fmt: str = "bf16") -> np.ndarray:
+                              threads: int | None = None, fmt: str = "bf16",
+                              start: int = 0) -> np.ndarray:
     """N(0,1) draws where each element, independently with probability
     ``frac`` (its own uniform from the OUTLIER stream), is multiplied by
-    ``scale`` before the rounding to bfloat16 (or ``fmt``)."""
+    ``scale`` before the rounding to bfloat16 (or ``fmt``); elements
+    start .. start+n-1."""
     kx = stream_key(seed, STREAM_X)
     ko = stream_key(seed, STREAM_OUTLIER)
 
     def fn(s, c):
-        z = raw(kx, 2 * s, 2 * c)
+        z = raw(kx, 2 * (start + s), 2 * c)
         g = (np.sqrt(-2.0 * np.log(_unit_open_left(z[1::2])))
              * np.cos(2.0 * math.pi * _unit_open_right(z[0::2])))
-        sel = _unit_open_right(raw(ko, s, c)) < frac
+        sel = _unit_open_right(raw(ko, start + s, c)) < frac
         g = np.where(sel, g * scale, g)
         return to_format(g, fmt)
 
@@ -360,7 +364,12 @@ ROPE_POS_VIDEO = [Case(
     weight=False, meta={"shape": [1, 6144, 32, 64], "grid": [8, 24, 32],
                         "pairs": [10, 11, 11], "theta": 10000.0})]
 
+# The five configurations in one step: the bandwidth stress shapes (the
+# largest problems) with the small case, the sweep and both fused forms.
+FIVE_CONFIGS = SMALL + SWEEP + ROPE_INTERLEAVED + ROPE_SPLIT + STRESS
+
 WORKLOADS = {
+    "five_configs": FIVE_CONFIGS,
     "small": SMALL,
     "sweep": SWEEP,
     "rope_interleaved": ROPE_INTERLEAVED,
@@ -386,14 +395,17 @@ STREAM_RESIDUAL = 5
 
 
 def make_x(case: Case, threads: int | None = None) -> np.ndarray:
+    """x [rows, in_width]; for a shard (``shard_case``) the rows
+    row_start .. row_start+rows-1 of the whole batch."""
     n = case.rows * case.in_width
     f = case.dtype
+    o = case.meta.get("row_start", 0) * case.in_width
     if case.x_dist == "normal":
-        x = normal_bf16(case.seed, STREAM_X, n, threads=threads, fmt=f)
+        x = normal_bf16(case.seed, STREAM_X, n, threads=threads, fmt=f, start=o)
     elif case.x_dist == "normal_outliers":
-        x = normal_with_outliers_bf16(case.seed, n, 0.01, 50.0, threads=threads, fmt=f)
+        x = normal_with_outliers_bf16(case.seed, n, 0.01, 50.0, threads=threads, fmt=f, start=o)
     elif case.x_dist == "uniform4":
-        x = uniform_bf16(case.seed, STREAM_X, n, -4.0, 4.0, threads=threads, fmt=f)
+        x = uniform_bf16(case.seed, STREAM_X, n, -4.0, 4.0, threads=threads, fmt=f, start=o)
     else:
         raise ValueError(case.x_dist)
     return x.reshape(case.rows, case.in_width)
@@ -419,14 +431,16 @@ def make_tables(case: Case):
 
 
 def make_cond(case: Case):
-    """AdaLN scale and shift, bfloat16 [n_cond, hidden]."""
+    """AdaLN scale and shift, [n_cond, hidden] in the case's format (for a
+    shard: the conditioning rows of its batch items)."""
     if case.kind != "adaln":
         return None, None
     n = case.n_cond * case.hidden
+    o = case.meta.get("row_start", 0) // case.rows_per_cond * case.hidden
     sc = normal_bf16(case.seed, STREAM_SCALE, n, 0.0, case.meta.get("scale_std", 0.5),
-                     fmt=case.dtype)
+                     fmt=case.dtype, start=o)
     sh = normal_bf16(case.seed, STREAM_SHIFT, n, 0.0, case.meta.get("shift_std", 0.5),
-                     fmt=case.dtype)
+                     fmt=case.dtype, start=o)
     return sc.reshape(case.n_cond, case.hidden), sh.reshape(case.n_cond, case.hidden)
 
 
@@ -435,10 +449,42 @@ def make_inputs(case: Case, threads: int | None = None) -> dict:
     scale, shift = make_cond(case)
     res = None
     if case.kind == "add_norm":
-        res = normal_bf16(case.seed, STREAM_RESIDUAL, case.elements,
-                          threads=threads, fmt=case.dtype).reshape(case.rows, case.hidden)
+        res = normal_bf16(case.seed, STREAM_RESIDUAL, case.elements, threads=threads,
+                          fmt=case.dtype, start=case.meta.get("row_start", 0) * case.hidden
+                          ).reshape(case.rows, case.hidden)
     return {"x": make_x(case, threads), "w": make_w(case) if case.weight else None,
             "cos": cos, "sin": sin, "scale": scale, "shift": shift, "res": res}
+
+
+def shard_rows(rows: int, world: int, rank: int):
+    """Rows [r0, r1) of a batch that rank ``rank`` of ``world`` takes: rows
+    are independent, so a contiguous split needs no exchange."""
+    base, extra = divmod(rows, world)
+    r0 = rank * base + min(rank, extra)
+    return r0, r0 + base + (1 if rank < extra else 0)
+
+
+def shard_case(case: Case, world: int, rank: int) -> Case:
+    """Rank ``rank``'s part of a batch of ``world`` x the case's rows (the
+    case as one GPU's share of a batch that grows with the GPU count).  The
+    shard's rows are rows [r0, r1) of that batch, generated from the same
+    counter-based streams; the weight and the tables are the case's own.
+    A shard starts at a whole sequence (tables), a whole position grid
+    (positions) and a whole batch item (conditioning), so its first row
+    uses the same table row, position and conditioning row as row 0."""
+    if world == 1:
+        return case
+    r0, r1 = shard_rows(world * case.rows, world, rank)
+    period = max(case.seq_len, 1)
+    if case.kind == "rope_pos":
+        g = case.meta["grid"]
+        period = g[0] * g[1] * g[2]
+    if case.kind == "adaln":
+        period = case.rows_per_cond
+    if r0 % period:
+        raise ValueError(f"{case.name}: shard start {r0} is not a multiple of {period}")
+    meta = dict(case.meta, row_start=r0, batch_rows=world * case.rows)
+    return Case(**{**case.__dict__, "rows": r1 - r0, "meta": meta})
 
 
 def algorithmic_bytes(case: Case, per_row_tables: bool = False) -> int:
