@@ -390,16 +390,39 @@ LTXK_API int ltxk_diag_missing_copy(void* out, const void* x, int64_t rows,
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Each call clears the fault word on `stream`
  * before its kernel.  A wait that runs out sets the word and leaves that
- * warp's remaining rows unwritten; no entry point reads this word back
- * (ltxk_fault_status reads the other entry points' word).  All calls share
- * the array, which keeps the last call's contents, so calls that overlap on
- * the GPU (other streams, other threads) race on it.
+ * warp's remaining rows unwritten; ltxk_noalloc_fault_status() reads the
+ * word back (and clears it), so check it after a call whose output matters.
+ * All calls share the array, which keeps the last call's contents, so calls
+ * that overlap on the GPU (other streams, other threads) race on it: on the
+ * fault word, one call's clear can erase another call's fault.
  */
 #define LTXK_NOALLOC_SCRATCH_WORDS 64
 #define LTXK_NOALLOC_MAX_HIDDEN 4096
 LTXK_API int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w,
                                    int64_t rows, int64_t hidden, float eps,
                                    ltxk_stream_t stream);
+
+/*
+ * ltxk_noalloc_fault_status -- waits for the current device to finish
+ * (cudaDeviceSynchronize), then reads the fault word of
+ * ltxk_rms_norm_noalloc's static array.  Returns LTXK_ERR_TIMEOUT if a
+ * bounded wait of the last call ran out (and clears the word), LTXK_OK if
+ * not, LTXK_ERR_CUDA if a CUDA call failed.  Allocates nothing.  Like the
+ * entry point it serves, the pages have no counterpart to it.
+ */
+LTXK_API int ltxk_noalloc_fault_status(void);
+
+/*
+ * ltxk_diag_noalloc_missing_copy -- diagnostic for the bounded waits of
+ * ltxk_rms_norm_noalloc: the same call (no weight, eps 1e-6) with the bulk
+ * copy of every warp's first row never issued, so that those waits run out
+ * after wait_limit_ns nanoseconds (1e3 .. 1e10).  No copy is left in
+ * flight.  Afterwards ltxk_noalloc_fault_status() returns LTXK_ERR_TIMEOUT.
+ * Returns an ltxk_status for the launch (the entry point's checks).
+ */
+LTXK_API int ltxk_diag_noalloc_missing_copy(void* out, const void* x, int64_t rows,
+                                            int64_t hidden, uint64_t wait_limit_ns,
+                                            ltxk_stream_t stream);
 
 /* Human-readable name of an ltxk_status (static string, never NULL). */
 LTXK_API const char* ltxk_status_string(int status);

@@ -65,7 +65,8 @@ __all__ = [
 EXPORTS = ("ltxk_rms_norm", "ltxk_rms_norm_rope", "ltxk_rms_norm_rope_seq",
            "ltxk_rms_norm_adaln", "ltxk_rms_norm_host", "ltxk_add_rms_norm",
            "ltxk_fault_status", "ltxk_set_path", "ltxk_diag_missing_copy",
-           "ltxk_rms_norm_noalloc", "ltxk_gelu_tanh", "ltxk_geglu",
+           "ltxk_rms_norm_noalloc", "ltxk_noalloc_fault_status",
+           "ltxk_diag_noalloc_missing_copy", "ltxk_gelu_tanh", "ltxk_geglu",
            "ltxk_rms_norm_dt", "ltxk_rms_norm_rope_dt", "ltxk_rms_norm_adaln_dt",
            "ltxk_add_rms_norm_dt", "ltxk_plan_launch_dt", "ltxk_rope",
            "ltxk_gelu_tanh_dt", "ltxk_geglu_dt", "ltxk_rope_tables",
@@ -113,6 +114,10 @@ def _load():
     lib.ltxk_rms_norm_host.restype = I32
     lib.ltxk_rms_norm_noalloc.argtypes = [P, P, P, I64, I64, F32, P]
     lib.ltxk_rms_norm_noalloc.restype = I32
+    lib.ltxk_noalloc_fault_status.argtypes = []
+    lib.ltxk_noalloc_fault_status.restype = I32
+    lib.ltxk_diag_noalloc_missing_copy.argtypes = [P, P, I64, I64, ctypes.c_uint64, P]
+    lib.ltxk_diag_noalloc_missing_copy.restype = I32
     lib.ltxk_rms_norm_dt.argtypes = [P, P, P, I64, I64, F32, I32, P]
     lib.ltxk_rms_norm_rope_dt.argtypes = [P, P, P, P, P, I64, I32, I32, I32, F32, I64, I32, P]
     lib.ltxk_rms_norm_adaln_dt.argtypes = [P, P, P, P, P, I64, I64, I64, F32, I32, P]
@@ -254,6 +259,14 @@ def ltxk_geglu_dt(out, x, rows, hidden, dtype, stream) -> int:
 
 def ltxk_fault_status() -> int:
     return _lib.ltxk_fault_status()
+
+
+def ltxk_noalloc_fault_status() -> int:
+    return _lib.ltxk_noalloc_fault_status()
+
+
+def ltxk_diag_noalloc_missing_copy(out, x, rows, hidden, wait_limit_ns, stream) -> int:
+    return _lib.ltxk_diag_noalloc_missing_copy(out, x, rows, hidden, wait_limit_ns, stream)
 
 
 def ltxk_set_path(path: int) -> int:

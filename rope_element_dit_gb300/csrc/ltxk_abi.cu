@@ -95,6 +95,9 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 #ifndef LTXK_PLAIN_MAX_SLOTS
 #define LTXK_PLAIN_MAX_SLOTS 16
 #endif
+#ifndef LTXK_ADALN_MAX_SLOTS
+#define LTXK_ADALN_MAX_SLOTS LTXK_PLAIN_MAX_SLOTS
+#endif
 #ifndef LTXK_ROPE_MAX_SLOTS_INTERLEAVED
 #define LTXK_ROPE_MAX_SLOTS_INTERLEAVED 4
 #endif
@@ -156,6 +159,9 @@ cudaError_t device_facts(int* dev, int* sms, unsigned int** fault) {
   return cudaSuccess;
 }
 
+}  // namespace
+
+namespace ltxk {
 // Resident CTAs per SM of `fn` with `block` threads and `smem` dynamic bytes;
 // opts the function in to that much dynamic shared memory first.
 cudaError_t resident_ctas(int dev, const void* fn, int block, int smem, int* per_sm) {
@@ -181,6 +187,10 @@ cudaError_t resident_ctas(int dev, const void* fn, int block, int smem, int* per
   *per_sm = it->second;
   return cudaSuccess;
 }
+}  // namespace ltxk
+
+namespace {
+using ltxk::resident_ctas;
 
 // ---- planning -------------------------------------------------------------
 
@@ -249,7 +259,8 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
     const int cap = max_vpl(fmt);
-    int max_slots = row_only                   ? LTXK_PLAIN_MAX_SLOTS
+    int max_slots = km == ltxk::kAdaLN         ? LTXK_ADALN_MAX_SLOTS
+                    : row_only                 ? LTXK_PLAIN_MAX_SLOTS
                     : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
                                                : LTXK_ROPE_MAX_SLOTS_SPLIT;
     if (max_slots > cap) max_slots = cap;

@@ -40,6 +40,13 @@ const void* rows_tma_split_ptr(int vec_per_lane);
 // Record a cudaError_t for ltxk_last_cuda_error() (calling thread).
 void record_cuda_error(int e);
 
+// Resident CTAs per SM of kernel `fn` with `block` threads and `smem` bytes
+// of dynamic shared memory on device `dev`, after opting the kernel in to
+// that much dynamic shared memory.  One record per (device, kernel) keeps
+// the opt-in monotonic (it is only ever raised), under one lock, for every
+// entry point that launches the kernel.
+cudaError_t resident_ctas(int dev, const void* fn, int block, int smem, int* per_sm);
+
 // The kernel-family setting of ltxk_set_path (LTXK_PATH_*).
 int current_path();
 

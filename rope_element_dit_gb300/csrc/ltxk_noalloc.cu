@@ -1,5 +1,6 @@
 // ltxk_noalloc.cu -- ltxk_rms_norm_noalloc: RMSNorm through the TMA-ring
-// kernel for callers that must not allocate device memory.
+// kernel for callers that must not allocate device memory, and the reader
+// of its fault word.
 //
 // Who needs this: code that runs where cudaMalloc is unavailable or
 // unwelcome. Examples are an engine whose device memory all comes from its
@@ -9,13 +10,12 @@
 // its bounded waits set.  Here that word lives in this file's static device
 // array, so this entry point, like the rest of the library, never allocates.
 //
-// The pages have no counterpart to this entry point.
+// The pages have no counterpart to these entry points.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <map>
 #include <mutex>
-#include <utility>
 
 #include "ltxk.h"
 #include "ltxk_kernels.cuh"
@@ -42,7 +42,6 @@ struct NoAllocDevice {
 
 std::mutex g_mu;
 std::map<int, NoAllocDevice> g_dev;
-std::map<std::pair<int, const void*>, int> g_occ;   // (device, kernel) -> CTAs per SM
 
 int fail(cudaError_t e) {
   ltxk::record_cuda_error(static_cast<int>(e));   // seen by ltxk_last_cuda_error()
@@ -76,30 +75,10 @@ cudaError_t device_setup(int dev, NoAllocDevice* out) {
   return cudaSuccess;
 }
 
-cudaError_t ctas_per_sm(int dev, const void* fn, int block, int smem, int* n) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  // Opt the kernel in to the largest ring this entry point uses, on every
-  // call: the library's other entry points share this kernel and may have
-  // set a smaller limit since.
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemTarget));
-  if (e != cudaSuccess) return e;
-  auto key = std::make_pair(dev, fn);
-  auto it = g_occ.find(key);
-  if (it == g_occ.end()) {
-    int k = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, fn, block, smem);
-    if (e != cudaSuccess) return e;
-    it = g_occ.emplace(key, k < 1 ? 1 : k).first;
-  }
-  *n = it->second;
-  return cudaSuccess;
-}
-
-}  // namespace
-
-extern "C" int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w, int64_t rows,
-                                     int64_t hidden, float eps, ltxk_stream_t stream) {
+// The call, with the diagnostic's two knobs: skip_first_copy leaves every
+// warp's first bulk copy unissued, so its wait runs out after wait_limit_ns.
+int noalloc_call(void* out, const void* x, const void* w, int64_t rows, int64_t hidden,
+                 float eps, ltxk_stream_t stream, int skip_first_copy, uint64_t wait_limit_ns) {
   if (out == nullptr || x == nullptr) return LTXK_ERR_NULL;
   if (rows < 0 || hidden <= 0) return LTXK_ERR_SHAPE;
   // Beyond the maximum this entry point handles: rows longer than one warp's
@@ -128,8 +107,11 @@ extern "C" int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w, in
   const int smem = static_cast<int>(ltxk::kTmaBarBytes + ltxk::kTmaWarps * stages * stride);
   const void* fn = ltxk::rows_tma_plain_ptr(vpl);
   if (fn == nullptr) return fail(cudaErrorInvalidDeviceFunction);
+  // The library's one record per (device, kernel) opts the kernel in to this
+  // much shared memory (only ever raising the limit) and caches the
+  // occupancy per shared-memory size.
   int per_sm = 0;
-  e = ctas_per_sm(dev, fn, ltxk::kTmaWarps * 32, smem, &per_sm);
+  e = ltxk::resident_ctas(dev, fn, ltxk::kTmaWarps * 32, smem, &per_sm);
   if (e != cudaSuccess) return fail(e);
   const int64_t needed = (rows + ltxk::kTmaWarps - 1) / ltxk::kTmaWarps;
   const int64_t cap = static_cast<int64_t>(d.sms) * per_sm;
@@ -141,10 +123,43 @@ extern "C" int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w, in
   ltxk::RowArgs a{static_cast<uint16_t*>(out), static_cast<const uint16_t*>(x),
                   static_cast<const uint16_t*>(w), nullptr, nullptr, rows, 1,
                   static_cast<int>(hidden), 0, eps};
-  ltxk::TmaArgs ta{a, stages, stride, kWaitLimitNs, 0, d.scratch};
+  ltxk::TmaArgs ta{a, stages, stride, wait_limit_ns, skip_first_copy, d.scratch};
   void* params[] = {&ta};
   e = cudaLaunchKernel(fn, dim3(grid), dim3(ltxk::kTmaWarps * 32), params,
                        static_cast<size_t>(smem), stream);
   if (e != cudaSuccess) return fail(e);
   return LTXK_OK;
+}
+
+}  // namespace
+
+extern "C" int ltxk_rms_norm_noalloc(void* out, const void* x, const void* w, int64_t rows,
+                                     int64_t hidden, float eps, ltxk_stream_t stream) {
+  return noalloc_call(out, x, w, rows, hidden, eps, stream, 0, kWaitLimitNs);
+}
+
+extern "C" int ltxk_noalloc_fault_status(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(e);
+  NoAllocDevice d;
+  e = device_setup(dev, &d);
+  if (e != cudaSuccess) return fail(e);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(e);
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, d.scratch, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(e);
+  if (word == 0) return LTXK_OK;
+  const unsigned int zero = 0;
+  e = cudaMemcpy(d.scratch, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(e);
+  return LTXK_ERR_TIMEOUT;
+}
+
+extern "C" int ltxk_diag_noalloc_missing_copy(void* out, const void* x, int64_t rows,
+                                              int64_t hidden, uint64_t wait_limit_ns,
+                                              ltxk_stream_t stream) {
+  if (wait_limit_ns < 1000ull || wait_limit_ns > 10000000000ull) return LTXK_ERR_SHAPE;
+  return noalloc_call(out, x, nullptr, rows, hidden, 1e-6f, stream, 1, wait_limit_ns);
 }
