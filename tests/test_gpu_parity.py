@@ -151,17 +151,29 @@ def gpu_adaln(x_dev, w_dev, sc_dev, sh_dev, rows, hidden, rows_per_cond, eps, ou
     return out
 
 
+# At most this fraction of a full-size AdaLN workload's elements may need the
+# bound's second clause (more than 1 ulp from the correctly rounded value):
+# only where the shift nearly cancels n*(1+scale) does the fp32 error of n
+# reach a bf16 spacing of the result.  Measured: 46 of 25.2 M.
+ADALN_STRICT_CAP = 2.0 ** -16
+
+
 def check_adaln(got_bits, x, w, scale, shift, rows_per_cond, eps, what, threads=1):
+    """Bounded comparison with the oracle; returns the total counts."""
     rows, H = x.shape
     _, ye = oracle.rms_norm_adaln(x, w, scale, shift, eps, rows_per_cond=rows_per_cond,
                                   threads=threads, exact=True)
     t = np.repeat(oracle.widen_bf16(shift), rows_per_cond, axis=0)[:rows]
     got = got_bits.reshape(rows, H)
     step = max(1, (1 << 24) // H)
+    tot = {"elements": 0, "exact": 0, "one_ulp": 0, "beyond_1ulp_within_bound": 0}
     for r0 in range(0, rows, step):
         r = compare_bf16_bounded(got[r0:r0 + step], ye[r0:r0 + step],
                                  adaln_bound(H, ye[r0:r0 + step], t[r0:r0 + step]))
         assert r["ok"], f"{what} rows {r0}+: {r}"
+        for k in tot:
+            tot[k] += r[k]
+    return tot
 
 
 @pytest.mark.parametrize("case", ALL_CASES, ids=[c.name for c in ALL_CASES])
@@ -189,8 +201,9 @@ def test_workload_full_size(case, path):
                   case.hidden, case.rows_per_cond, case.eps, out=out)
         torch.cuda.synchronize()
         check_guard(whole, n)
-        check_adaln(to_host(out), x, w, inp["scale"], inp["shift"], case.rows_per_cond,
-                    case.eps, case.name, threads=THREADS)
+        r = check_adaln(to_host(out), x, w, inp["scale"], inp["shift"], case.rows_per_cond,
+                        case.eps, case.name, threads=THREADS)
+        assert r["beyond_1ulp_within_bound"] <= ADALN_STRICT_CAP * r["elements"], r
         assert L.ltxk_fault_status() == L.OK
         return
     if case.mode is None:

@@ -105,6 +105,16 @@ CASES = [
 ]
 
 
+# At most this fraction of the elements of a full-size workload may need the
+# bound's second clause (more than 1 ulp from the correctly rounded value):
+# only an output that nearly cancels, |a s + b c| below about 2^-14 (|a|+|b|),
+# can be moved past 1 ulp by an error of a few 2^-24 (|a|+|b|), and for N(0,1)
+# pairs that is a fraction of order 1e-5 of the outputs, of which only some
+# land past the next rounding boundary.  Measured: 45 / 34 of 33.5 M (text,
+# either pairing), 6 / 3 of 12.6 M (video).
+STRICT_CAP = 2.0 ** -16
+
+
 @pytest.mark.parametrize("rows,heads,D,grid,pairs", CASES)
 @pytest.mark.parametrize("mode", [0, 1])
 def test_rope_bf16(rows, heads, D, grid, pairs, mode):
@@ -112,6 +122,8 @@ def test_rope_bf16(rows, heads, D, grid, pairs, mode):
     got = run(x, heads, D, mode, grid, pairs, 10000.0, "bf16")
     r = check(got, x, heads, D, mode, grid, pairs, 10000.0, "bf16", f"{rows}x{heads}x{D}")
     assert r["exact"] >= 0.98 * r["elements"]   # the bound is for cancelling pairs only
+    if rows * heads * D >= 1 << 23:             # the full-size text and video workloads
+        assert r["beyond_1ulp_within_bound"] <= STRICT_CAP * r["elements"], r
 
 
 @pytest.mark.parametrize("fmt", ["f16", "f32"])
