@@ -95,9 +95,6 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 #ifndef LTXK_PLAIN_MAX_SLOTS
 #define LTXK_PLAIN_MAX_SLOTS 16
 #endif
-#ifndef LTXK_ADALN_MAX_SLOTS
-#define LTXK_ADALN_MAX_SLOTS LTXK_PLAIN_MAX_SLOTS
-#endif
 #ifndef LTXK_ROPE_MAX_SLOTS_INTERLEAVED
 #define LTXK_ROPE_MAX_SLOTS_INTERLEAVED 4
 #endif
@@ -259,8 +256,7 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
     const int64_t units = km == ltxk::kSplitHalf ? nv / 2 : nv;
     const int slots_per_unit = km == ltxk::kSplitHalf ? 2 : 1;
     const int cap = max_vpl(fmt);
-    int max_slots = km == ltxk::kAdaLN         ? LTXK_ADALN_MAX_SLOTS
-                    : row_only                 ? LTXK_PLAIN_MAX_SLOTS
+    int max_slots = row_only                   ? LTXK_PLAIN_MAX_SLOTS
                     : km == ltxk::kInterleaved ? LTXK_ROPE_MAX_SLOTS_INTERLEAVED
                                                : LTXK_ROPE_MAX_SLOTS_SPLIT;
     if (max_slots > cap) max_slots = cap;
