@@ -507,8 +507,20 @@ __device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
   return rsqrtf(__fdiv_rn(ss, static_cast<float>(a.hidden)) + a.eps);
 }
 
-// Scale (and rotate) the thread's slots of one row and store them.
-template <int MODE, int VPL, int GT, int FMT>
+// x * w for pair i of a slot, exact for 16-bit formats (two significands of
+// at most 11 bits); without a weight (W false: w == NULL, a weight of ones)
+// it is x itself, so nothing is loaded, widened or multiplied.
+template <bool W, int FMT>
+__device__ __forceinline__ float2 times_w(const typename Io<FMT>::Vec& x,
+                                          const typename Io<FMT>::Vec& w, int i) {
+  if constexpr (W) return __fmul2_rn(Io<FMT>::pair(x, i), Io<FMT>::pair(w, i));
+  else return Io<FMT>::pair(x, i);
+}
+
+// Scale (and rotate) the thread's slots of one row and store them.  W says
+// whether the row has a weight (a.w != NULL); the kernels dispatch on it once
+// per launch, so a weightless norm skips the weight entirely.
+template <int MODE, int VPL, int GT, int FMT, bool W>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
                                              typename Io<FMT>::Vec (&v)[VPL],
                                              const SlotMap<MODE, VPL, GT>& m, float inv_rms) {
@@ -516,29 +528,27 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   using Vec = typename I::Vec;
 #pragma unroll
   for (int k = 0; k < VPL; ++k) I::launder_vec(v[k]);
-  const bool has_w = a.w != nullptr;
   const int64_t rb = row * a.hidden;
-  const Vec ones = I::ones();
   const float2 inv2 = make_float2(inv_rms, inv_rms);
   if constexpr (ChunkMap<MODE, FMT>::value) {
     // the same arithmetic as below, on the chunk map
     const int64_t cb = MODE == kAdaLN ? div_fast(row, a.rows_per_cond, a.cond_mul) * a.hidden : 0;
     const float2 one2 = make_float2(1.f, 1.f);
     m.each_chunk_slot([&](int k, int lo, int hi, bool ok_lo, bool ok_hi) {
-      const Vec wv = has_w ? load_chunks_ro(a.w, 0, lo, hi, ok_lo, ok_hi) : ones;
+      Vec wv{};
+      if constexpr (W) wv = load_chunks_ro(a.w, 0, lo, hi, ok_lo, ok_hi);
       float2 o[4];
       if constexpr (MODE == kAdaLN) {
         const Vec sv = load_chunks_ro(a.scale, cb, lo, hi, ok_lo, ok_hi);
         const Vec tv = load_chunks_ro(a.shift, cb, lo, hi, ok_lo, ok_hi);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 n = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+          const float2 n = __fmul2_rn(times_w<W, FMT>(v[k], wv, i), inv2);
           o[i] = __ffma2_rn(n, __fadd2_rn(one2, I::pair(sv, i)), I::pair(tv, i));
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          o[i] = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+        for (int i = 0; i < 4; ++i) o[i] = __fmul2_rn(times_w<W, FMT>(v[k], wv, i), inv2);
       }
       store_chunks(a.out, rb, lo, hi, ok_lo, ok_hi, I::pack(o[0], o[1], o[2], o[3]));
     });
@@ -546,11 +556,12 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
   } else if constexpr (MODE == kPlain || MODE == kAddNorm) {
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
-      const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
+      Vec wv{};
+      if constexpr (W) wv = I::load_ro(a.w, off);
       float2 o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)   // (x * w) exact for 16-bit formats; one rounding by inv_rms
-        o[i] = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+        o[i] = __fmul2_rn(times_w<W, FMT>(v[k], wv, i), inv2);
       I::store(a.out, rb + off, I::pack(o[0], o[1], o[2], o[3]));
     });
     return;
@@ -561,13 +572,14 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
     const float2 one2 = make_float2(1.f, 1.f);
     m.each_slot([&](int k, int off, int, bool ok) {
       if (!ok) return;
-      const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
+      Vec wv{};
+      if constexpr (W) wv = I::load_ro(a.w, off);
       const Vec sv = I::load_ro(a.scale, cb + off);
       const Vec tv = I::load_ro(a.shift, cb + off);
       float2 o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 n = __fmul2_rn(__fmul2_rn(I::pair(v[k], i), I::pair(wv, i)), inv2);
+        const float2 n = __fmul2_rn(times_w<W, FMT>(v[k], wv, i), inv2);
         o[i] = __ffma2_rn(n, __fadd2_rn(one2, I::pair(sv, i)), I::pair(tv, i));
       }
       I::store(a.out, rb + off, I::pack(o[0], o[1], o[2], o[3]));
@@ -588,7 +600,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       }
       m.each_slot([&](int k, int off, int pair0, bool ok) {
         if (!ok) return;
-        const Vec wv = has_w ? I::load_ro(a.w, off) : ones;
+        Vec wv{};
+        if constexpr (W) wv = I::load_ro(a.w, off);
         const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
         const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
         const float2 c[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
@@ -599,9 +612,12 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
           // pairs 2h and 2h+1 of the slot are rotation pairs 2h and 2h+1:
           // lane x of each float2 is the first of them, lane y the second
           const float2 x0 = I::pair(v[k], 2 * h), x1 = I::pair(v[k], 2 * h + 1);
-          const float2 w0 = I::pair(wv, 2 * h), w1 = I::pair(wv, 2 * h + 1);
-          const float2 u = __fmul2_rn(make_float2(x0.x, x1.x), make_float2(w0.x, w1.x));   // a * w
-          const float2 q = __fmul2_rn(make_float2(x0.y, x1.y), make_float2(w0.y, w1.y));   // b * w
+          float2 u = make_float2(x0.x, x1.x), q = make_float2(x0.y, x1.y);
+          if constexpr (W) {
+            const float2 w0 = I::pair(wv, 2 * h), w1 = I::pair(wv, 2 * h + 1);
+            u = __fmul2_rn(u, make_float2(w0.x, w1.x));   // a * w
+            q = __fmul2_rn(q, make_float2(w0.y, w1.y));   // b * w
+          }
           const float2 ra = __fmul2_rn(diff_of_products2(u, c[h], q, s[h]), inv2);
           const float2 rb2 = __fmul2_rn(diff_of_products2(u, s[h], neg2(q), c[h]), inv2);
           o[2 * h] = make_float2(ra.x, rb2.x);
@@ -623,8 +639,11 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       m.each_pair([&](int j, int lo_off, int hi_off, int pair0, bool ok) {
         if (!ok) return;
         const int kl = 2 * j, kh = 2 * j + 1;
-        const Vec wl = has_w ? I::load_ro(a.w, lo_off) : ones;
-        const Vec wh = has_w ? I::load_ro(a.w, hi_off) : ones;
+        Vec wl{}, wh{};
+        if constexpr (W) {
+          wl = I::load_ro(a.w, lo_off);
+          wh = I::load_ro(a.w, hi_off);
+        }
         const float4 c0 = same_cols ? c0h : ld_ro16f(ct + pair0);
         const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
         const float4 s0 = same_cols ? s0h : ld_ro16f(st + pair0);
@@ -636,8 +655,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         float2 ol[4], oh[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // rotation pairs 2i, 2i+1: (lo pair i, hi pair i)
-          const float2 u = __fmul2_rn(I::pair(v[kl], i), I::pair(wl, i));
-          const float2 q = __fmul2_rn(I::pair(v[kh], i), I::pair(wh, i));
+          const float2 u = times_w<W, FMT>(v[kl], wl, i);
+          const float2 q = times_w<W, FMT>(v[kh], wh, i);
           ol[i] = __fmul2_rn(diff_of_products2(u, c[i], q, s[i]), inv2);
           oh[i] = __fmul2_rn(diff_of_products2(u, s[i], neg2(q), c[i]), inv2);
         }
@@ -803,7 +822,8 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    row_epilogue<MODE, VPL, GT, FMT>(a, row, v, m, inv_rms_of(ss, a));
+    if (a.w != nullptr) row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a));
+    else row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a));
     if constexpr (kPipe) {
 #pragma unroll
       for (int k = 0; k < VPL; ++k) v[k] = nv[k];
@@ -958,7 +978,8 @@ rows_tma_kernel(const TmaArgs ta) {
       }
     }
     const float ss = warp_sum(slots_sumsq<kBf16>(v));
-    row_epilogue<MODE, VPL, 32, kBf16>(a, row, v, m, inv_rms_of(ss, a));
+    if (a.w != nullptr) row_epilogue<MODE, VPL, 32, kBf16, true>(a, row, v, m, inv_rms_of(ss, a));
+    else row_epilogue<MODE, VPL, 32, kBf16, false>(a, row, v, m, inv_rms_of(ss, a));
   }
 }
 
