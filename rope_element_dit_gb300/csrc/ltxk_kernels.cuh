@@ -346,13 +346,54 @@ struct Io<kF32> {
   __device__ static void put(void* p, int64_t e, float f) { static_cast<float*>(p)[e] = f; }
 };
 
+// Mixed-precision FMA (sm_100 and later): a*b + c with a and b the 16-bit
+// halves of 32-bit words (bf16 for FMT 0, fp16 for FMT 1), widened exactly,
+// c and the result fp32, one rounding.  It reads the halves where they are,
+// so no widening instruction is needed.  `LTXK_MIXED_FMA` 0 keeps the
+// widen-then-f32x2 forms; both give the same bits.  Measured on GB300 (event
+// means, 3 x 200 launches): interleaved RoPE [2 x 4096 x 32x128]
+// 26.52 -> 24.95 us, RMSNorm [2x4096x3072] 18.03 -> 17.70 us; the
+// bandwidth-bound shapes unchanged.
+#ifndef LTXK_MIXED_FMA
+#define LTXK_MIXED_FMA 1
+#endif
+
+// (lo(a)*lo(b) + c.x, hi(a)*hi(b) + c.y)
+template <int FMT>
+__device__ __forceinline__ float2 fma_halves(uint32_t a, uint32_t b, float2 c) {
+  float2 d;
+  if constexpr (FMT == kBf16) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %4;\n\tfma.rn.f32.bf16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "r"(a), "r"(b), "f"(c.x), "f"(c.y));
+  } else {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %4;\n\tfma.rn.f32.f16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "r"(a), "r"(b), "f"(c.x), "f"(c.y));
+  }
+  return d;
+}
+
+// Exact products of same halves, (lo(a)*lo(b), hi(a)*hi(b)): two 16-bit
+// significands fit fp32, and adding -0 keeps every product, signed zeros
+// included, unchanged.
+template <int FMT>
+__device__ __forceinline__ float2 mul_halves(uint32_t a, uint32_t b) {
+  return fma_halves<FMT>(a, b, make_float2(-0.f, -0.f));
+}
+
 // Sum of squares of a slot's 8 values, as two fp32 partial sums (even, odd).
 template <int FMT>
 __device__ __forceinline__ float2 sumsq8(const typename Io<FMT>::Vec& v, float2 s) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 p = Io<FMT>::pair(v, i);
-    s = __ffma2_rn(p, p, s);
+    if constexpr (FMT != kF32 && LTXK_MIXED_FMA != 0) {
+      const uint32_t u = word_of(v, i);
+      s = fma_halves<FMT>(u, u, s);
+    } else {
+      const float2 p = Io<FMT>::pair(v, i);
+      s = __ffma2_rn(p, p, s);
+    }
   }
   return s;
 }
@@ -513,8 +554,47 @@ __device__ __forceinline__ float inv_rms_of(float ss, const RowArgs& a) {
 template <bool W, int FMT>
 __device__ __forceinline__ float2 times_w(const typename Io<FMT>::Vec& x,
                                           const typename Io<FMT>::Vec& w, int i) {
-  if constexpr (W) return __fmul2_rn(Io<FMT>::pair(x, i), Io<FMT>::pair(w, i));
+  if constexpr (W && FMT != kF32 && LTXK_MIXED_FMA != 0)
+    return mul_halves<FMT>(word_of(x, i), word_of(w, i));
+  else if constexpr (W) return __fmul2_rn(Io<FMT>::pair(x, i), Io<FMT>::pair(w, i));
   else return Io<FMT>::pair(x, i);
+}
+
+// Issue a rotation row's shared cos/sin loads together with the row's x
+// loads (1), or in the epilogue after the reduction (0).  Rows that are
+// software-pipelined keep them in the epilogue.  Measured on GB300 with the
+// mixed-precision FMA forms (event means, 3 x 200 launches): interleaved
+// [2 x 4096 x 32x128] 24.95 -> 24.01 us.
+#ifndef LTXK_TABLE_EARLY
+#define LTXK_TABLE_EARLY 1
+#endif
+
+// The cos/sin vectors a thread uses for every slot of a row, when its slot
+// stride keeps it on the same rotation columns.
+struct RowTables {
+  float4 c[2], s[2];
+};
+
+template <int MODE, int VPL, int GT>
+__device__ __forceinline__ bool shares_columns(const SlotMap<MODE, VPL, GT>& m) {
+  return MODE == kInterleaved ? m.a1 == 0 : m.b1 == 0;
+}
+
+template <int MODE, int VPL, int GT>
+__device__ __forceinline__ void load_row_tables(const RowArgs& a, int64_t row,
+                                                const SlotMap<MODE, VPL, GT>& m, RowTables& tb) {
+  const int64_t pos = row - div_fast(row, a.table_rows, a.table_mul) * a.table_rows;
+  const float* ct = a.cos_t + pos * m.P;
+  const float* st = a.sin_t + pos * m.P;
+  if constexpr (MODE == kInterleaved) {
+    tb.c[0] = ld_ro16f(ct + (m.a0 >> 1));
+    tb.s[0] = ld_ro16f(st + (m.a0 >> 1));
+  } else {
+    tb.c[0] = ld_ro16f(ct + m.b0 * 8);
+    tb.c[1] = ld_ro16f(ct + m.b0 * 8 + 4);
+    tb.s[0] = ld_ro16f(st + m.b0 * 8);
+    tb.s[1] = ld_ro16f(st + m.b0 * 8 + 4);
+  }
 }
 
 // Scale (and rotate) the thread's slots of one row and store them.  W says
@@ -523,7 +603,8 @@ __device__ __forceinline__ float2 times_w(const typename Io<FMT>::Vec& x,
 template <int MODE, int VPL, int GT, int FMT, bool W>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
                                              typename Io<FMT>::Vec (&v)[VPL],
-                                             const SlotMap<MODE, VPL, GT>& m, float inv_rms) {
+                                             const SlotMap<MODE, VPL, GT>& m, float inv_rms,
+                                             const RowTables* early = nullptr) {
   using I = Io<FMT>;
   using Vec = typename I::Vec;
 #pragma unroll
@@ -594,7 +675,10 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       // of this thread uses the same four rotation columns: load them once.
       const bool same_cols = m.a1 == 0;
       float4 c4h = make_float4(0.f, 0.f, 0.f, 0.f), s4h = c4h;
-      if (same_cols) {
+      if (same_cols && early != nullptr) {
+        c4h = early->c[0];
+        s4h = early->s[0];
+      } else if (same_cols) {
         c4h = ld_ro16f(ct + (m.a0 >> 1));
         s4h = ld_ro16f(st + (m.a0 >> 1));
       }
@@ -611,12 +695,21 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         for (int h = 0; h < 2; ++h) {
           // pairs 2h and 2h+1 of the slot are rotation pairs 2h and 2h+1:
           // lane x of each float2 is the first of them, lane y the second
-          const float2 x0 = I::pair(v[k], 2 * h), x1 = I::pair(v[k], 2 * h + 1);
-          float2 u = make_float2(x0.x, x1.x), q = make_float2(x0.y, x1.y);
-          if constexpr (W) {
-            const float2 w0 = I::pair(wv, 2 * h), w1 = I::pair(wv, 2 * h + 1);
-            u = __fmul2_rn(u, make_float2(w0.x, w1.x));   // a * w
-            q = __fmul2_rn(q, make_float2(w0.y, w1.y));   // b * w
+          float2 u, q;
+          if constexpr (W && FMT != kF32 && LTXK_MIXED_FMA != 0) {
+            const float2 p0 = mul_halves<FMT>(word_of(v[k], 2 * h), word_of(wv, 2 * h));
+            const float2 p1 = mul_halves<FMT>(word_of(v[k], 2 * h + 1), word_of(wv, 2 * h + 1));
+            u = make_float2(p0.x, p1.x);   // a * w
+            q = make_float2(p0.y, p1.y);   // b * w
+          } else {
+            const float2 x0 = I::pair(v[k], 2 * h), x1 = I::pair(v[k], 2 * h + 1);
+            u = make_float2(x0.x, x1.x);
+            q = make_float2(x0.y, x1.y);
+            if constexpr (W) {
+              const float2 w0 = I::pair(wv, 2 * h), w1 = I::pair(wv, 2 * h + 1);
+              u = __fmul2_rn(u, make_float2(w0.x, w1.x));   // a * w
+              q = __fmul2_rn(q, make_float2(w0.y, w1.y));   // b * w
+            }
           }
           const float2 ra = __fmul2_rn(diff_of_products2(u, c[h], q, s[h]), inv2);
           const float2 rb2 = __fmul2_rn(diff_of_products2(u, s[h], neg2(q), c[h]), inv2);
@@ -630,7 +723,12 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       // per half-head (b1 == 0), the columns are the same for every pair.
       const bool same_cols = m.b1 == 0;
       float4 c0h = make_float4(0.f, 0.f, 0.f, 0.f), c1h = c0h, s0h = c0h, s1h = c0h;
-      if (same_cols) {
+      if (same_cols && early != nullptr) {
+        c0h = early->c[0];
+        c1h = early->c[1];
+        s0h = early->s[0];
+        s1h = early->s[1];
+      } else if (same_cols) {
         c0h = ld_ro16f(ct + m.b0 * 8);
         c1h = ld_ro16f(ct + m.b0 * 8 + 4);
         s0h = ld_ro16f(st + m.b0 * 8);
@@ -783,11 +881,17 @@ rows_vec_kernel(const RowArgs a) {
                     static_cast<uint32_t>(a.hidden) * I::kBytes);
     }
     Vec nv[kPipe ? VPL : 1];
+    constexpr bool kEarly = (MODE == kInterleaved || MODE == kSplitHalf) && !kPipe &&
+                            LTXK_TABLE_EARLY != 0;
+    RowTables tb;
     if constexpr (kPipe) {
       const int64_t next = row + row_step;
       if (next < a.rows) load_row(nv, a.x, next * a.hidden);
     } else {
       load_row(v, a.x, rb);
+      if constexpr (kEarly) {
+        if (shares_columns(m)) load_row_tables(a, row, m, tb);
+      }
     }
     if constexpr ((MODE == kInterleaved || MODE == kSplitHalf) && LTXK_TABLE_PREFETCH > 0) {
       const int64_t pos = row - div_fast(row, a.table_rows, a.table_mul) * a.table_rows;
@@ -822,8 +926,9 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    if (a.w != nullptr) row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a));
-    else row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a));
+    const RowTables* early = kEarly && shares_columns(m) ? &tb : nullptr;
+    if (a.w != nullptr) row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a), early);
+    else row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a), early);
     if constexpr (kPipe) {
 #pragma unroll
       for (int k = 0; k < VPL; ++k) v[k] = nv[k];
