@@ -28,6 +28,11 @@
 //     exact in fp32 for bf16 and fp16 rows (two significands of at most 11
 //     bits), so each output is one fp32 rounding away from (x w) * inv_rms
 //     before the final rounding; fp32 rows add one rounding of x * w.
+//   * For bf16 and fp16 rows the squares and the products x * w come from
+//     the mixed-precision FMA of sm_100 and later (fma.rn.f32.bf16 / .f16),
+//     which reads the 16-bit halves of a register in place: no widening
+//     instructions, the same bits.  The epilogue is compiled with and
+//     without a weight and chosen once per launch.
 //   * RoPE rotates (u, v) = (x_a w_a, x_b w_b) (both exact) and scales by
 //     inv_rms afterwards; u c - v s and u s + v c are evaluated with Kahan's
 //     2x2-determinant algorithm (W. Kahan; error bound in Jeannerod, Louvet &
