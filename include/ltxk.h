@@ -455,7 +455,8 @@ typedef struct {
     int block_threads;   /* threads per CTA */
     int rows_per_cta;    /* rows a CTA works on at a time */
     int stages;          /* TMA ring: row buffers per warp (else 0) */
-    int smem_bytes;      /* dynamic shared memory per CTA */
+    int smem_bytes;      /* dynamic shared memory per CTA: the TMA ring, or AdaLN's
+                            staged conditioning row (register kernel, 16-bit rows) */
 } ltxk_plan;
 
 /*

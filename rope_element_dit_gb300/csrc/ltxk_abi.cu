@@ -70,7 +70,9 @@ int bucket_vpl(int need) {
   return 16;
 }
 
-int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC_BLOCK; }
+// Threads per CTA of the register kernel of kernel mode km with g warps per
+// row (the kernels' own rule, ltxk::vec_block).
+int block_for_group(int km, int g) { return ltxk::vec_block(km, g); }
 
 // Grid shape.  1: at most the resident CTAs, striding over the rows
 // (persistent); 0: one CTA per row group, scheduled by the hardware.
@@ -100,6 +102,9 @@ int block_for_group(int g) { return 32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC
 #endif
 #ifndef LTXK_ROPE_MAX_SLOTS_SPLIT
 #define LTXK_ROPE_MAX_SLOTS_SPLIT 8
+#endif
+#ifndef LTXK_ADALN_STAGE
+#define LTXK_ADALN_STAGE 1
 #endif
 #ifndef LTXK_PERSISTENT_ROPE
 #define LTXK_PERSISTENT_ROPE 1
@@ -204,8 +209,8 @@ int check_shape(int op, int64_t rows, int64_t hidden, int head_dim, int mode) {
   return LTXK_OK;
 }
 
-int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int mode,
-              bool vector_ok, int path, ltxk_plan* p) {
+int make_plan_core(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int mode,
+                   bool vector_ok, int path, ltxk_plan* p) {
   if (fmt != ltxk::kBf16 && fmt != ltxk::kF16 && fmt != ltxk::kF32) return LTXK_ERR_DTYPE;
   const int st = check_shape(op, rows, hidden, head_dim, mode);
   if (st != LTXK_OK) return st;
@@ -230,7 +235,7 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
         p->kernel = LTXK_KERNEL_ROWS_VEC;
         p->group_warps = g;
         p->vec_per_lane = 4;
-        p->block_threads = block_for_group(g);
+        p->block_threads = block_for_group(km, g);
         p->rows_per_cta = p->block_threads / (32 * g);
         return LTXK_OK;
       }
@@ -245,7 +250,7 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
       p->kernel = LTXK_KERNEL_ROWS_VEC;
       p->group_warps = 2;
       p->vec_per_lane = 4;
-      p->block_threads = block_for_group(2);
+      p->block_threads = block_for_group(km, 2);
       p->rows_per_cta = p->block_threads / 64;
       return LTXK_OK;
     }
@@ -281,7 +286,7 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
         p->smem_bytes = static_cast<int>(ltxk::kTmaBarBytes + ltxk::kTmaWarps * stages * stride);
       } else {
         p->kernel = LTXK_KERNEL_ROWS_VEC;
-        p->block_threads = block_for_group(g);
+        p->block_threads = block_for_group(km, g);
         p->rows_per_cta = p->block_threads / (32 * g);
       }
       return LTXK_OK;
@@ -292,6 +297,25 @@ int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int m
   p->block_threads = ltxk::kElemBlock;
   p->rows_per_cta = 1;
   return LTXK_OK;
+}
+
+// Dynamic shared memory of a register-kernel launch: AdaLN's conditioning
+// row on 16-bit rows (scale and shift, 2 * e * hidden bytes), which each CTA
+// stages when it fits without an opt-in (48 KB); 0 otherwise.
+int stage_cond_bytes(int km, int fmt, int64_t hidden) {
+  if (LTXK_ADALN_STAGE == 0 || km != ltxk::kAdaLN || fmt == ltxk::kF32) return 0;
+  const int64_t b = 2 * hidden * elem_bytes(fmt);
+  return b <= 48 * 1024 ? static_cast<int>(b) : 0;
+}
+
+int make_plan(int op, int fmt, int64_t rows, int64_t hidden, int head_dim, int mode,
+              bool vector_ok, int path, ltxk_plan* p) {
+  const int st = make_plan_core(op, fmt, rows, hidden, head_dim, mode, vector_ok, path, p);
+  if (st == LTXK_OK && p->kernel == LTXK_KERNEL_ROWS_VEC) {
+    const int km = kernel_mode(op, mode);
+    p->smem_bytes = stage_cond_bytes(km, fmt, hidden);
+  }
+  return st;
 }
 
 template <int FMT>
@@ -350,7 +374,12 @@ int launch(int op, int mode, int fmt, const ltxk::RowArgs& args, bool vector_ok,
   unsigned int* fault = nullptr;
   cudaError_t e = device_facts(&dev, &sms, &fault);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = resident_ctas(dev, fn, p.block_threads, p.smem_bytes, &per_sm);
+  // the register kernel's dynamic shared memory holds AdaLN's staged
+  // conditioning row (the plan sizes it; 0 otherwise)
+  const int dyn_smem = p.smem_bytes;
+  ltxk::RowArgs a = args;
+  a.stage_cond = p.kernel == LTXK_KERNEL_ROWS_VEC && p.smem_bytes > 0 ? 1 : 0;
+  e = resident_ctas(dev, fn, p.block_threads, dyn_smem, &per_sm);
   if (e != cudaSuccess) return fail_cuda(e);
   const int64_t needed = (args.rows + p.rows_per_cta - 1) / p.rows_per_cta;
   const bool persistent =
@@ -367,9 +396,9 @@ int launch(int op, int mode, int fmt, const ltxk::RowArgs& args, bool vector_ok,
     e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params,
                          static_cast<size_t>(p.smem_bytes), stream);
   } else {
-    ltxk::RowArgs a = args;
     void* params[] = {&a};
-    e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params, 0, stream);
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(p.block_threads), params,
+                         static_cast<size_t>(dyn_smem), stream);
   }
   if (e != cudaSuccess) return fail_cuda(e);
   return LTXK_OK;
@@ -454,7 +483,7 @@ int adaln_fmt(void* out, const void* x, const void* w, const void* scale, const 
   if (rows == 0) return LTXK_OK;
   const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
                          aligned_to(scale, 16) && aligned_to(shift, 16);
-  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps,
+  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps, 0,
                   scale, shift, rows_per_cond};
   a.cond_mul = div_mul(rows_per_cond);
   return launch(LTXK_OP_RMS_NORM_ADALN, 0, fmt, a, vector_ok, stream, g_path.load());
@@ -482,7 +511,7 @@ int add_norm_fmt(void* out, void* residual_out, const void* x, const void* resid
   if (rows == 0) return LTXK_OK;
   const bool vector_ok = aligned_to(out, 16) && aligned_to(x, 16) && (!w || aligned_to(w, 16)) &&
                          aligned_to(residual, 16) && aligned_to(residual_out, 16);
-  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps,
+  ltxk::RowArgs a{out, x, w, nullptr, nullptr, rows, 1, static_cast<int>(hidden), 0, eps, 0,
                   nullptr, nullptr, 0, residual, residual_out};
   return launch(LTXK_OP_ADD_RMS_NORM, 0, fmt, a, vector_ok, stream, g_path.load());
 }

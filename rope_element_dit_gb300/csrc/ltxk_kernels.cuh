@@ -70,6 +70,9 @@ struct RowArgs {
   int hidden;
   int head_dim;
   float eps;
+  int stage_cond;           // 1: AdaLN's conditioning row (scale, then shift)
+                            //    is staged in dynamic shared memory (this
+                            //    fills the padding before the next pointer)
   const void* scale;        // AdaLN: [n_cond, hidden]
   const void* shift;        // AdaLN: [n_cond, hidden]
   int64_t rows_per_cond;    // AdaLN: row r uses conditioning row r / rows_per_cond
@@ -181,6 +184,19 @@ __device__ __forceinline__ void prefetch_line(const void* p) {
 // overlaps the wait for x instead of following it (0 = off, 1 = L1, 2 = L2).
 #ifndef LTXK_TABLE_PREFETCH
 #define LTXK_TABLE_PREFETCH 0
+#endif
+
+// AdaLN rows of 16-bit formats: each CTA stages the conditioning row of
+// its first row in shared memory (1), or every slot reads scale and shift
+// through L1/L2 (0).
+#ifndef LTXK_ADALN_STAGE
+#define LTXK_ADALN_STAGE 1
+#endif
+// Split-half rotation, 16-bit rows: each thread keeps the weight of its own
+// slots in registers for all the rows it serves (1), or loads it in every
+// row's epilogue (0).
+#ifndef LTXK_W_REGS
+#define LTXK_W_REGS 1
 #endif
 
 // Rows ahead that the register kernel asks the bulk-copy engine to bring
@@ -622,7 +638,9 @@ template <int MODE, int VPL, int GT, int FMT, bool W>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
                                              typename Io<FMT>::Vec (&v)[VPL],
                                              const SlotMap<MODE, VPL, GT>& m, float inv_rms,
-                                             const RowTables* early = nullptr) {
+                                             const RowTables* early = nullptr,
+                                             const unsigned char* cond_s = nullptr,
+                                             const typename Io<FMT>::Vec* wr = nullptr) {
   using I = Io<FMT>;
   using Vec = typename I::Vec;
 #pragma unroll
@@ -665,8 +683,13 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       if (vec >= m.nv) return;
       if constexpr (W) wv = I::load_ro(a.w, vec * 8);
       if constexpr (MODE == kAdaLN) {
-        sv = I::load_ro(a.scale, cb + vec * 8);
-        tv = I::load_ro(a.shift, cb + vec * 8);
+        if (cond_s != nullptr) {   // this row's conditioning row, staged
+          sv = *reinterpret_cast<const Vec*>(cond_s + vec * 8 * I::kBytes);
+          tv = *reinterpret_cast<const Vec*>(cond_s + (a.hidden + vec * 8) * I::kBytes);
+        } else {
+          sv = I::load_ro(a.scale, cb + vec * 8);
+          tv = I::load_ro(a.shift, cb + vec * 8);
+        }
       }
     };
     fetch(0, wn, sn, tn);
@@ -793,8 +816,13 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         const int kl = 2 * j, kh = 2 * j + 1;
         Vec wl{}, wh{};
         if constexpr (W) {
-          wl = I::load_ro(a.w, lo_off);
-          wh = I::load_ro(a.w, hi_off);
+          if (wr != nullptr) {   // the thread's weight, kept in registers
+            wl = wr[kl];
+            wh = wr[kh];
+          } else {
+            wl = I::load_ro(a.w, lo_off);
+            wh = I::load_ro(a.w, hi_off);
+          }
         }
         const float4 c0 = same_cols ? c0h : ld_ro16f(ct + pair0);
         const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
@@ -821,15 +849,32 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
 
 // ---- register kernel: G warps per row, row loaded straight into registers -
 
-// Threads per CTA of the register kernel when a row group is smaller.
+// Threads per CTA of the register kernel when a row group is smaller.  Plain
+// and AdaLN rows of one or two warps use LTXK_VEC_BLOCK_SMALL_ROWS: eight or
+// four rows per CTA, which halves the per-row share of a CTA's set-up
+// (AdaLN's staged conditioning row above all).  Measured on GB300 (event
+// means): AdaLN [2x6144x2048] 21.05 -> 20.77 us, [2x1024x2048] 9.65 -> 8.55 us,
+// the stress rows unchanged; four-warp rows keep 128 threads (with 256 they
+// were slower: [4x4096x3072] 30.5 -> 33.1 us), and so do the residual-add
+// rows (two rows of inputs in registers: at 256 threads only one CTA fits
+// on an SM).
 #ifndef LTXK_VEC_BLOCK
 #define LTXK_VEC_BLOCK 128
 #endif
+#ifndef LTXK_VEC_BLOCK_SMALL_ROWS
+#define LTXK_VEC_BLOCK_SMALL_ROWS 256
+#endif
 
-template <int G>
+__host__ __device__ constexpr int vec_block(int mode, int g) {
+  return (mode == kPlain || mode == kAdaLN) && g <= 2
+             ? LTXK_VEC_BLOCK_SMALL_ROWS
+             : (32 * g >= LTXK_VEC_BLOCK ? 32 * g : LTXK_VEC_BLOCK);
+}
+
+template <int MODE, int G>
 struct GroupShape {
   static constexpr int kThreadsPerGroup = 32 * G;
-  static constexpr int kBlock = 32 * G >= LTXK_VEC_BLOCK ? 32 * G : LTXK_VEC_BLOCK;
+  static constexpr int kBlock = vec_block(MODE, G);
   static constexpr int kGroupsPerCta = kBlock / kThreadsPerGroup;
 };
 
@@ -873,6 +918,13 @@ struct Pipelined {
           : (MODE == kSplitHalf && FMT != kF32 && G <= 8 && LTXK_PIPELINE_SPLIT != 0);
 };
 
+// Split-half rows of 16-bit formats keep the thread's weight in registers
+// within the same budget (fp32 rows would spill).
+template <int MODE, int FMT>
+struct WeightInRegs {
+  static constexpr bool value = MODE == kSplitHalf && FMT != kF32 && LTXK_W_REGS != 0;
+};
+
 template <int MODE, int G, int VPL, int FMT>
 struct RegBudget {
   static constexpr int kW = Io<FMT>::kWords;
@@ -886,7 +938,7 @@ struct RegBudget {
 };
 template <int MODE, int G, int VPL, int FMT>
 struct VecLaunch {
-  static constexpr int kBlock = GroupShape<G>::kBlock;
+  static constexpr int kBlock = GroupShape<MODE, G>::kBlock;
   static constexpr int kMin = 65536 / (kBlock * RegBudget<MODE, G, VPL, FMT>::kRegs);
   static constexpr int kMinBlocks = kMin < 1 ? 1 : kMin;
 };
@@ -897,7 +949,7 @@ __global__ void __launch_bounds__(VecLaunch<MODE, G, VPL, FMT>::kBlock,
 rows_vec_kernel(const RowArgs a) {
   using I = Io<FMT>;
   using Vec = typename I::Vec;
-  using S = GroupShape<G>;
+  using S = GroupShape<MODE, G>;
   constexpr int GT = S::kThreadsPerGroup;
   static_assert(MODE != kSplitHalf || VPL % 2 == 0, "split-half slots come in pairs");
   __shared__ float red[2][S::kGroupsPerCta][G];
@@ -926,6 +978,56 @@ rows_vec_kernel(const RowArgs a) {
     }
   };
   if (kPipe && first < a.rows) load_row(v, a.x, first * a.hidden);
+  // AdaLN, 16-bit rows: the CTA stages the conditioning row of its first row
+  // (scale, then shift) in shared memory once, after that row's x loads are
+  // out; its rows of that conditioning row read it there, the others from
+  // memory.  Every slot would otherwise wait on two L1/L2 loads.
+  constexpr bool kStageCond = MODE == kAdaLN && FMT != kF32 && LTXK_ADALN_STAGE != 0;
+  extern __shared__ __align__(16) unsigned char stage_smem[];
+  const unsigned char* cond_base = nullptr;
+  int64_t staged_cond = -1;
+  bool preloaded = false;
+  if constexpr (kStageCond) {
+    if (a.stage_cond != 0) {   // the same for the whole CTA
+      if (!kPipe && first < a.rows) {
+        load_row(v, a.x, first * a.hidden);
+        preloaded = true;
+      }
+      const int64_t r0 = static_cast<int64_t>(blockIdx.x) * S::kGroupsPerCta;
+      if (r0 < a.rows) {
+        const int nvec = a.hidden * I::kBytes / 16;   // 16-byte vectors per row
+        staged_cond = div_fast(r0, a.rows_per_cond, a.cond_mul);
+        const unsigned char* scp =
+            static_cast<const unsigned char*>(a.scale) + staged_cond * nvec * 16;
+        const unsigned char* shp =
+            static_cast<const unsigned char*>(a.shift) + staged_cond * nvec * 16;
+        uint4* d = reinterpret_cast<uint4*>(stage_smem);
+        for (int i = tid; i < nvec; i += static_cast<int>(blockDim.x)) {
+          d[i] = ld_ro16(scp + i * 16);
+          d[nvec + i] = ld_ro16(shp + i * 16);
+        }
+        cond_base = stage_smem;
+      }
+      __syncthreads();
+    }
+  }
+  // Split-half rotation: the thread's weight vectors, loaded once (after the
+  // first row's x loads) for all the rows the persistent CTA serves.
+  constexpr bool kWRegs = WeightInRegs<MODE, FMT>::value;
+  Vec wreg[kWRegs ? VPL : 1];
+  if constexpr (kWRegs) {
+    if (a.w != nullptr) {
+      if (!kPipe && first < a.rows) {
+        load_row(v, a.x, first * a.hidden);
+        preloaded = true;
+      }
+      m.each_pair([&](int j, int lo_off, int hi_off, int, bool ok) {
+        if (!ok) return;
+        wreg[2 * j] = I::load_ro(a.w, lo_off);
+        wreg[2 * j + 1] = I::load_ro(a.w, hi_off);
+      });
+    }
+  }
   for (int64_t row = first; row < a.rows; row += row_step) {
     const int64_t rb = row * a.hidden;
     if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
@@ -942,7 +1044,12 @@ rows_vec_kernel(const RowArgs a) {
       const int64_t next = row + row_step;
       if (next < a.rows) load_row(nv, a.x, next * a.hidden);
     } else {
-      load_row(v, a.x, rb);
+      if constexpr (kStageCond || kWRegs) {
+        if (preloaded) preloaded = false;   // the first row went out before the set-up
+        else load_row(v, a.x, rb);
+      } else {
+        load_row(v, a.x, rb);
+      }
       if constexpr (kEarly) {
         if (shares_columns(m)) load_row_tables(a, row, m, tb);
       }
@@ -981,8 +1088,16 @@ rows_vec_kernel(const RowArgs a) {
       parity ^= 1;
     }
     const RowTables* early = kEarly && shares_columns(m) ? &tb : nullptr;
-    if (a.w != nullptr) row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a), early);
-    else row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a), early);
+    const unsigned char* cond_s = nullptr;
+    if constexpr (kStageCond) {
+      if (cond_base != nullptr && div_fast(row, a.rows_per_cond, a.cond_mul) == staged_cond)
+        cond_s = cond_base;
+    }
+    if (a.w != nullptr)
+      row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a), early, cond_s,
+                                             kWRegs ? wreg : nullptr);
+    else
+      row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a), early, cond_s);
     if constexpr (kPipe) {
 #pragma unroll
       for (int k = 0; k < VPL; ++k) v[k] = nv[k];

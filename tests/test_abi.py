@@ -126,6 +126,8 @@ def test_rope_validation(L):
     (0, 7, 264, 0, 0, True, 1, 1, 4),
     (0, 7, 4, 0, 0, True, 2, 8, 0),          # hidden % 8 != 0
     (0, 7, 3072, 0, 0, False, 2, 8, 0),      # unaligned pointers
+    (3, 4096, 2048, 0, 0, True, 1, 1, 8),    # residual add: 128-thread CTAs
+    (2, 4096, 2048, 0, 0, True, 1, 1, 8),    # AdaLN: 256-thread CTAs
     # fused
     (1, 8192, 4096, 128, 0, True, 1, 4, 4),  # fused rows split over 4 warps
     (1, 6144, 2048, 64, 1, True, 1, 1, 8),
@@ -144,9 +146,14 @@ def test_plan(L, op, rows, hidden, D, mode, vec, kernel, G, vpl):
         nv = hidden // 8
         assert 32 * G * vpl >= nv
     if kernel == L.KERNEL_ROWS_VEC:
-        assert p.block_threads == max(128, 32 * G)
+        # plain and AdaLN rows of one or two warps run eight or four rows per
+        # 256-thread CTA, the others 128 threads (or one row group)
+        row_only = op in (L.OP_RMS_NORM, L.OP_RMS_NORM_ADALN)
+        assert p.block_threads == (256 if row_only and G <= 2 else max(128, 32 * G))
         assert p.rows_per_cta == p.block_threads // (32 * G)
-        assert p.stages == 0 and p.smem_bytes == 0
+        # AdaLN's 16-bit rows stage the CTA's conditioning row (scale, shift)
+        assert p.stages == 0
+        assert p.smem_bytes == (4 * hidden if op == L.OP_RMS_NORM_ADALN else 0)
     if kernel == L.KERNEL_ROWS_TMA:
         stride = (hidden * 2 + 127) // 128 * 128
         assert p.block_threads == 256 and p.rows_per_cta == 8
@@ -235,8 +242,15 @@ def test_adaln_validation(L):
 def test_adaln_plan(L):
     st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 2048, 0, 0, True)
     assert st == L.OK and (p.kernel, p.group_warps, p.vec_per_lane) == (1, 1, 8)
+    # 16-bit rows stage the CTA's conditioning row (scale, shift) in shared
+    # memory, up to hidden 12288 (48 KB, no opt-in); fp32 rows do not
+    assert p.smem_bytes == 4 * 2048
     st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 3072, 0, 0, True)
-    assert (p.kernel, p.group_warps, p.vec_per_lane) == (1, 4, 4)
+    assert (p.kernel, p.group_warps, p.vec_per_lane) == (1, 4, 4) and p.smem_bytes == 4 * 3072
+    st, p = L.ltxk_plan_launch_dt(L.OP_RMS_NORM_ADALN, L.DTYPE_F32, 12288, 2048, 0, 0, True)
+    assert p.kernel == L.KERNEL_ROWS_VEC and p.smem_bytes == 0
+    st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 8, 16384, 0, 0, True)
+    assert p.kernel == L.KERNEL_ROWS_VEC and p.smem_bytes == 0
     st, p = L.ltxk_plan_launch(L.OP_RMS_NORM_ADALN, 12288, 3072, 0, 0, False)
     assert p.kernel == L.KERNEL_ROWS_ELEM
     try:   # the TMA ring has no AdaLN form: the register kernel stays
