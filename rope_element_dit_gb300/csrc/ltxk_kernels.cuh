@@ -631,6 +631,23 @@ __device__ __forceinline__ void load_row_tables(const RowArgs& a, int64_t row,
   }
 }
 
+// Split-half rows of 16-bit formats with at most 8 slots per lane keep the
+// thread's weight in registers within the same budget (fp32 rows and wider
+// slot sets would spill).
+// The interleaved rows keep loading theirs: in registers (16 more per
+// thread, 6 instead of 8 CTAs per SM) [2x4096, 32x128] measured 24.1 ->
+// 24.8 us on GB300 (event means).
+#ifndef LTXK_W_REGS_INTERLEAVED
+#define LTXK_W_REGS_INTERLEAVED 0
+#endif
+template <int MODE, int VPL, int FMT>
+struct WeightInRegs {
+  static constexpr bool value =
+      FMT != kF32 && VPL <= 8 &&
+      ((MODE == kSplitHalf && LTXK_W_REGS != 0) ||
+       (MODE == kInterleaved && LTXK_W_REGS_INTERLEAVED != 0));
+};
+
 // Scale (and rotate) the thread's slots of one row and store them.  W says
 // whether the row has a weight (a.w != NULL); the kernels dispatch on it once
 // per launch, so a weightless norm skips the weight entirely.
@@ -762,7 +779,8 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       m.each_slot([&](int k, int off, int pair0, bool ok) {
         if (!ok) return;
         Vec wv{};
-        if constexpr (W) wv = I::load_ro(a.w, off);
+        if constexpr (W && WeightInRegs<MODE, VPL, FMT>::value) wv = wr[k];
+        else if constexpr (W) wv = I::load_ro(a.w, off);
         const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
         const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
         const float2 c[2] = {make_float2(c4.x, c4.y), make_float2(c4.z, c4.w)};
@@ -815,14 +833,12 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         if (!ok) return;
         const int kl = 2 * j, kh = 2 * j + 1;
         Vec wl{}, wh{};
-        if constexpr (W) {
-          if (wr != nullptr) {   // the thread's weight, kept in registers
-            wl = wr[kl];
-            wh = wr[kh];
-          } else {
-            wl = I::load_ro(a.w, lo_off);
-            wh = I::load_ro(a.w, hi_off);
-          }
+        if constexpr (W && WeightInRegs<MODE, VPL, FMT>::value) {   // kept in registers
+          wl = wr[kl];
+          wh = wr[kh];
+        } else if constexpr (W) {
+          wl = I::load_ro(a.w, lo_off);
+          wh = I::load_ro(a.w, hi_off);
         }
         const float4 c0 = same_cols ? c0h : ld_ro16f(ct + pair0);
         const float4 c1 = same_cols ? c1h : ld_ro16f(ct + pair0 + 4);
@@ -918,12 +934,6 @@ struct Pipelined {
           : (MODE == kSplitHalf && FMT != kF32 && G <= 8 && LTXK_PIPELINE_SPLIT != 0);
 };
 
-// Split-half rows of 16-bit formats keep the thread's weight in registers
-// within the same budget (fp32 rows would spill).
-template <int MODE, int FMT>
-struct WeightInRegs {
-  static constexpr bool value = MODE == kSplitHalf && FMT != kF32 && LTXK_W_REGS != 0;
-};
 
 template <int MODE, int G, int VPL, int FMT>
 struct RegBudget {
@@ -1013,7 +1023,7 @@ rows_vec_kernel(const RowArgs a) {
   }
   // Split-half rotation: the thread's weight vectors, loaded once (after the
   // first row's x loads) for all the rows the persistent CTA serves.
-  constexpr bool kWRegs = WeightInRegs<MODE, FMT>::value;
+  constexpr bool kWRegs = WeightInRegs<MODE, VPL, FMT>::value;
   Vec wreg[kWRegs ? VPL : 1];
   if constexpr (kWRegs) {
     if (a.w != nullptr) {
@@ -1021,11 +1031,17 @@ rows_vec_kernel(const RowArgs a) {
         load_row(v, a.x, first * a.hidden);
         preloaded = true;
       }
-      m.each_pair([&](int j, int lo_off, int hi_off, int, bool ok) {
-        if (!ok) return;
-        wreg[2 * j] = I::load_ro(a.w, lo_off);
-        wreg[2 * j + 1] = I::load_ro(a.w, hi_off);
-      });
+      if constexpr (MODE == kInterleaved) {
+        m.each_slot([&](int k, int off, int, bool ok) {
+          if (ok) wreg[k] = I::load_ro(a.w, off);
+        });
+      } else {
+        m.each_pair([&](int j, int lo_off, int hi_off, int, bool ok) {
+          if (!ok) return;
+          wreg[2 * j] = I::load_ro(a.w, lo_off);
+          wreg[2 * j + 1] = I::load_ro(a.w, hi_off);
+        });
+      }
     }
   }
   for (int64_t row = first; row < a.rows; row += row_step) {
