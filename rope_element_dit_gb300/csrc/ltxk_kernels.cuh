@@ -631,27 +631,29 @@ __device__ __forceinline__ void load_row_tables(const RowArgs& a, int64_t row,
   }
 }
 
-// Split-half rows of 16-bit formats with at most 8 slots per lane keep the
-// thread's weight in registers within the same budget (fp32 rows and wider
-// slot sets would spill).
+// Split-half rows of 16-bit formats, of at most 8 warps and 8 slots per
+// lane, keep the thread's weight in registers within the same budget (fp32
+// rows, wider slot sets and the 512- and 1024-thread row groups would spill).
 // The interleaved rows keep loading theirs: in registers (16 more per
 // thread, 6 instead of 8 CTAs per SM) [2x4096, 32x128] measured 24.1 ->
 // 24.8 us on GB300 (event means).
 #ifndef LTXK_W_REGS_INTERLEAVED
 #define LTXK_W_REGS_INTERLEAVED 0
 #endif
-template <int MODE, int VPL, int FMT>
+template <int MODE, int G, int VPL, int FMT>
 struct WeightInRegs {
   static constexpr bool value =
-      FMT != kF32 && VPL <= 8 &&
+      FMT != kF32 && G <= 8 && VPL <= 8 &&
       ((MODE == kSplitHalf && LTXK_W_REGS != 0) ||
        (MODE == kInterleaved && LTXK_W_REGS_INTERLEAVED != 0));
 };
 
 // Scale (and rotate) the thread's slots of one row and store them.  W says
 // whether the row has a weight (a.w != NULL); the kernels dispatch on it once
-// per launch, so a weightless norm skips the weight entirely.
-template <int MODE, int VPL, int GT, int FMT, bool W>
+// per launch, so a weightless norm skips the weight entirely.  WR: the
+// rotation forms take the thread's weight vectors from wr[] (registers the
+// caller loaded once) instead of loading them.
+template <int MODE, int VPL, int GT, int FMT, bool W, bool WR = false>
 __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
                                              typename Io<FMT>::Vec (&v)[VPL],
                                              const SlotMap<MODE, VPL, GT>& m, float inv_rms,
@@ -779,7 +781,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
       m.each_slot([&](int k, int off, int pair0, bool ok) {
         if (!ok) return;
         Vec wv{};
-        if constexpr (W && WeightInRegs<MODE, VPL, FMT>::value) wv = wr[k];
+        if constexpr (W && WR) wv = wr[k];
         else if constexpr (W) wv = I::load_ro(a.w, off);
         const float4 c4 = same_cols ? c4h : ld_ro16f(ct + pair0);
         const float4 s4 = same_cols ? s4h : ld_ro16f(st + pair0);
@@ -833,7 +835,7 @@ __device__ __forceinline__ void row_epilogue(const RowArgs& a, int64_t row,
         if (!ok) return;
         const int kl = 2 * j, kh = 2 * j + 1;
         Vec wl{}, wh{};
-        if constexpr (W && WeightInRegs<MODE, VPL, FMT>::value) {   // kept in registers
+        if constexpr (W && WR) {   // kept in registers by the caller
           wl = wr[kl];
           wh = wr[kh];
         } else if constexpr (W) {
@@ -1023,7 +1025,7 @@ rows_vec_kernel(const RowArgs a) {
   }
   // Split-half rotation: the thread's weight vectors, loaded once (after the
   // first row's x loads) for all the rows the persistent CTA serves.
-  constexpr bool kWRegs = WeightInRegs<MODE, VPL, FMT>::value;
+  constexpr bool kWRegs = WeightInRegs<MODE, G, VPL, FMT>::value;
   Vec wreg[kWRegs ? VPL : 1];
   if constexpr (kWRegs) {
     if (a.w != nullptr) {
@@ -1110,8 +1112,8 @@ rows_vec_kernel(const RowArgs a) {
         cond_s = cond_base;
     }
     if (a.w != nullptr)
-      row_epilogue<MODE, VPL, GT, FMT, true>(a, row, v, m, inv_rms_of(ss, a), early, cond_s,
-                                             kWRegs ? wreg : nullptr);
+      row_epilogue<MODE, VPL, GT, FMT, true, kWRegs>(a, row, v, m, inv_rms_of(ss, a), early,
+                                                     cond_s, wreg);
     else
       row_epilogue<MODE, VPL, GT, FMT, false>(a, row, v, m, inv_rms_of(ss, a), early, cond_s);
     if constexpr (kPipe) {
