@@ -200,7 +200,10 @@ __device__ __forceinline__ void prefetch_line(const void* p) {
 #endif
 
 // Rows ahead that the register kernel asks the bulk-copy engine to bring
-// into L2 (0 = off).
+// into L2 (0 = off).  Measured on GB300 with the persistent RoPE grids
+// (event means): one row ahead, interleaved [2x4096, 32x128] 23.8 -> 25.0 us
+// and split-half [6144, 32x64] 14.8 -> 14.9 us; two rows ahead 25.8 and
+// 16.0 us.
 #ifndef LTXK_L2_PREFETCH_ROWS
 #define LTXK_L2_PREFETCH_ROWS 0
 #endif
