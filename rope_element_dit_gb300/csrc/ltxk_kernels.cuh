@@ -198,6 +198,17 @@ __device__ __forceinline__ void prefetch_line(const void* p) {
 #ifndef LTXK_W_REGS
 #define LTXK_W_REGS 1
 #endif
+// Software-pipelined rotation rows: the next row's shared cos/sin vectors
+// are loaded together with its x (1), instead of in its epilogue after the
+// reduction (0), where each row's cold table row was a DRAM round trip the
+// warp waited on.  They cost 16 registers per thread (LTXK_TABLE_NEXT_REGS):
+// split-half [6144, 32x64] runs at 198 registers, 2 instead of 3 CTAs of 128
+// threads per SM, and still gains: 14.58 -> 14.26 us and 14.77 -> 14.26 us
+// (GB300, event means, 3 x 300 launches, two boxes).  Held within the old
+// budget instead (3 CTAs per SM, 44 bytes spilled) it gave 14.50 us.
+#ifndef LTXK_TABLE_NEXT
+#define LTXK_TABLE_NEXT 1
+#endif
 
 // Rows ahead that the register kernel asks the bulk-copy engine to bring
 // into L2 (0 = off).  Measured on GB300 with the persistent RoPE grids
@@ -931,6 +942,9 @@ struct GroupShape {
 #ifndef LTXK_PIPELINE_SPLIT
 #define LTXK_PIPELINE_SPLIT 1
 #endif
+#ifndef LTXK_TABLE_NEXT_REGS
+#define LTXK_TABLE_NEXT_REGS (LTXK_TABLE_NEXT != 0 ? 16 : 0)
+#endif
 template <int MODE, int G, int FMT>
 struct Pipelined {
   static constexpr bool value =
@@ -945,6 +959,9 @@ struct RegBudget {
   static constexpr int kW = Io<FMT>::kWords;
   static constexpr int kRegs =
       kW * VPL * (Pipelined<MODE, G, FMT>::value ? 2 : 1) +
+      (Pipelined<MODE, G, FMT>::value && (MODE == kInterleaved || MODE == kSplitHalf)
+           ? LTXK_TABLE_NEXT_REGS   // the next row's cos/sin vectors
+           : 0) +
                  (MODE == kPlain          ? LTXK_REG_EXTRA_PLAIN
                   : MODE == kInterleaved  ? LTXK_REG_EXTRA_INTERLEAVED
                   : MODE == kSplitHalf    ? LTXK_REG_EXTRA_SPLIT
@@ -1049,6 +1066,15 @@ rows_vec_kernel(const RowArgs a) {
       }
     }
   }
+  // Pipelined rotation rows: the next row's shared cos/sin vectors go out
+  // with its x loads (LTXK_TABLE_NEXT), held in registers until its epilogue;
+  // tbc holds the current row's.
+  constexpr bool kTableNext = kPipe && (MODE == kInterleaved || MODE == kSplitHalf) &&
+                              LTXK_TABLE_NEXT != 0;
+  RowTables tbc, tbn;
+  if constexpr (kTableNext) {
+    if (first < a.rows && shares_columns(m)) load_row_tables(a, first, m, tbc);
+  }
   for (int64_t row = first; row < a.rows; row += row_step) {
     const int64_t rb = row * a.hidden;
     if (LTXK_L2_PREFETCH_ROWS > 0 && t == 0 && (a.hidden & 7) == 0) {
@@ -1063,7 +1089,12 @@ rows_vec_kernel(const RowArgs a) {
     RowTables tb;
     if constexpr (kPipe) {
       const int64_t next = row + row_step;
-      if (next < a.rows) load_row(nv, a.x, next * a.hidden);
+      if (next < a.rows) {
+        load_row(nv, a.x, next * a.hidden);
+        if constexpr (kTableNext) {
+          if (shares_columns(m)) load_row_tables(a, next, m, tbn);
+        }
+      }
     } else {
       if constexpr (kStageCond || kWRegs) {
         if (preloaded) preloaded = false;   // the first row went out before the set-up
@@ -1109,6 +1140,7 @@ rows_vec_kernel(const RowArgs a) {
       parity ^= 1;
     }
     const RowTables* early = kEarly && shares_columns(m) ? &tb : nullptr;
+    if constexpr (kTableNext) early = shares_columns(m) ? &tbc : nullptr;
     const unsigned char* cond_s = nullptr;
     if constexpr (kStageCond) {
       if (cond_base != nullptr && div_fast(row, a.rows_per_cond, a.cond_mul) == staged_cond)
@@ -1122,6 +1154,7 @@ rows_vec_kernel(const RowArgs a) {
     if constexpr (kPipe) {
 #pragma unroll
       for (int k = 0; k < VPL; ++k) v[k] = nv[k];
+      if constexpr (kTableNext) tbc = tbn;
     }
   }
 }
