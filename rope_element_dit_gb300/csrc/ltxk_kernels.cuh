@@ -203,9 +203,11 @@ __device__ __forceinline__ void prefetch_line(const void* p) {
 // reduction (0), where each row's cold table row was a DRAM round trip the
 // warp waited on.  They cost 16 registers per thread (LTXK_TABLE_NEXT_REGS):
 // split-half [6144, 32x64] runs at 198 registers, 2 instead of 3 CTAs of 128
-// threads per SM, and still gains: 14.58 -> 14.26 us and 14.77 -> 14.26 us
-// (GB300, event means, 3 x 300 launches, two boxes).  Held within the old
-// budget instead (3 CTAs per SM, 44 bytes spilled) it gave 14.50 us.
+// threads per SM, and still gains on most boxes: 14.58 -> 14.26 us,
+// 14.77 -> 14.26 us, 14.37 -> 14.38 us (GB300, event means, 3-4 x 300
+// launches, three boxes).  Held within the old budget instead (3 CTAs per
+// SM, 44 bytes spilled) it gave 14.50 us; two warps per row with it, 14.19
+// and 14.32 us against 14.62 and 14.38 us (not adopted: within the spread).
 #ifndef LTXK_TABLE_NEXT
 #define LTXK_TABLE_NEXT 1
 #endif
@@ -1139,8 +1141,9 @@ rows_vec_kernel(const RowArgs a) {
       for (int i = 0; i < G; ++i) ss += red[parity][group][i];
       parity ^= 1;
     }
-    const RowTables* early = kEarly && shares_columns(m) ? &tb : nullptr;
-    if constexpr (kTableNext) early = shares_columns(m) ? &tbc : nullptr;
+    const RowTables* early = kEarly && shares_columns(m)        ? &tb
+                             : kTableNext && shares_columns(m) ? &tbc
+                                                               : nullptr;
     const unsigned char* cond_s = nullptr;
     if constexpr (kStageCond) {
       if (cond_base != nullptr && div_fast(row, a.rows_per_cond, a.cond_mul) == staged_cond)
