@@ -43,8 +43,11 @@
 //   * CTAs stride over rows, so any grid covers any row count: the host
 //     launches one CTA per row group for the row-only forms and persistent
 //     grids for the fused ones; split-half rows of the 16-bit formats are
-//     software-pipelined (a warp loads its next row before this row's
-//     epilogue).
+//     software-pipelined (a warp loads its next row, and that row's cos/sin
+//     vectors, before this row's epilogue) and keep the thread's weight
+//     vectors in registers for all their rows.
+//   * Read-only rows a CTA uses for many of its rows are staged once: AdaLN's
+//     conditioning row (scale, shift) goes to shared memory.
 #pragma once
 
 #include <cuda_bf16.h>
