@@ -449,3 +449,42 @@ def test_rope_tables_validation(L):
     assert f(A + 2, B, 16, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_ALIGN
     assert f(A, A + 64, 16, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.ERR_OVERLAP  # 16 x 64 x 4 B
     assert f(A, B, 0, 128, 16, 1, 1, 64, 0, 0, 1e4, None) == L.OK              # no tokens
+
+
+# The launch each bench workload shape gets: (kernel, warps per row, slots per
+# lane, threads per CTA, rows per CTA, dynamic shared memory).  The committed
+# ncu figures (launch lists, captures, DRAM traffic per kernel instance) were
+# taken on these launches; a planner change that moves a shape to another
+# instance or CTA shape has to be measured again.
+BENCH_PLANS = [
+    ("rms_norm_1x1024x2048", (1, 2, 4, 256, 4, 0)),
+    ("rms_norm_2x1024x2048", (1, 2, 4, 256, 4, 0)),
+    ("rms_norm_4x1024x2048", (1, 1, 8, 256, 8, 0)),
+    ("rms_norm_2x4096x3072", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_4x4096x3072", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_rope_interleaved_2x4096x32x128", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_split_rope_1x6144x32x64", (1, 1, 8, 128, 4, 0)),
+    ("rms_norm_4x16384x4096", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_262143x2560", (1, 1, 12, 256, 8, 0)),
+    ("rms_norm_65536x5120", (1, 2, 12, 256, 4, 0)),
+    ("rms_norm_adaln_2x6144x2048", (1, 1, 8, 256, 8, 8192)),
+    ("add_rms_norm_4x4096x3072", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_f16_4x4096x3072", (1, 4, 4, 128, 1, 0)),
+    ("rms_norm_f32_4x4096x3072", (1, 4, 4, 128, 1, 0)),
+]
+
+
+@pytest.mark.parametrize("name,plan", BENCH_PLANS)
+def test_bench_workload_plans(L, name, plan):
+    import sys
+    sys.path.insert(0, ROOT)
+    import synth
+    case = {c.name: c for w in synth.WORKLOADS.values() for c in w}[name]
+    op = {"norm": L.OP_RMS_NORM, "rope": L.OP_RMS_NORM_ROPE, "adaln": L.OP_RMS_NORM_ADALN,
+          "add_norm": L.OP_ADD_RMS_NORM}[case.kind]
+    dt = {"bf16": L.DTYPE_BF16, "f16": L.DTYPE_F16, "f32": L.DTYPE_F32}[case.dtype]
+    st, p = L.ltxk_plan_launch_dt(op, dt, case.rows, case.hidden, case.head_dim or 0,
+                                  case.mode or 0, True)
+    assert st == L.OK
+    assert (p.kernel, p.group_warps, p.vec_per_lane, p.block_threads, p.rows_per_cta,
+            p.smem_bytes) == plan
